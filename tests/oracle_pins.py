@@ -1,0 +1,248 @@
+"""Pins for the oracle: checks against what the pages and mathematics fix.
+
+Each ``check_*`` takes a loaded oracle library and returns a list of failure
+strings (empty = pass), so that the same checks serve the normal test run and the
+planted-mistake run (tests/test_oracle_mutants.py), which must see every planted
+mistake caught by at least one of them.
+
+What pins what:
+  * GeLU      -- the tanh form stays within its published error of the exact
+                 x*Phi(x) (max |diff| ~4.73e-4, Hendrycks & Gimpel 2016); the
+                 algebraic identity gelu(x) - gelu(-x) = x; gelu(0) = 0;
+                 gelu'(0) = 1/2; the asymptotes; gelu' against central
+                 differences of gelu.
+  * forward   -- t = 1 reduces to the textbook MLP, built here from numpy
+                 matmuls; for t = 2, 4, 8 the sum of the shard partials plus b
+                 equals the unsharded result and each partial is the column /
+                 row block product of the "Megatron-LM" report, section 4.1
+                 (Z = Y_1 B_1 + Y_2 B_2 for t = 2).
+  * backward  -- central finite differences of L = sum(dZ * Z) for every element
+                 of X, A, a, B and b; the dX shard partials against numpy.
+  * closed forms -- X = 0 gives Z = gelu(a) B + b and dA = 0; A = 0, a = 0 give
+                 Z = b, dY = dZ B^T / 2, dX = 0; db is the column sum of dZ.
+  * slices    -- the exact row/column slices equal the full result.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import oracle
+
+
+def _rel(x, ref):
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.max(np.abs(ref)) if ref.size else 0.0
+    num = np.max(np.abs(x - ref)) if ref.size else 0.0
+    return num / den if den > 0 else num
+
+
+def _rand(rng, shape, std=1.0):
+    return rng.standard_normal(shape) * std
+
+
+def _case(T, h, F, seed, stds=(1.0, 0.5, 0.5, 0.5, 0.5, 1.0)):
+    rng = np.random.default_rng(seed)
+    sX, sA, sa, sB, sb, sdZ = stds
+    return (_rand(rng, (T, h), sX), _rand(rng, (h, F), sA), _rand(rng, (F,), sa),
+            _rand(rng, (F, h), sB), _rand(rng, (h,), sb), _rand(rng, (T, h), sdZ))
+
+
+def check_gelu_vs_erf(lib):
+    x = np.linspace(-8.0, 8.0, 160001)
+    exact = 0.5 * x * (1.0 + np.vectorize(math.erf)(x / math.sqrt(2.0)))
+    err = np.max(np.abs(oracle.gelu(x, lib=lib) - exact))
+    # the tanh form's largest deviation from x*Phi(x) is 4.73e-4 (near |x| = 2.7);
+    # a wrong constant (0.04 or 0.05 for 0.044715, or sqrt(pi/2) for
+    # sqrt(2/pi)) moves it to >= 2.8e-3.
+    return [] if err <= 5.0e-4 else ["gelu deviates from x*Phi(x) by %.3e" % err]
+
+
+def check_gelu_identities(lib):
+    f = []
+    x = np.linspace(-6.0, 6.0, 1201)
+    d = oracle.gelu(x, lib=lib) - oracle.gelu(-x, lib=lib) - x
+    if np.max(np.abs(d)) > 1e-14:
+        f.append("gelu(x) - gelu(-x) != x (%.3e)" % np.max(np.abs(d)))
+    if lib.oracle_gelu(0.0) != 0.0:
+        f.append("gelu(0) != 0")
+    if abs(lib.oracle_gelu_prime(0.0) - 0.5) > 1e-15:
+        f.append("gelu'(0) != 1/2")
+    if abs(lib.oracle_gelu(30.0) - 30.0) > 1e-12 or abs(lib.oracle_gelu(-30.0)) > 1e-12:
+        f.append("gelu asymptotes wrong")
+    if abs(lib.oracle_gelu_prime(30.0) - 1.0) > 1e-12 or abs(lib.oracle_gelu_prime(-30.0)) > 1e-12:
+        f.append("gelu' asymptotes wrong")
+    return f
+
+
+def check_gelu_prime_fd(lib):
+    x = np.linspace(-6.0, 6.0, 2401)
+    eps = 1e-5
+    fd = (oracle.gelu(x + eps, lib=lib) - oracle.gelu(x - eps, lib=lib)) / (2 * eps)
+    err = np.max(np.abs(fd - oracle.gelu_prime(x, lib=lib)))
+    return [] if err <= 1e-9 else ["gelu' disagrees with central differences by %.3e" % err]
+
+
+def _numpy_forward(X, A, a, B, b, lib):
+    H = X @ A + a
+    Y = oracle.gelu(H, lib=lib)
+    return H, Y, Y @ B + b
+
+
+def check_forward_numpy(lib):
+    f = []
+    for (T, h, F), t, seed in [((5, 7, 16), 1, 1), ((6, 8, 16), 2, 2), ((9, 12, 32), 4, 3),
+                               ((4, 16, 64), 8, 4), ((1, 3, 8), 8, 5)]:
+        X, A, a, B, b, _ = _case(T, h, F, seed)
+        out = oracle.forward(X, A, a, B, b, t, parts=True, lib=lib)
+        H, Y, Z = _numpy_forward(X, A, a, B, b, lib)
+        for name, got, ref in (("H", out["H"], H), ("Y", out["Y"], Y), ("Z", out["Z"], Z)):
+            if _rel(got, ref) > 1e-12:
+                f.append("forward %s t=%d rel %.3e vs numpy" % (name, t, _rel(got, ref)))
+        Fs = F // t
+        for i in range(t):
+            S = slice(i * Fs, (i + 1) * Fs)
+            ref = Y[:, S] @ B[S, :]
+            if _rel(out["Zpart"][i], ref) > 1e-12:
+                f.append("Z partial %d of t=%d wrong" % (i, t))
+        if _rel(out["Zpart"].sum(axis=0) + b, out["Z"]) > 1e-12:
+            f.append("sum of partials + b != Z for t=%d" % t)
+    return f
+
+
+def check_worked_example_t2(lib):
+    """Two shards exactly as the report's section 4.1 writes them:
+    Y_1 = f(X W_{1,1}), Y_2 = f(X W_{1,2}), Z = Y_1 W_{2,1} + Y_2 W_{2,2} (+ b)."""
+    X, A, a, B, b, _ = _case(4, 6, 10, 11)
+    A1, A2 = A[:, :5], A[:, 5:]
+    a1, a2 = a[:5], a[5:]
+    B1, B2 = B[:5, :], B[5:, :]
+    Y1 = oracle.gelu(X @ A1 + a1, lib=lib)
+    Y2 = oracle.gelu(X @ A2 + a2, lib=lib)
+    Zref = Y1 @ B1 + Y2 @ B2 + b
+    out = oracle.forward(X, A, a, B, b, 2, parts=True, lib=lib)
+    f = []
+    if _rel(out["Z"], Zref) > 1e-12:
+        f.append("t=2 worked example: Z differs (%.3e)" % _rel(out["Z"], Zref))
+    if _rel(out["Zpart"][0], Y1 @ B1) > 1e-12 or _rel(out["Zpart"][1], Y2 @ B2) > 1e-12:
+        f.append("t=2 worked example: partials differ")
+    if _rel(out["Y"], np.concatenate([Y1, Y2], axis=1)) > 1e-12:
+        f.append("t=2 worked example: Y is not [Y_1, Y_2]")
+    return f
+
+
+def _loss(lib, X, A, a, B, b, dZ, t):
+    return float(np.sum(dZ * oracle.forward(X, A, a, B, b, t, lib=lib)["Z"]))
+
+
+def check_backward_fd(lib, shapes=((3, 4, 8),), ts=(1, 2, 4), eps=1e-6, tol=1e-6):
+    f = []
+    for (T, h, F) in shapes:
+        for t in ts:
+            X, A, a, B, b, dZ = _case(T, h, F, 100 + t)
+            fw = oracle.forward(X, A, a, B, b, t, lib=lib)
+            bw = oracle.backward(X, A, B, fw["H"], fw["Y"], dZ, t, lib=lib)
+            params = {"X": X, "A": A, "a": a, "B": B, "b": b}
+            grads = {"X": bw["dX"], "A": bw["dA"], "a": bw["da"], "B": bw["dB"], "b": bw["db"]}
+            for name, p in params.items():
+                fd = np.empty_like(p)
+                flat = p.reshape(-1)
+                for idx in range(flat.size):
+                    old = flat[idx]
+                    flat[idx] = old + eps
+                    lp = _loss(lib, X, A, a, B, b, dZ, t)
+                    flat[idx] = old - eps
+                    lm = _loss(lib, X, A, a, B, b, dZ, t)
+                    flat[idx] = old
+                    fd.reshape(-1)[idx] = (lp - lm) / (2 * eps)
+                r = _rel(grads[name], fd)
+                if r > tol:
+                    f.append("d%s (T=%d h=%d F=%d t=%d) vs finite differences: rel %.3e"
+                             % (name, T, h, F, t, r))
+    return f
+
+
+def check_backward_partials(lib):
+    f = []
+    for t in (1, 2, 4):
+        X, A, a, B, b, dZ = _case(6, 8, 16, 200 + t)
+        fw = oracle.forward(X, A, a, B, b, t, lib=lib)
+        bw = oracle.backward(X, A, B, fw["H"], fw["Y"], dZ, t, parts=True, lib=lib)
+        Fs = 16 // t
+        for i in range(t):
+            S = slice(i * Fs, (i + 1) * Fs)
+            if _rel(bw["dXpart"][i], bw["dY"][:, S] @ A[:, S].T) > 1e-12:
+                f.append("dX partial %d of t=%d wrong" % (i, t))
+        if _rel(bw["dXpart"].sum(axis=0), bw["dX"]) > 1e-12:
+            f.append("sum of dX partials != dX for t=%d" % t)
+    return f
+
+
+def check_closed_forms(lib):
+    f = []
+    T, h, F, t = 5, 6, 12, 3
+    X, A, a, B, b, dZ = _case(T, h, F, 300)
+    # X = 0: H = a in every row, so Z = gelu(a) B + b and dA = X^T dY = 0
+    Z0 = np.zeros_like(X)
+    fw = oracle.forward(Z0, A, a, B, b, t, lib=lib)
+    bw = oracle.backward(Z0, A, B, fw["H"], fw["Y"], dZ, t, lib=lib)
+    zref = np.tile(oracle.gelu(a, lib=lib) @ B + b, (T, 1))
+    if _rel(fw["Z"], zref) > 1e-12:
+        f.append("X = 0: Z != gelu(a) B + b")
+    if np.max(np.abs(bw["dA"])) != 0.0:
+        f.append("X = 0: dA != 0")
+    # A = 0, a = 0: H = 0, Y = 0, Z = b, dY = dZ B^T * gelu'(0) = dZ B^T / 2, dX = 0
+    A0 = np.zeros_like(A)
+    a0 = np.zeros_like(a)
+    fw = oracle.forward(X, A0, a0, B, b, t, lib=lib)
+    bw = oracle.backward(X, A0, B, fw["H"], fw["Y"], dZ, t, lib=lib)
+    if _rel(fw["Z"], np.tile(b, (T, 1))) > 0:
+        f.append("A = 0, a = 0: Z != b")
+    if _rel(bw["dY"], 0.5 * dZ @ B.T) > 1e-12:
+        f.append("A = 0, a = 0: dY != dZ B^T / 2")
+    if np.max(np.abs(bw["dX"])) != 0.0:
+        f.append("A = 0, a = 0: dX != 0")
+    if np.max(np.abs(bw["dB"])) != 0.0:
+        f.append("A = 0, a = 0: dB != 0 (Y = 0)")
+    # db is the column sum of dZ whatever the weights
+    if _rel(bw["db"], dZ.sum(axis=0)) > 1e-13:
+        f.append("db != column sum of dZ")
+    return f
+
+
+def check_slice_vs_full(lib):
+    f = []
+    for (T, h, F), t, seed in [((13, 10, 24), 2, 400), ((128, 32, 64), 4, 401), ((7, 5, 16), 1, 402)]:
+        X, A, a, B, b, dZ = _case(T, h, F, seed)
+        full = oracle.forward_backward(X, A, a, B, b, dZ, t, lib=lib)
+        rng = np.random.default_rng(seed)
+        R = np.sort(rng.choice(T, size=min(T, 5), replace=False))
+        J = np.sort(rng.choice(F, size=min(F, 7), replace=False))
+        s = oracle.slice_(X, A, a, B, b, dZ, t, R, J, lib=lib)
+        pairs = [("Hr", full["H"][R]), ("Yr", full["Y"][R]), ("dYr", full["dY"][R]),
+                 ("Zr", full["Z"][R]), ("dXr", full["dX"][R]),
+                 ("Hc", full["H"][:, J]), ("Yc", full["Y"][:, J]), ("dYc", full["dY"][:, J]),
+                 ("dAc", full["dA"][:, J]), ("daJ", full["da"][J]), ("dBr", full["dB"][J]),
+                 ("db", full["db"])]
+        for k, ref in pairs:
+            if _rel(s[k], ref) > 1e-12:
+                f.append("slice %s differs from the full oracle (T=%d t=%d): %.3e"
+                         % (k, T, t, _rel(s[k], ref)))
+    return f
+
+
+ALL = [check_gelu_vs_erf, check_gelu_identities, check_gelu_prime_fd, check_forward_numpy,
+       check_worked_example_t2, check_backward_fd, check_backward_partials,
+       check_closed_forms, check_slice_vs_full]
+
+
+def run_all(lib) -> list:
+    out = []
+    for c in ALL:
+        try:
+            out += ["%s: %s" % (c.__name__, m) for m in c(lib)]
+        except Exception as e:  # a planted mistake may also make a check raise
+            out.append("%s raised %r" % (c.__name__, e))
+    return out

@@ -1,0 +1,59 @@
+"""Plant plausible mistakes in a copy of the oracle and check the pins catch each.
+
+Every mutant is a one-line edit of ``oracle/oracle.c`` compiled into a temporary
+library on the CPU; the shipped oracle is never touched.  A mutant that no pin
+catches would mean the pins leave that part of the oracle unchecked.
+"""
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+import oracle_pins
+
+MUTANTS = {
+    # the bias b added once per shard instead of once after the all-reduce
+    "bias_per_shard": ("Z[r * h + j] = b[j] + sum[j];", "Z[r * h + j] = t * b[j] + sum[j];"),
+    # wrong cubic coefficient in the tanh argument of GeLU
+    "gelu_constant": ("    double u = c * (x + 0.044715 * x * x * x);\n    return",
+                      "    double u = c * (x + 0.05 * x * x * x);\n    return"),
+    # derivative of tanh(u) without the inner derivative du/dx
+    "gelu_prime_chain": ("0.5 * x * (1.0 - th * th) * du;", "0.5 * x * (1.0 - th * th);"),
+    # sign error in dY
+    "dY_sign": ("dY[r * F + f] = g * oracle_gelu_prime", "dY[r * F + f] = -g * oracle_gelu_prime"),
+    # transposed / misindexed operand in dA = X^T dY
+    "dA_index": ("for (int64_t f = 0; f < F; ++f) dAk[f] += x * dYr[f];",
+                 "for (int64_t f = 0; f < F; ++f) dAk[f] += x * dYr[F - 1 - f];"),
+    # the backward all-reduce drops the last shard
+    "dX_drop_shard": ("                if (dXpart) dXpart[((int64_t)i * T + r) * h + k] = p;\n"
+                      "                sum += p;",
+                      "                if (dXpart) dXpart[((int64_t)i * T + r) * h + k] = p;\n"
+                      "                if (i + 1 < t || t == 1) sum += p;"),
+    # da summed over the wrong column
+    "da_column": ("for (int64_t r = 0; r < T; ++r) s += dY[r * F + f];",
+                  "for (int64_t r = 0; r < T; ++r) s += dY[r * F + (f + 1) % F];"),
+    # the forward uses the wrong shard range for the row-parallel GEMM
+    "shard_range": ("for (int64_t f = i * Fs; f < (i + 1) * Fs; ++f) {\n                    const double yf = Yr[f];",
+                    "for (int64_t f = i * Fs; f < (i + 1) * Fs - 1; ++f) {\n                    const double yf = Yr[f];"),
+    # the slice oracle reads the wrong token row
+    "slice_row": ("const int64_t r = R[q];", "const int64_t r = (R[q] + 1) % T;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name):
+    old, new = MUTANTS[name]
+    src = open(oracle._SRC).read()
+    assert src.count(old) == 1, "mutation site for %s not found exactly once" % name
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "mutant.c")
+        so = os.path.join(d, "libmutant.so")
+        with open(c, "w") as fh:
+            fh.write(src.replace(old, new))
+        subprocess.run(["gcc", "-O2", "-fopenmp", "-std=c11", "-shared", "-fPIC", c, "-o", so, "-lm"],
+                       check=True)
+        lib = oracle.load(so)
+        failures = oracle_pins.run_all(lib)
+    assert failures, "planted mistake %r passed every pin" % name
