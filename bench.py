@@ -1,0 +1,380 @@
+#!/usr/bin/env python
+"""Throughput of the TP-MLP block (forward + backward) on GB300.
+
+One step = tpmlp_forward + tpmlp_backward over one batch of the workload
+(default: h8192 -- T=4096 tokens, h=8192, F=32768, t=8 shards, bf16), inputs
+resident in HBM.  FLOPs per step: 3 x (2 GEMMs x 2*T*h*F) = 12*T*h*F.
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs an independent
+replica of the workload (the path has no cross-GPU step here): weak scaling.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on a token sample
+  python bench.py --sweep                # microbatch sweep, one line per b
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from tensor_transformer_mlp_tma_gb300 import inputs  # noqa: E402
+from tensor_transformer_mlp_tma_gb300.workloads import HEADLINE, WORKLOADS  # noqa: E402
+
+METRIC = "TP-MLP fwd+bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes (read + write) per launch of each tensor-core GEMM, from one ncu
+# capture, with the hash of the kernel source they were taken at.  A kernel whose
+# source has changed since reports traffic null.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    p = os.path.join(ROOT, "tensor_transformer_mlp_tma_gb300", "csrc", "tc_gemm.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:12]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.idx = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", str(self.period)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle leg
+def oracle_sample(w, tokens: int):
+    """Time the fp64 oracle on the first `tokens` rows of the workload (full
+    weights); returns (seconds, flops, threads)."""
+    import oracle
+    inp = inputs.for_workload(w, tokens=tokens)
+    lib = oracle.load()
+    f64 = {k: oracle._f64(v) for k, v in inp.items()}
+    t0 = time.perf_counter()
+    oracle.forward_backward(f64["X"], f64["A"], f64["a"], f64["B"], f64["b"], f64["dZ"], w.shards[-1], lib=lib)
+    dt = time.perf_counter() - t0
+    return dt, 12.0 * tokens * w.hidden * w.ffn, oracle.num_threads(lib)
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle as it stands, on host cores."""
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    import oracle
+    inp = inputs.for_workload(w, tokens=args.oracle_tokens)
+    lib = oracle.load()
+    f64 = {k: oracle._f64(v) for k, v in inp.items()}
+    t = w.shards[-1]
+
+    def step():
+        oracle.forward_backward(f64["X"], f64["A"], f64["a"], f64["B"], f64["b"], f64["dZ"], t, lib=lib)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = 12.0 * args.oracle_tokens * w.hidden * w.ffn
+    val = flops / dt / 1e12
+    sample = "first %d of %d token rows of %s per step, full weights, fp64" % (args.oracle_tokens, w.tokens, w.name)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, t, world),
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": oracle.num_threads(lib), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, t, world):
+    return {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden, "ffn": w.ffn, "t": t,
+            "dtype": w.dtype, "parallelism": "replicas x%d" % world if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (A, B 537 MB each; ~3.2 GB touched per step)"
+            if w.name == "h8192" else "per-step working set larger than L2"}
+
+
+# ------------------------------------------------------------------ GPU leg
+def run_ours(args, rank, world, local, w=None, quiet=False):
+    from tensor_transformer_mlp_tma_gb300 import tpmlp
+    w = w or WORKLOADS[args.workload]
+    t = args.t or w.shards[-1]
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    dt = inputs.torch_dtype(w.dtype)
+    host = inputs.for_workload(w, seed=args.seed + rank)
+    d = {k: v.to(dev) for k, v in host.items()}
+    T, h, F = w.tokens, w.hidden, w.ffn
+    ctx = tpmlp.Context(T, h, F, t, dt, device=dev)
+    Z = torch.empty((T, h), dtype=dt, device=dev)
+    g = {"dX": torch.empty((T, h), dtype=dt, device=dev), "dA": torch.empty((h, F), dtype=dt, device=dev),
+         "da": torch.empty((F,), dtype=dt, device=dev), "dB": torch.empty((F, h), dtype=dt, device=dev),
+         "db": torch.empty((h,), dtype=dt, device=dev)}
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        tpmlp.forward(ctx, d["X"], d["A"], d["a"], d["B"], d["b"], Z=Z, stream=stream)
+        tpmlp.backward(ctx, d["dZ"], stream=stream, **g)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    st = tpmlp.check_device_status(ctx, stream)
+    if st != tpmlp.OK:
+        raise RuntimeError("device status after warm-up: %s" % tpmlp.status_string(st))
+
+    # ---- timed region: inputs resident in HBM
+    tpmlp.profile_reset()
+    tpmlp.profile_enable(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    launches0 = tpmlp.launch_count()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clocks:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    launches = tpmlp.launch_count() - launches0
+    tpmlp.profile_enable(False)
+    kernels = tpmlp.profile_collect()
+    ms = e0.elapsed_time(e1) / args.steps
+    st = tpmlp.check_device_status(ctx, stream)
+    if st != tpmlp.OK:
+        raise RuntimeError("device status after timed region: %s" % tpmlp.status_string(st))
+    ms_max = max_over_ranks(ms, world)
+    flops = 12.0 * T * h * F
+    value = flops * world / (ms_max * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    # dominant kernel: largest share of the timed region
+    name, (n, tot) = max(kernels.items(), key=lambda kv: kv[1][1])
+    per_launch_ms = tot / n
+    gemm_flops = {"fc1_bias_gelu": 2.0 * T * h * F, "fc2_shard_fold": 2.0 * T * h * F,
+                  "bwd_dY_dgelu": 2.0 * T * h * F, "bwd_dB": 2.0 * T * h * F, "bwd_dA": 2.0 * T * h * F,
+                  "bwd_dX_shard_fold": 2.0 * T * h * F}
+    if name in gemm_flops:
+        achieved = gemm_flops[name] / (per_launch_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        tr = NCU_TRAFFIC.get(name)
+        traffic = tr[0] if tr and tr[1] == kernel_source_hash() else None
+        roof = {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": peak, "unit": UNIT,
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": "%s bf16_tflops_sustained (kernel timed inside a long step)" % peak_src}
+    else:  # a column sum: HBM bound
+        roof = {"bound": "hbm", "kernel": name, "achieved": None, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": None, "traffic": None}
+
+    # ---- end to end: pinned host inputs in, results out, every step
+    e2e = None
+    if not args.no_e2e:
+        hX = host["X"].pin_memory()
+        hdZ = host["dZ"].pin_memory()
+        oZ = torch.empty((T, h), dtype=dt).pin_memory()
+        odX = torch.empty((T, h), dtype=dt).pin_memory()
+        oda = torch.empty((F,), dtype=dt).pin_memory()
+        odb = torch.empty((h,), dtype=dt).pin_memory()
+        dX_in = torch.empty_like(d["X"])
+        dZ_in = torch.empty_like(d["dZ"])
+
+        def e2e_step():
+            dX_in.copy_(hX, non_blocking=True)
+            dZ_in.copy_(hdZ, non_blocking=True)
+            tpmlp.forward(ctx, dX_in, d["A"], d["a"], d["B"], d["b"], Z=Z, stream=stream)
+            tpmlp.backward(ctx, dZ_in, stream=stream, **g)
+            oZ.copy_(Z, non_blocking=True)
+            odX.copy_(g["dX"], non_blocking=True)
+            oda.copy_(g["da"], non_blocking=True)
+            odb.copy_(g["db"], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, args.warmup)):
+                e2e_step()
+            torch.cuda.synchronize(dev)
+            barrier(world)
+            f0 = torch.cuda.Event(enable_timing=True)
+            f1 = torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            for _ in range(args.steps):
+                e2e_step()
+            f1.record(stream)
+            torch.cuda.synchronize(dev)
+        barrier(world)
+        ems = max_over_ranks(f0.elapsed_time(f1) / args.steps, world)
+        esz = hX.element_size()
+        e2e = {"value": flops * world / (ems * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ems,
+               "h2d_bytes_per_step": (hX.numel() + hdZ.numel()) * esz,
+               "d2h_bytes_per_step": (oZ.numel() + odX.numel() + oda.numel() + odb.numel()) * esz,
+               "what": "X and dZ copied in from pinned host memory, Z, dX, da, db copied out, every "
+                       "step; weights and weight gradients stay resident"}
+
+    clk = clocks.summary()
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": config_of(w, t, world),
+            "frac_of_peak": value / world / peaks["bf16_tflops_sustained"],
+            "peak_tflops": peaks["bf16_tflops_sustained"], "peak_source": peak_src,
+            "roofline": roof, "e2e": e2e, "gpu_launches": int(sum_over_ranks(launches, world)),
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
+            "kernels": {k: {"launches": n, "ms_per_launch": tot / n, "share": tot / sum(v[1] for v in kernels.values())}
+                        for k, (n, tot) in kernels.items()}}
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--t", type=int, default=0, help="shard count (default: the workload's)")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--sweep", action="store_true", help="microbatch sweep h12288-b{1,2,4,8}")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-tokens", type=int, default=32,
+                    help="token rows of the oracle's bounded sample")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if args.sweep:
+        for b in (1, 2, 4, 8):
+            line = run_ours(args, rank, world, local, w=WORKLOADS["h12288-b%d" % b])
+            if rank == 0:
+                print(json.dumps(line), flush=True)
+        return
+    line = run_ours(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            w = WORKLOADS[args.workload]
+            secs, fl, cores = oracle_sample(w, args.oracle_tokens)
+            line["cpu_baseline"] = {"value": fl / secs / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                    "sample": "first %d of %d token rows of %s, full weights, fp64 (%.1f s)"
+                                              % (args.oracle_tokens, w.tokens, w.name, secs)}
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

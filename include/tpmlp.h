@@ -1,0 +1,176 @@
+/*
+ * tpmlp -- the tensor-parallel Transformer MLP block on one GB300 (sm_103a).
+ *
+ *     Z = GeLU(X A + a) B + b
+ *
+ * The method ("Megatron-LM" industry report, section 4.1, basic principle of
+ * tensor parallelism): the first weight A is split by columns into t shards
+ * [A_1 .. A_t] (with its bias a), the second weight B by rows into [B_1 .. B_t];
+ * the input X is replicated; shard i computes Y_i = GeLU(X A_i + a_i) and the
+ * partial product Z_i = Y_i B_i; an all-reduce sums the Z_i.  Section 4.2 of the
+ * same report adds that the exchange runs in both directions, i.e. the backward
+ * pass sums the shard contributions to dX.  Here all t shards live on one GPU:
+ * the column-parallel GEMM of every shard is one launch (the shards are disjoint
+ * column blocks) and each all-reduce is a fixed-order fp32 sum of the t shard
+ * partials, Z = b + (((Z_1 + Z_2) + Z_3) + ... + Z_t), done on chip.  Repeated
+ * calls with the same inputs give bit-identical outputs.
+ *
+ * Layout.  Every tensor is row-major, contiguous and in device memory:
+ *   X[T,h]  A[h,F]  a[F]  B[F,h]  b[h]  Z[T,h]  H,Y[T,F]  (T tokens, h hidden,
+ *   F ffn).  Shard i (0-based) owns columns [i*F/t, (i+1)*F/t) of A and a and
+ *   the same rows of B.  Weights are in the math layout X.A, not in the
+ *   [out, in] layout of a PyTorch Linear.
+ *
+ * Types.  Every input and output of one call has the shape's dtype (fp32 or
+ * bf16).  bf16 runs on the tensor cores (tcgen05, fp32 accumulation, fp32
+ * epilogue math, round-to-nearest-even on store); fp32 runs on plain FFMA
+ * kernels (no TF32).
+ *
+ * Ownership.  The caller owns all memory.  The library allocates no device
+ * memory; it keeps only host-side caches (device properties, kernel attributes).
+ *
+ * Streams and errors.  Calls are asynchronous on the given CUDA stream (a
+ * cudaStream_t passed as void*, NULL = the legacy default stream).  The return
+ * value covers host-side validation and launch errors only.  Errors found on the
+ * device (a bounded wait that ran out) are recorded in the status word at the
+ * start of the workspace and read by tpmlp_check_device_status().
+ *
+ * Thread safety.  Calls may be made from several host threads; each call only
+ * reads its arguments and the shared caches are locked.
+ */
+#ifndef TPMLP_H
+#define TPMLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TPMLP_OK = 0,
+    TPMLP_ERR_INVALID_ARG = 1, /* a NULL pointer, a size <= 0, t out of [1,16], F % t != 0 */
+    TPMLP_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels take (alignment, F/t % 64) */
+    TPMLP_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
+    TPMLP_ERR_TIMEOUT = 4,     /* a bounded device-side wait ran out (device status word) */
+    TPMLP_ERR_DEVICE = 5       /* no usable sm_100-family device */
+} tpmlp_status;
+
+typedef enum { TPMLP_F32 = 0, TPMLP_BF16 = 1 } tpmlp_dtype;
+
+/* Kernel family.  DEFAULT: tensor cores for bf16, FFMA for fp32.  SIMT: FFMA
+ * kernels for either dtype (a second, independent GPU path used to cross-check
+ * the tensor-core kernels). */
+typedef enum { TPMLP_ALGO_DEFAULT = 0, TPMLP_ALGO_SIMT = 1 } tpmlp_algo;
+
+typedef struct {
+    int64_t tokens; /* T >= 0 (T = 0 is an empty batch) */
+    int64_t hidden; /* h > 0 */
+    int64_t ffn;    /* F > 0, F % t == 0 */
+    int32_t t;      /* number of tensor-parallel shards, 1..16 */
+    int32_t dtype;  /* tpmlp_dtype */
+    int32_t algo;   /* tpmlp_algo */
+    int32_t reserved; /* must be 0 */
+} tpmlp_shape;
+
+/* What the forward pass keeps for the backward pass.  The caller allocates H and
+ * Y (T*F elements each, tpmlp_saved_bytes() in total); tpmlp_forward() fills in
+ * X, A and B with the pointers it was given.  H may be NULL in a forward-only
+ * (inference) call, in which case the pre-activation is not stored; Y is always
+ * needed because the row-parallel GEMM reads it. */
+typedef struct {
+    const void *X;
+    const void *A;
+    const void *B;
+    void *H; /* pre-activation X A + a, [T,F] */
+    void *Y; /* GeLU(H), [T,F] */
+} tpmlp_saved;
+
+/* Offsets into the workspace, for callers that want the intermediates. */
+typedef enum {
+    TPMLP_WS_STATUS = 0,  /* uint32 status word (tpmlp_status), then a uint32 detail word */
+    TPMLP_WS_PARTIALS = 1, /* fp32 column-sum partials */
+    TPMLP_WS_DY = 2        /* dY = (dZ B^T) * GeLU'(H), [T,F] in the shape's dtype */
+} tpmlp_ws_region;
+
+/* Human-readable name of a status code (static storage). */
+const char *tpmlp_status_string(tpmlp_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int tpmlp_version(void);
+
+/* Bytes the caller must allocate for H and Y together (2*T*F elements); 0 when
+ * the shape is invalid. */
+size_t tpmlp_saved_bytes(const tpmlp_shape *shape);
+
+/* Bytes of device workspace forward and backward need: the status word, the
+ * column-sum partials and the dY intermediate.  A 256-byte aligned buffer of at
+ * least this size, whose first 8 bytes are zero before first use, is required.
+ * 0 when the shape is invalid. */
+size_t tpmlp_workspace_bytes(const tpmlp_shape *shape);
+
+/* Byte offset of a region inside the workspace (see tpmlp_ws_region);
+ * (size_t)-1 when the shape or region is invalid. */
+size_t tpmlp_workspace_offset(const tpmlp_shape *shape, int region);
+
+/* Forward pass ("Megatron-LM" report, section 4.1):
+ *   H = X A + a,  Y = GeLU(H)   -- the column-parallel GEMM of all t shards,
+ *                                  bias and GeLU fused in its epilogue;
+ *   Z = b + sum_{i=1..t} Y_i B_i -- the row-parallel GEMM; the t shard partials
+ *                                  are summed in order on chip, then b is added.
+ * X[T,h], A[h,F], a[F], B[F,h], b[h] are inputs; Z[T,h] is the output; saved->Y
+ * (and saved->H unless NULL) receive the activations.  GeLU is the tanh form
+ * 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+ * Errors: INVALID_ARG for NULL shape/pointers (saved->H excepted), bad sizes;
+ * UNSUPPORTED on the tensor-core path when a pointer is not 16-byte aligned,
+ * h or F is not a multiple of 8, or t > 1 and F/t is not a multiple of 64;
+ * CUDA when a launch fails.  Nothing is launched when an error is returned. */
+tpmlp_status tpmlp_forward(const tpmlp_shape *shape, const void *X, const void *A, const void *a,
+                           const void *B, const void *b, void *Z, tpmlp_saved *saved,
+                           void *workspace, void *stream);
+
+/* Backward pass for the scalar loss L = sum(dZ * Z) (the chain rule; the report
+ * states only that the exchange also runs backward, section 4.2):
+ *   db = 1^T dZ,  dY = (dZ B^T) * GeLU'(H),  da = 1^T dY,
+ *   dB = Y^T dZ,  dA = X^T dY,  dX = sum_{i=1..t} dY_i A_i^T  (fixed-order sum).
+ * dZ[T,h] and the saved activations are inputs; dX[T,h], dA[h,F], da[F],
+ * dB[F,h], db[h] are outputs.  dY is left in the workspace (TPMLP_WS_DY).
+ * With T = 0 the weight and bias gradients are set to zero.
+ * Errors: as tpmlp_forward; saved->H, saved->Y, X, A, B must all be set. */
+tpmlp_status tpmlp_backward(const tpmlp_shape *shape, const void *dZ, const tpmlp_saved *saved,
+                            void *dX, void *dA, void *da, void *dB, void *db,
+                            void *workspace, void *stream);
+
+/* Synchronises the stream, reads the workspace status word, clears it and
+ * returns it (TPMLP_OK when no device-side error was recorded). */
+tpmlp_status tpmlp_check_device_status(void *workspace, void *stream);
+
+/* Upper limit, in nanoseconds, of every device-side wait of later launches
+ * (default 2e9).  A wait that runs out records TPMLP_ERR_TIMEOUT and the kernel
+ * returns after releasing what it holds. */
+void tpmlp_set_wait_limit_ns(uint64_t ns);
+
+/* Launches one small kernel that waits on a barrier nothing arrives on, for at
+ * most wait_ns, then records TPMLP_ERR_TIMEOUT in the workspace status word and
+ * returns (after freeing the tensor memory it allocated).  It exercises the
+ * error path of the bounded waits without faulting or hanging the GPU. */
+tpmlp_status tpmlp_debug_timeout_probe(void *workspace, uint64_t wait_ns, void *stream);
+
+/* Number of kernels this library has launched since it was loaded. */
+uint64_t tpmlp_launch_count(void);
+
+/* Per-kernel timing.  While enabled, every launch is bracketed by CUDA events
+ * on its own stream; tpmlp_profile_collect() waits for them and adds their
+ * durations to a per-kernel table (name, launches, total milliseconds). */
+void tpmlp_profile_enable(int on);
+void tpmlp_profile_reset(void);
+tpmlp_status tpmlp_profile_collect(void);
+int tpmlp_profile_count(void);
+int tpmlp_profile_entry(int i, char *name, int name_len, int64_t *launches, double *total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPMLP_H */

@@ -1,0 +1,440 @@
+// The C ABI of libtpmlp.so (declared in include/tpmlp.h): argument validation,
+// workspace layout, the launch sequence of the forward and backward passes, the
+// device status word and per-kernel timing.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kernels.h"
+#include "tpmlp.h"
+
+namespace {
+
+using tpmlp::Epi;
+using tpmlp::GemmArgs;
+
+std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_wait_ns{2000000000ull};
+
+// ---- per-kernel timing --------------------------------------------------------
+struct PendingTiming {
+    std::string name;
+    cudaEvent_t e0, e1;
+};
+struct TimingTotal {
+    int64_t launches = 0;
+    double ms = 0.0;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<PendingTiming> g_pending;
+std::vector<cudaEvent_t> g_event_pool;
+std::vector<std::pair<std::string, TimingTotal>> g_totals;
+
+cudaEvent_t get_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Brackets one launch with events on its stream when timing is on.
+struct Timed {
+    const char *name;
+    cudaStream_t st;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    Timed(const char *n, cudaStream_t s) : name(n), st(s) {
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        if (!g_prof_on) return;
+        e0 = get_event();
+        e1 = get_event();
+        if (e0 && e1) cudaEventRecord(e0, st);
+    }
+    ~Timed() {
+        if (!e0 || !e1) return;
+        cudaEventRecord(e1, st);
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        g_pending.push_back({name, e0, e1});
+    }
+};
+
+// ---- device properties -----------------------------------------------------------
+int num_sms_current() {
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache[dev] == 0) {
+        int n = 0, major = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return 0;
+        int minor = 0;
+        if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return 0;
+        cache[dev] = (major == 10 && minor == 3) ? n : -1;  // the kernels are built for sm_103a only
+    }
+    return cache[dev];
+}
+
+// ---- shapes and workspace --------------------------------------------------------------
+bool shape_valid(const tpmlp_shape *s) {
+    if (!s) return false;
+    if (s->tokens < 0 || s->hidden <= 0 || s->ffn <= 0) return false;
+    if (s->t < 1 || s->t > 16 || s->ffn % s->t != 0) return false;
+    if (s->dtype != TPMLP_F32 && s->dtype != TPMLP_BF16) return false;
+    if (s->algo != TPMLP_ALGO_DEFAULT && s->algo != TPMLP_ALGO_SIMT) return false;
+    if (s->reserved != 0) return false;
+    // int32 tile and grid arithmetic inside the kernels
+    if (s->tokens > (1LL << 30) || s->hidden > (1LL << 30) || s->ffn > (1LL << 30)) return false;
+    return true;
+}
+
+size_t elt(const tpmlp_shape *s) { return s->dtype == TPMLP_BF16 ? 2 : 4; }
+
+bool use_tc(const tpmlp_shape *s) { return s->dtype == TPMLP_BF16 && s->algo == TPMLP_ALGO_DEFAULT; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+constexpr size_t STATUS_BYTES = 1024;
+
+size_t partials_bytes(const tpmlp_shape *s) {
+    const int64_t T = s->tokens, h = s->hidden, F = s->ffn;
+    const int64_t p1 = tpmlp::colsum_chunks(T, h) * h;
+    const int64_t p2 = tpmlp::colsum_chunks(T, F) * F;
+    return align_up(static_cast<size_t>(p1 > p2 ? p1 : p2) * sizeof(float), 1024);
+}
+
+size_t dy_offset(const tpmlp_shape *s) { return STATUS_BYTES + partials_bytes(s); }
+
+size_t dy_bytes(const tpmlp_shape *s) {
+    return align_up(static_cast<size_t>(s->tokens) * static_cast<size_t>(s->ffn) * elt(s), 1024);
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned_elt(const void *p, size_t e) { return (reinterpret_cast<uintptr_t>(p) % e) == 0; }
+
+// Checks common to forward and backward.  Returns OK, INVALID_ARG or UNSUPPORTED.
+tpmlp_status check_ptrs(const tpmlp_shape *s, std::initializer_list<const void *> required,
+                        std::initializer_list<const void *> optional) {
+    for (const void *p : required)
+        if (!p) return TPMLP_ERR_INVALID_ARG;
+    const size_t e = elt(s);
+    for (const void *p : required)
+        if (!aligned_elt(p, e)) return TPMLP_ERR_UNSUPPORTED;
+    for (const void *p : optional)
+        if (p && !aligned_elt(p, e)) return TPMLP_ERR_UNSUPPORTED;
+    if (use_tc(s)) {
+        // TMA: 16-byte aligned bases and row pitches; shard boundaries on 64-element k-blocks.
+        for (const void *p : required)
+            if (!aligned16(p)) return TPMLP_ERR_UNSUPPORTED;
+        for (const void *p : optional)
+            if (p && !aligned16(p)) return TPMLP_ERR_UNSUPPORTED;
+        if (s->hidden % 8 != 0 || s->ffn % 8 != 0) return TPMLP_ERR_UNSUPPORTED;
+        if (s->t > 1 && (s->ffn / s->t) % 64 != 0) return TPMLP_ERR_UNSUPPORTED;
+    }
+    return TPMLP_OK;
+}
+
+tpmlp_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA; }
+
+// One GEMM launch on the selected path.
+cudaError_t gemm(const tpmlp_shape *s, const char *name, Epi epi, const GemmArgs &g, int sms,
+                 cudaStream_t st) {
+    Timed timed(name, st);
+    cudaError_t e;
+    if (use_tc(s))
+        e = tpmlp::launch_tc_gemm(epi, g, sms, st);
+    else
+        e = tpmlp::launch_simt_gemm(epi, s->dtype == TPMLP_BF16, g, st);
+    if (e == cudaSuccess && g.M > 0 && g.N > 0) g_launches.fetch_add(1);
+    return e;
+}
+
+cudaError_t colsum(const tpmlp_shape *s, const char *name, const void *x, int64_t rows, int64_t cols,
+                   float *partials, void *out, cudaStream_t st) {
+    Timed timed(name, st);
+    int n = 0;
+    cudaError_t e = tpmlp::launch_colsum(s->dtype == TPMLP_BF16, x, rows, cols, partials, out, st, &n);
+    g_launches.fetch_add(static_cast<uint64_t>(n));
+    return e;
+}
+
+GemmArgs base_args(uint32_t *status) {
+    GemmArgs g;
+    std::memset(&g, 0, sizeof(g));
+    g.nshards = 1;
+    g.status = status;
+    g.wait_ns = g_wait_ns.load();
+    g.group_m = 1;
+    return g;
+}
+
+// Raster order: the operand with fewer bytes is the one re-read across the N
+// (or M) tiles that run together, the other one streams through once.
+int pick_group(const GemmArgs &g) {
+    const int64_t m_tiles = (g.M + 127) / 128;
+    const double a_bytes = static_cast<double>(g.M) * g.K, b_bytes = static_cast<double>(g.N) * g.K;
+    return a_bytes <= b_bytes ? static_cast<int>(m_tiles) : 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *tpmlp_status_string(tpmlp_status s) {
+    switch (s) {
+        case TPMLP_OK: return "ok";
+        case TPMLP_ERR_INVALID_ARG: return "invalid argument";
+        case TPMLP_ERR_UNSUPPORTED: return "unsupported argument (alignment or shard size)";
+        case TPMLP_ERR_CUDA: return "CUDA error";
+        case TPMLP_ERR_TIMEOUT: return "device-side wait timed out";
+        case TPMLP_ERR_DEVICE: return "no usable sm_100-family device";
+    }
+    return "unknown status";
+}
+
+int tpmlp_version(void) { return 100; }
+
+size_t tpmlp_saved_bytes(const tpmlp_shape *s) {
+    if (!shape_valid(s)) return 0;
+    return 2 * static_cast<size_t>(s->tokens) * static_cast<size_t>(s->ffn) * elt(s);
+}
+
+size_t tpmlp_workspace_bytes(const tpmlp_shape *s) {
+    if (!shape_valid(s)) return 0;
+    return dy_offset(s) + dy_bytes(s);
+}
+
+size_t tpmlp_workspace_offset(const tpmlp_shape *s, int region) {
+    if (!shape_valid(s)) return static_cast<size_t>(-1);
+    switch (region) {
+        case TPMLP_WS_STATUS: return 0;
+        case TPMLP_WS_PARTIALS: return STATUS_BYTES;
+        case TPMLP_WS_DY: return dy_offset(s);
+    }
+    return static_cast<size_t>(-1);
+}
+
+tpmlp_status tpmlp_forward(const tpmlp_shape *s, const void *X, const void *A, const void *a,
+                           const void *B, const void *b, void *Z, tpmlp_saved *saved,
+                           void *workspace, void *stream) {
+    if (!shape_valid(s) || !saved || !workspace) return TPMLP_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return TPMLP_ERR_UNSUPPORTED;
+    tpmlp_status rc = check_ptrs(s, {X, A, a, B, b, Z, saved->Y}, {saved->H});
+    if (rc != TPMLP_OK) return rc;
+    saved->X = X;
+    saved->A = A;
+    saved->B = B;
+    const int64_t T = s->tokens, h = s->hidden, F = s->ffn;
+    if (T == 0) return TPMLP_OK;
+    const int sms = num_sms_current();
+    if (sms == 0) return TPMLP_ERR_CUDA;
+    if (use_tc(s) && sms < 0) return TPMLP_ERR_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t *status = static_cast<uint32_t *>(workspace);
+
+    // Column-parallel GEMM of all shards, bias and GeLU fused: H = X A + a, Y = GeLU(H).
+    GemmArgs g1 = base_args(status);
+    g1.a = X, g1.a_mn = false;  // X[T,h]: K-major
+    g1.b = A, g1.b_mn = true;   // A[h,F]: N contiguous, MN-major
+    g1.M = T, g1.N = F, g1.K = h, g1.kshard = h;
+    g1.out0 = saved->H, g1.out1 = saved->Y, g1.bias = a;
+    g1.group_m = pick_group(g1);
+    cudaError_t e = gemm(s, "fc1_bias_gelu", tpmlp::EPI_BIAS_GELU, g1, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    // Row-parallel GEMM, one accumulation per shard, shard partials folded in order, + b.
+    GemmArgs g2 = base_args(status);
+    g2.a = saved->Y, g2.a_mn = false;  // Y[T,F]: K-major
+    g2.b = B, g2.b_mn = true;          // B[F,h]: MN-major
+    g2.M = T, g2.N = h, g2.K = F;
+    g2.nshards = s->t, g2.kshard = F / s->t;
+    g2.out0 = Z, g2.bias = b;
+    g2.group_m = pick_group(g2);
+    e = gemm(s, "fc2_shard_fold", tpmlp::EPI_FOLD_BIAS, g2, sms, st);
+    return from_cuda(e);
+}
+
+tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_saved *saved, void *dX,
+                            void *dA, void *da, void *dB, void *db, void *workspace, void *stream) {
+    if (!shape_valid(s) || !saved || !workspace) return TPMLP_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return TPMLP_ERR_UNSUPPORTED;
+    tpmlp_status rc =
+        check_ptrs(s, {dZ, saved->X, saved->A, saved->B, saved->H, saved->Y, dX, dA, da, dB, db}, {});
+    if (rc != TPMLP_OK) return rc;
+    const int64_t T = s->tokens, h = s->hidden, F = s->ffn;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        // Empty batch: the weight and bias gradients are sums over no tokens.
+        cudaError_t e = cudaMemsetAsync(dA, 0, static_cast<size_t>(h) * F * elt(s), st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dB, 0, static_cast<size_t>(F) * h * elt(s), st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(da, 0, static_cast<size_t>(F) * elt(s), st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(db, 0, static_cast<size_t>(h) * elt(s), st);
+        return from_cuda(e);
+    }
+    const int sms = num_sms_current();
+    if (sms == 0) return TPMLP_ERR_CUDA;
+    if (use_tc(s) && sms < 0) return TPMLP_ERR_DEVICE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint32_t *status = reinterpret_cast<uint32_t *>(ws);
+    float *partials = reinterpret_cast<float *>(ws + STATUS_BYTES);
+    void *dY = ws + dy_offset(s);
+
+    // db = column sums of dZ
+    cudaError_t e = colsum(s, "colsum_db", dZ, T, h, partials, db, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    // dY = (dZ B^T) * GeLU'(H)
+    GemmArgs g3 = base_args(status);
+    g3.a = dZ, g3.a_mn = false;        // dZ[T,h]: K-major
+    g3.b = saved->B, g3.b_mn = false;  // B[F,h] as [N=F, K=h]: K-major
+    g3.M = T, g3.N = F, g3.K = h, g3.kshard = h;
+    g3.out0 = dY, g3.aux = saved->H;
+    g3.group_m = pick_group(g3);
+    e = gemm(s, "bwd_dY_dgelu", tpmlp::EPI_DGELU, g3, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    // da = column sums of dY
+    e = colsum(s, "colsum_da", dY, T, F, partials, da, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    // dB = Y^T dZ
+    GemmArgs g4 = base_args(status);
+    g4.a = saved->Y, g4.a_mn = true;  // Y[T,F] as [K=T, M=F]: MN-major
+    g4.b = dZ, g4.b_mn = true;        // dZ[T,h] as [K=T, N=h]: MN-major
+    g4.M = F, g4.N = h, g4.K = T, g4.kshard = T;
+    g4.out0 = dB;
+    g4.group_m = pick_group(g4);
+    e = gemm(s, "bwd_dB", tpmlp::EPI_STORE, g4, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    // dA = X^T dY
+    GemmArgs g5 = base_args(status);
+    g5.a = saved->X, g5.a_mn = true;  // X[T,h] as [K=T, M=h]: MN-major
+    g5.b = dY, g5.b_mn = true;        // dY[T,F] as [K=T, N=F]: MN-major
+    g5.M = h, g5.N = F, g5.K = T, g5.kshard = T;
+    g5.out0 = dA;
+    g5.group_m = pick_group(g5);
+    e = gemm(s, "bwd_dA", tpmlp::EPI_STORE, g5, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    // dX = sum_i dY_i A_i^T, shard partials folded in order (the backward all-reduce)
+    GemmArgs g6 = base_args(status);
+    g6.a = dY, g6.a_mn = false;        // dY[T,F]: K-major
+    g6.b = saved->A, g6.b_mn = false;  // A[h,F] as [N=h, K=F]: K-major
+    g6.M = T, g6.N = h, g6.K = F;
+    g6.nshards = s->t, g6.kshard = F / s->t;
+    g6.out0 = dX;
+    g6.group_m = pick_group(g6);
+    e = gemm(s, "bwd_dX_shard_fold", tpmlp::EPI_FOLD, g6, sms, st);
+    return from_cuda(e);
+}
+
+tpmlp_status tpmlp_check_device_status(void *workspace, void *stream) {
+    if (!workspace) return TPMLP_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t words[2] = {0, 0};
+    cudaError_t e = cudaMemcpyAsync(words, workspace, sizeof(words), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return TPMLP_ERR_CUDA;
+    if (words[0] != 0) {
+        e = cudaMemsetAsync(workspace, 0, sizeof(words), st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return TPMLP_ERR_CUDA;
+    }
+    if (words[0] > TPMLP_ERR_DEVICE) return TPMLP_ERR_DEVICE;
+    return static_cast<tpmlp_status>(words[0]);
+}
+
+void tpmlp_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns == 0 ? 1 : ns); }
+
+tpmlp_status tpmlp_debug_timeout_probe(void *workspace, uint64_t wait_ns, void *stream) {
+    if (!workspace) return TPMLP_ERR_INVALID_ARG;
+    if (wait_ns > 10000000000ull) return TPMLP_ERR_INVALID_ARG;  // at most 10 s
+    const int sms = num_sms_current();
+    if (sms == 0) return TPMLP_ERR_CUDA;
+    if (sms < 0) return TPMLP_ERR_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Timed timed("timeout_probe", st);
+    cudaError_t e = tpmlp::launch_timeout_probe(static_cast<uint32_t *>(workspace), wait_ns, st);
+    if (e == cudaSuccess) g_launches.fetch_add(1);
+    return from_cuda(e);
+}
+
+uint64_t tpmlp_launch_count(void) { return g_launches.load(); }
+
+void tpmlp_profile_enable(int on) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_on = on != 0;
+}
+
+void tpmlp_profile_reset(void) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    for (auto &p : g_pending) {
+        g_event_pool.push_back(p.e0);
+        g_event_pool.push_back(p.e1);
+    }
+    g_pending.clear();
+    g_totals.clear();
+}
+
+tpmlp_status tpmlp_profile_collect(void) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    tpmlp_status rc = TPMLP_OK;
+    for (auto &p : g_pending) {
+        float ms = 0.0f;
+        if (cudaEventSynchronize(p.e1) != cudaSuccess || cudaEventElapsedTime(&ms, p.e0, p.e1) != cudaSuccess) {
+            rc = TPMLP_ERR_CUDA;
+        } else {
+            bool found = false;
+            for (auto &t : g_totals)
+                if (t.first == p.name) {
+                    t.second.launches += 1;
+                    t.second.ms += ms;
+                    found = true;
+                    break;
+                }
+            if (!found) {
+                TimingTotal tt;
+                tt.launches = 1;
+                tt.ms = ms;
+                g_totals.emplace_back(p.name, tt);
+            }
+        }
+        g_event_pool.push_back(p.e0);
+        g_event_pool.push_back(p.e1);
+    }
+    g_pending.clear();
+    return rc;
+}
+
+int tpmlp_profile_count(void) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    return static_cast<int>(g_totals.size());
+}
+
+int tpmlp_profile_entry(int i, char *name, int name_len, int64_t *launches, double *total_ms) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (i < 0 || i >= static_cast<int>(g_totals.size())) return -1;
+    const auto &t = g_totals[static_cast<size_t>(i)];
+    if (name && name_len > 0) {
+        std::strncpy(name, t.first.c_str(), static_cast<size_t>(name_len - 1));
+        name[name_len - 1] = '\0';
+    }
+    if (launches) *launches = t.second.launches;
+    if (total_ms) *total_ms = t.second.ms;
+    return 0;
+}
+
+}  // extern "C"

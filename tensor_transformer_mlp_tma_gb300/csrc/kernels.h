@@ -1,0 +1,56 @@
+// Host-side launchers of the kernels behind the C ABI (internal to libtpmlp.so).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace tpmlp {
+
+// Epilogues of the GEMM kernels.  Each names the step of the MLP it finishes.
+enum Epi : int {
+    EPI_BIAS_GELU = 0,  // H = acc + a (optional store), Y = GeLU(H)        -- column-parallel GEMM
+    EPI_FOLD_BIAS = 1,  // Z = b + ((Z_1 + Z_2) + ...)                      -- row-parallel GEMM
+    EPI_DGELU = 2,      // dY = acc * GeLU'(H)                              -- dZ B^T
+    EPI_STORE = 3,      // out = acc                                       -- dB, dA
+    EPI_FOLD = 4,       // dX = ((P_1 + P_2) + ...)                        -- dY A^T
+};
+
+// One GEMM  out[M,N] = sum_k opA(m,k) opB(k,n)  over row-major operands.
+//   A operand: K-major ([M,K] row-major, a_mn = false) or MN-major ([K,M], a_mn = true)
+//   B operand: K-major ([N,K] row-major, b_mn = false) or MN-major ([K,N], b_mn = true)
+// The K range is split into `nshards` consecutive ranges of `kshard` elements;
+// each range is accumulated on its own and, for the FOLD epilogues, the range
+// partials are summed in ascending order.  For the other epilogues nshards = 1.
+struct GemmArgs {
+    const void *a;
+    bool a_mn;
+    const void *b;
+    bool b_mn;
+    int64_t M, N, K;
+    int nshards;
+    int64_t kshard;
+    void *out0;        // H / Z / dY / dB / dA / dX
+    void *out1;        // Y for EPI_BIAS_GELU
+    const void *aux;   // H for EPI_DGELU
+    const void *bias;  // a for EPI_BIAS_GELU, b for EPI_FOLD_BIAS
+    uint32_t *status;  // device status word
+    uint64_t wait_ns;
+    int group_m;       // raster: tiles walk `group_m` M-tiles fastest, then N
+};
+
+// Tensor-core path: bf16 operands, fp32 accumulation in TMEM (tcgen05).
+cudaError_t launch_tc_gemm(Epi epi, const GemmArgs &g, int num_sms, cudaStream_t st);
+
+// FFMA path: element type fp32 (is_bf16 = false) or bf16, fp32 accumulation.
+cudaError_t launch_simt_gemm(Epi epi, bool is_bf16, const GemmArgs &g, cudaStream_t st);
+
+// Deterministic column sums out[c] = sum_r x[r,c] in two launches (per-chunk fp32
+// partials into `partials`, then an in-order sum of the chunks).
+int64_t colsum_chunks(int64_t rows, int64_t cols);
+cudaError_t launch_colsum(bool is_bf16, const void *x, int64_t rows, int64_t cols, float *partials,
+                          void *out, cudaStream_t st, int *launches);
+
+// A kernel that waits on a barrier nothing arrives on and reports the timeout.
+cudaError_t launch_timeout_probe(uint32_t *status, uint64_t wait_ns, cudaStream_t st);
+
+}  // namespace tpmlp

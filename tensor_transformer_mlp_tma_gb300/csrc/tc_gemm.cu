@@ -1,0 +1,494 @@
+// Tensor-core GEMMs of the TP-MLP block on sm_103a: TMA -> shared memory ring ->
+// tcgen05.mma (one thread) -> fp32 accumulators in tensor memory -> epilogue
+// warps (tcgen05.ld) -> fused bias / GeLU / GeLU' / shard fold -> global memory.
+//
+// One persistent CTA per SM, 10 warps:
+//   warp 0      TMA producer (one elected lane): fills a 4-stage ring of
+//               128x64 A tiles and 256x64 B tiles, 128-byte swizzled.
+//   warp 1      MMA issuer (one elected lane) and owner of the 512 TMEM columns:
+//               two 128x256 fp32 accumulators, used alternately per
+//               "accumulation unit" (one K range of one output tile).
+//   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (its rows) and
+//               columns 128*((w-2)/4)..+127 of the accumulator.
+//
+// The all-reduce of the t shard partials ("Megatron-LM" report, section 4.1,
+// Z = sum_i Y_i B_i; section 4.2 for dX in the backward direction) becomes the
+// FOLD epilogues: each shard's K range is its own accumulation unit, so each
+// partial Z_i is a complete fp32 product in TMEM; the epilogue threads pull it
+// into registers and add it to their running sum in shard order
+// ((Z_1 + Z_2) + Z_3) + ..., releasing the TMEM buffer at once so the tensor
+// core starts the next shard in the other buffer without waiting.
+//
+// Every wait is bounded (mbar_wait); a wait that runs out records
+// TPMLP_ERR_TIMEOUT in the status word, raises a CTA-wide abort flag, and the CTA
+// drains its own copies and MMAs and frees its tensor memory before returning.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace tpmlp {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // 64 bf16 = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;
+constexpr int B_STAGE = BN * BK * 2;
+constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int NUM_THREADS = 320;
+constexpr int EPI_THREADS = 256;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int SMEM_DYN = STAGES * STAGE_BYTES + 1024;  // + slack to align to 1024
+constexpr int MN_BLOCK_BYTES = 64 * BK * 2;             // one 64(MN) x 64(K) TMA box
+
+constexpr uint32_t STATUS_TIMEOUT = 4;  // TPMLP_ERR_TIMEOUT
+
+struct Params {
+    int M, N;
+    int m_tiles, n_tiles, group_m;
+    int nshards, kb_per_shard;
+    void *out0;
+    void *out1;
+    const void *aux;
+    const void *bias;
+    uint32_t *status;
+    unsigned long long wait_ns;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, const Params &p, int &mb, int &nb) {
+    const int per_group = p.group_m * p.n_tiles;
+    const int g = tile / per_group;
+    const int first_m = g * p.group_m;
+    const int gsize = min(p.m_tiles - first_m, p.group_m);
+    const int local = tile - g * per_group;
+    mb = first_m + local % gsize;
+    nb = local / gsize;
+}
+
+// Records a timeout once in the status word (detail = which role gave up).
+__device__ __forceinline__ void record_timeout(const Params &p, volatile int *abort_flag,
+                                               uint32_t role) {
+    *abort_flag = 1;
+    if (p.status) {
+        if (atomicCAS(p.status, 0u, STATUS_TIMEOUT) == 0u) atomicExch(p.status + 1, role);
+    }
+}
+
+__device__ __forceinline__ float gelu_f(float x) {
+    const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
+    return 0.5f * x * (1.0f + ptx::tanh_approx(u));
+}
+
+__device__ __forceinline__ float gelu_prime_f(float x) {
+    const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
+    const float th = ptx::tanh_approx(u);
+    const float du = 0.7978845608028654f * (1.0f + 3.0f * 0.044715f * x * x);
+    return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * du;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void unpack_bf16(uint32_t u, float &lo, float &hi) {
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&u);
+    lo = __low2float(v);
+    hi = __high2float(v);
+}
+
+// Stores 8 consecutive fp32 values as bf16 at out[off .. off+7] (16 bytes).
+__device__ __forceinline__ void store8(void *out, int64_t off, const float *v) {
+    uint4 w;
+    w.x = pack_bf16(v[0], v[1]);
+    w.y = pack_bf16(v[2], v[3]);
+    w.z = pack_bf16(v[4], v[5]);
+    w.w = pack_bf16(v[6], v[7]);
+    *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(out) + off) = w;
+}
+
+__device__ __forceinline__ void load8(const void *in, int64_t off, float *v) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(in) + off));
+    unpack_bf16(w.x, v[0], v[1]);
+    unpack_bf16(w.y, v[2], v[3]);
+    unpack_bf16(w.z, v[4], v[5]);
+    unpack_bf16(w.w, v[6], v[7]);
+}
+
+// Epilogue of one group of 8 columns for the non-fold kinds.
+template <int EPI>
+__device__ __forceinline__ void epi8(const Params &p, int64_t row, int col, float *acc) {
+    const int64_t off = row * p.N + col;
+    if constexpr (EPI == EPI_BIAS_GELU) {
+        float bias[8];
+        load8(p.bias, col, bias);
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            acc[i] += bias[i];
+            y[i] = gelu_f(acc[i]);
+        }
+        if (p.out0) store8(p.out0, off, acc);
+        store8(p.out1, off, y);
+    } else if constexpr (EPI == EPI_DGELU) {
+        float hv[8];
+        load8(p.aux, off, hv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] *= gelu_prime_f(hv[i]);
+        store8(p.out0, off, acc);
+    } else if constexpr (EPI == EPI_FOLD_BIAS) {
+        float bias[8];
+        load8(p.bias, col, bias);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += bias[i];
+        store8(p.out0, off, acc);
+    } else {  // EPI_STORE, EPI_FOLD
+        store8(p.out0, off, acc);
+    }
+}
+
+template <int EPI, bool A_MN, bool B_MN>
+__global__ void __maxnreg__(200)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const Params p) {
+    constexpr bool FOLD = (EPI == EPI_FOLD_BIAS || EPI == EPI_FOLD);
+    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_full[STAGES];
+    __shared__ __align__(8) uint64_t bar_empty[STAGES];
+    __shared__ __align__(8) uint64_t bar_tfull[2];
+    __shared__ __align__(8) uint64_t bar_tempty[2];
+    __shared__ __align__(8) uint64_t bar_done;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile int abort_sh;
+
+    const uint32_t smem_base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&bar_full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bar_empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(ptx::smem_u32(&bar_tfull[b]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bar_tempty[b]), EPI_THREADS);
+        }
+        ptx::mbar_init(ptx::smem_u32(&bar_done), 1);
+        abort_sh = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = tmem_base_sh;
+
+    const int num_tiles = p.m_tiles * p.n_tiles;
+    const int kb_total = p.nshards * p.kb_per_shard;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords(tile, p, mb, nb);
+                const int m0 = mb * BM, n0 = nb * BN;
+                for (int kb = 0; kb < kb_total; ++kb) {
+                    if (!ptx::mbar_wait(ptx::smem_u32(&bar_empty[stage]), phase ^ 1u, p.wait_ns,
+                                        &abort_sh)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full = ptx::smem_u32(&bar_full[stage]);
+                    const uint32_t sa = smem_base + stage * STAGE_BYTES;
+                    const uint32_t sb = sa + A_STAGE;
+                    const int k0 = kb * BK;
+                    ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
+                    if constexpr (!A_MN) {
+                        ptx::tma_load_2d(sa, &tmA, full, k0, m0);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BM / 64; ++j)
+                            ptx::tma_load_2d(sa + j * MN_BLOCK_BYTES, &tmA, full, m0 + 64 * j, k0);
+                    }
+                    if constexpr (!B_MN) {
+                        ptx::tma_load_2d(sb, &tmB, full, k0, n0);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j)
+                            ptx::tma_load_2d(sb + j * MN_BLOCK_BYTES, &tmB, full, n0 + 64 * j, k0);
+                    }
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) record_timeout(p, &abort_sh, 1);
+            // Let every copy this thread started land before the CTA can exit.
+            const int64_t tail = issued < STAGES ? issued : STAGES;
+            for (int64_t i = issued - tail; i < issued; ++i) {
+                const int s = static_cast<int>(i % STAGES);
+                const uint32_t ph = static_cast<uint32_t>((i / STAGES) & 1);
+                if (!ptx::mbar_wait(ptx::smem_u32(&bar_full[s]), ph, p.wait_ns, nullptr))
+                    record_timeout(p, &abort_sh, 2);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t unit = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                for (int s = 0; s < p.nshards && ok; ++s, ++unit) {
+                    const uint32_t buf = unit & 1u, use = unit >> 1;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&bar_tempty[buf]), (use & 1u) ^ 1u, p.wait_ns,
+                                        &abort_sh)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    for (int kb = 0; kb < p.kb_per_shard; ++kb) {
+                        if (!ptx::mbar_wait(ptx::smem_u32(&bar_full[stage]), phase, p.wait_ns,
+                                            &abort_sh)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint32_t sa = smem_base + stage * STAGE_BYTES;
+                        const uint32_t sb = sa + A_STAGE;
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            const uint64_t ad = A_MN ? ptx::sdesc_sw128(sa + k * 2048, MN_BLOCK_BYTES, 1024)
+                                                     : ptx::sdesc_sw128(sa + k * 32, 16, 1024);
+                            const uint64_t bd = B_MN ? ptx::sdesc_sw128(sb + k * 2048, MN_BLOCK_BYTES, 1024)
+                                                     : ptx::sdesc_sw128(sb + k * 32, 16, 1024);
+                            ptx::umma_f16_ss(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                        }
+                        ptx::umma_commit(ptx::smem_u32(&bar_empty[stage]));
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    ptx::umma_commit(ptx::smem_u32(&bar_tfull[buf]));
+                }
+            }
+            if (!ok) record_timeout(p, &abort_sh, 3);
+            // Retire every MMA this thread issued before TMEM can be freed.
+            ptx::umma_commit(ptx::smem_u32(&bar_done));
+            if (!ptx::mbar_wait(ptx::smem_u32(&bar_done), 0, p.wait_ns, nullptr))
+                record_timeout(p, &abort_sh, 4);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - 2;                         // 0..7
+        const int quarter = warp & 3;                    // TMEM lanes this warp may read
+        const int half = ew >> 2;                        // column half of the 256-wide tile
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        uint32_t unit = 0;
+        bool ok = true;
+        float sum[FOLD ? 128 : 1];
+        (void)sum;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, p, mb, nb);
+            const int64_t row = static_cast<int64_t>(mb) * BM + quarter * 32 + lane;
+            const int col0 = nb * BN + half * 128;
+            const bool row_ok = row < p.M;
+            for (int s = 0; s < p.nshards; ++s, ++unit) {
+                const uint32_t buf = unit & 1u, use = unit >> 1;
+                bool got = ptx::mbar_wait(ptx::smem_u32(&bar_tfull[buf]), use & 1u, p.wait_ns, &abort_sh);
+                got = __all_sync(0xffffffffu, got);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t taddr = tmem_base + lane_off + buf * BN + half * 128;
+                if constexpr (FOLD) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+                        ptx::tmem_ld_wait(r);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float v = __uint_as_float(r[i]);
+                            sum[c * 32 + i] = (s == 0) ? v : sum[c * 32 + i] + v;
+                        }
+                    }
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(ptx::smem_u32(&bar_tempty[buf]));
+                    if (s == p.nshards - 1 && row_ok) {
+#pragma unroll
+                        for (int g = 0; g < 16; ++g) {
+                            const int col = col0 + g * 8;
+                            float v[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) v[i] = sum[g * 8 + i];
+                            if (col < p.N) epi8<EPI>(p, row, col, v);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+                        ptx::tmem_ld_wait(r);
+                        if (row_ok) {
+#pragma unroll
+                            for (int g = 0; g < 4; ++g) {
+                                const int col = col0 + c * 32 + g * 8;
+                                float v[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[g * 8 + i]);
+                                if (col < p.N) epi8<EPI>(p, row, col, v);
+                            }
+                        }
+                    }
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(ptx::smem_u32(&bar_tempty[buf]));
+                }
+            }
+        }
+        if (!ok) record_timeout(p, &abort_sh, 5);
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] with a box of box_cols (inner) x box_rows.
+static bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, uint32_t box_cols,
+                     uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int EPI, bool A_MN, bool B_MN>
+static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
+    auto kern = gemm_kernel<EPI, A_MN, B_MN>;
+    // The shared-memory opt-in is a per-device function attribute: set it once per device.
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!attr_set[dev]) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN);
+            if (e != cudaSuccess) return e;
+            attr_set[dev] = true;
+        }
+    }
+
+    CUtensorMap ma, mb;
+    // A operand: K-major [M,K] with a 64 x 128 box, or MN-major [K,M] with 64 x 64 boxes.
+    const bool oka = A_MN ? make_map(&ma, g.a, g.K, g.M, 64, BK) : make_map(&ma, g.a, g.M, g.K, BK, BM);
+    const bool okb = B_MN ? make_map(&mb, g.b, g.K, g.N, 64, BK) : make_map(&mb, g.b, g.N, g.K, BK, BN);
+    if (!oka || !okb) return cudaErrorInvalidValue;
+
+    Params p;
+    p.M = static_cast<int>(g.M);
+    p.N = static_cast<int>(g.N);
+    p.m_tiles = static_cast<int>((g.M + BM - 1) / BM);
+    p.n_tiles = static_cast<int>((g.N + BN - 1) / BN);
+    p.group_m = g.group_m < 1 ? 1 : (g.group_m > p.m_tiles ? p.m_tiles : g.group_m);
+    p.nshards = g.nshards;
+    p.kb_per_shard = static_cast<int>((g.kshard + BK - 1) / BK);
+    p.out0 = g.out0;
+    p.out1 = g.out1;
+    p.aux = g.aux;
+    p.bias = g.bias;
+    p.status = g.status;
+    p.wait_ns = g.wait_ns;
+    const int tiles = p.m_tiles * p.n_tiles;
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    kern<<<grid, NUM_THREADS, SMEM_DYN, st>>>(ma, mb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace tc
+
+cudaError_t launch_tc_gemm(Epi epi, const GemmArgs &g, int num_sms, cudaStream_t st) {
+    using namespace tc;
+    if (g.M <= 0 || g.N <= 0 || g.K <= 0) return cudaSuccess;
+    switch (epi) {
+        case EPI_BIAS_GELU:  // X[T,h] (K-major) . A[h,F] (MN-major)
+            if (!g.a_mn && g.b_mn) return launch_t<EPI_BIAS_GELU, false, true>(g, num_sms, st);
+            break;
+        case EPI_FOLD_BIAS:  // Y[T,F] (K-major) . B[F,h] (MN-major)
+            if (!g.a_mn && g.b_mn) return launch_t<EPI_FOLD_BIAS, false, true>(g, num_sms, st);
+            break;
+        case EPI_DGELU:  // dZ[T,h] (K-major) . B[F,h]^T (K-major)
+            if (!g.a_mn && !g.b_mn) return launch_t<EPI_DGELU, false, false>(g, num_sms, st);
+            break;
+        case EPI_STORE:  // Y^T . dZ and X^T . dY: both operands MN-major
+            if (g.a_mn && g.b_mn) return launch_t<EPI_STORE, true, true>(g, num_sms, st);
+            break;
+        case EPI_FOLD:  // dY[T,F] (K-major) . A[h,F]^T (K-major)
+            if (!g.a_mn && !g.b_mn) return launch_t<EPI_FOLD, false, false>(g, num_sms, st);
+            break;
+    }
+    return cudaErrorNotSupported;
+}
+
+}  // namespace tpmlp

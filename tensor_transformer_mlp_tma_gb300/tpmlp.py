@@ -1,0 +1,233 @@
+"""ctypes binding of libtpmlp.so (C ABI in include/tpmlp.h): argument marshalling
+only.  Every step of the forward and backward pass runs in the library's CUDA
+kernels; PyTorch supplies device memory and the current stream.
+
+Importing this module loads the compiled library and raises if it is missing:
+there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtpmlp.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(6)
+F32, BF16 = 0, 1
+ALGO_DEFAULT, ALGO_SIMT = 0, 1
+WS_STATUS, WS_PARTIALS, WS_DY = 0, 1, 2
+
+_DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("tokens", ctypes.c_int64), ("hidden", ctypes.c_int64), ("ffn", ctypes.c_int64),
+                ("t", ctypes.c_int32), ("dtype", ctypes.c_int32), ("algo", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class Saved(ctypes.Structure):
+    _fields_ = [("X", ctypes.c_void_p), ("A", ctypes.c_void_p), ("B", ctypes.c_void_p),
+                ("H", ctypes.c_void_p), ("Y", ctypes.c_void_p)]
+
+
+class TpmlpError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libtpmlp.so is not built (expected at %s); run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, sz, i32, i64, u64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64
+    SP = ctypes.POINTER(Shape)
+    decl = {
+        "tpmlp_status_string": (ctypes.c_char_p, [i32]),
+        "tpmlp_version": (i32, []),
+        "tpmlp_saved_bytes": (sz, [SP]),
+        "tpmlp_workspace_bytes": (sz, [SP]),
+        "tpmlp_workspace_offset": (sz, [SP, i32]),
+        "tpmlp_forward": (i32, [SP, vp, vp, vp, vp, vp, vp, ctypes.POINTER(Saved), vp, vp]),
+        "tpmlp_backward": (i32, [SP, vp, ctypes.POINTER(Saved), vp, vp, vp, vp, vp, vp, vp]),
+        "tpmlp_check_device_status": (i32, [vp, vp]),
+        "tpmlp_set_wait_limit_ns": (None, [u64]),
+        "tpmlp_debug_timeout_probe": (i32, [vp, u64, vp]),
+        "tpmlp_launch_count": (u64, []),
+        "tpmlp_profile_enable": (None, [i32]),
+        "tpmlp_profile_reset": (None, []),
+        "tpmlp_profile_collect": (i32, []),
+        "tpmlp_profile_count": (i32, []),
+        "tpmlp_profile_entry": (i32, [i32, ctypes.c_char_p, i32, ctypes.POINTER(i64),
+                                      ctypes.POINTER(ctypes.c_double)]),
+    }
+    for name, (res, args) in decl.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.tpmlp_status_string(int(status)).decode()
+
+
+def make_shape(tokens: int, hidden: int, ffn: int, t: int, dtype, algo: int = ALGO_DEFAULT) -> Shape:
+    if isinstance(dtype, torch.dtype):
+        dtype = _DTYPES[dtype]
+    return Shape(int(tokens), int(hidden), int(ffn), int(t), int(dtype), int(algo), 0)
+
+
+def saved_bytes(shape: Shape) -> int:
+    return int(lib.tpmlp_saved_bytes(ctypes.byref(shape)))
+
+
+def workspace_bytes(shape: Shape) -> int:
+    return int(lib.tpmlp_workspace_bytes(ctypes.byref(shape)))
+
+
+def workspace_offset(shape: Shape, region: int) -> int:
+    return int(lib.tpmlp_workspace_offset(ctypes.byref(shape), int(region)))
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise TpmlpError(status, what)
+
+
+def _need(x, name, dtype, shape):
+    if not (x.is_cuda and x.is_contiguous()):
+        raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    if x.dtype != dtype:
+        raise ValueError("%s has dtype %s, expected %s" % (name, x.dtype, dtype))
+    if tuple(x.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(x.shape), tuple(shape)))
+
+
+def new_workspace(shape: Shape, device=None) -> torch.Tensor:
+    """A zeroed workspace of the size the library asks for (uint8, 256-byte aligned)."""
+    n = workspace_bytes(shape)
+    if n == 0:
+        raise ValueError("invalid shape")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+class Context:
+    """The buffers one layer needs between forward and backward: H, Y and the
+    workspace, plus the ctypes shape and saved-activation records."""
+
+    def __init__(self, tokens, hidden, ffn, t, dtype, algo=ALGO_DEFAULT, device=None, keep_H=True):
+        self.shape = make_shape(tokens, hidden, ffn, t, dtype, algo)
+        if saved_bytes(self.shape) == 0 and tokens > 0:
+            raise ValueError("invalid shape (tokens=%d hidden=%d ffn=%d t=%d)" % (tokens, hidden, ffn, t))
+        self.dtype = dtype
+        dev = device or "cuda"
+        self.H = torch.empty((tokens, ffn), dtype=dtype, device=dev) if keep_H else None
+        self.Y = torch.empty((tokens, ffn), dtype=dtype, device=dev)
+        self.workspace = new_workspace(self.shape, dev)
+        self.saved = Saved(None, None, None, _ptr(self.H), _ptr(self.Y))
+        self._keep = []
+
+    @property
+    def dY(self) -> torch.Tensor:
+        """The dY intermediate of the last backward (a view into the workspace)."""
+        T, F = self.shape.tokens, self.shape.ffn
+        off = workspace_offset(self.shape, WS_DY)
+        esz = 2 if self.dtype == torch.bfloat16 else 4
+        return self.workspace[off:off + T * F * esz].view(self.dtype).view(T, F)
+
+
+def forward(ctx: Context, X, A, a, B, b, Z=None, stream=None):
+    """Z = GeLU(X A + a) B + b with the t-shard fold; fills ctx.H, ctx.Y."""
+    s = ctx.shape
+    T, h, F = s.tokens, s.hidden, s.ffn
+    for x, n, shp in ((X, "X", (T, h)), (A, "A", (h, F)), (a, "a", (F,)), (B, "B", (F, h)), (b, "b", (h,))):
+        _need(x, n, ctx.dtype, shp)
+    if Z is None:
+        Z = torch.empty((T, h), dtype=ctx.dtype, device=X.device)
+    _need(Z, "Z", ctx.dtype, (T, h))
+    ctx._keep = [X, A, B]
+    st = lib.tpmlp_forward(ctypes.byref(s), _ptr(X), _ptr(A), _ptr(a), _ptr(B), _ptr(b), _ptr(Z),
+                           ctypes.byref(ctx.saved), _ptr(ctx.workspace), _stream(stream))
+    _check(st, "tpmlp_forward")
+    return Z
+
+
+def backward(ctx: Context, dZ, dX=None, dA=None, da=None, dB=None, db=None, stream=None):
+    """dX, dA, da, dB, db for L = sum(dZ * Z), using what forward saved in ctx."""
+    s = ctx.shape
+    T, h, F = s.tokens, s.hidden, s.ffn
+    dev = dZ.device
+    _need(dZ, "dZ", ctx.dtype, (T, h))
+    out = {}
+    for name, val, shp in (("dX", dX, (T, h)), ("dA", dA, (h, F)), ("da", da, (F,)),
+                           ("dB", dB, (F, h)), ("db", db, (h,))):
+        if val is None:
+            val = torch.empty(shp, dtype=ctx.dtype, device=dev)
+        _need(val, name, ctx.dtype, shp)
+        out[name] = val
+    st = lib.tpmlp_backward(ctypes.byref(s), _ptr(dZ), ctypes.byref(ctx.saved), _ptr(out["dX"]),
+                            _ptr(out["dA"]), _ptr(out["da"]), _ptr(out["dB"]), _ptr(out["db"]),
+                            _ptr(ctx.workspace), _stream(stream))
+    _check(st, "tpmlp_backward")
+    return out
+
+
+def check_device_status(ctx_or_ws, stream=None) -> int:
+    ws = ctx_or_ws.workspace if isinstance(ctx_or_ws, Context) else ctx_or_ws
+    return int(lib.tpmlp_check_device_status(_ptr(ws), _stream(stream)))
+
+
+def set_wait_limit_ns(ns: int):
+    lib.tpmlp_set_wait_limit_ns(int(ns))
+
+
+def debug_timeout_probe(workspace, wait_ns: int, stream=None) -> int:
+    return int(lib.tpmlp_debug_timeout_probe(_ptr(workspace), int(wait_ns), _stream(stream)))
+
+
+def launch_count() -> int:
+    return int(lib.tpmlp_launch_count())
+
+
+def profile_enable(on: bool = True):
+    lib.tpmlp_profile_enable(1 if on else 0)
+
+
+def profile_reset():
+    lib.tpmlp_profile_reset()
+
+
+def profile_collect() -> dict:
+    """{kernel name: (launches, total ms)} of the launches timed since the reset."""
+    _check(lib.tpmlp_profile_collect(), "tpmlp_profile_collect")
+    out = {}
+    buf = ctypes.create_string_buffer(128)
+    for i in range(lib.tpmlp_profile_count()):
+        n = ctypes.c_int64()
+        ms = ctypes.c_double()
+        if lib.tpmlp_profile_entry(i, buf, 128, ctypes.byref(n), ctypes.byref(ms)) == 0:
+            out[buf.value.decode()] = (int(n.value), float(ms.value))
+    return out

@@ -1,0 +1,141 @@
+"""The C ABI without a GPU: the library builds, loads and exports every symbol
+include/tpmlp.h declares; size queries and host-side validation return the
+documented values.  Only argument checks that fail before any CUDA call are
+exercised here (no pointer is ever dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def tp():
+    from tensor_transformer_mlp_tma_gb300 import build
+    build.build()
+    from tensor_transformer_mlp_tma_gb300 import tpmlp
+    return tpmlp
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "tpmlp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tpmlp_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("tpmlp_forward", "tpmlp_backward", "tpmlp_saved_bytes", "tpmlp_workspace_bytes",
+              "tpmlp_check_device_status", "tpmlp_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(tp):
+    lib = ctypes.CDLL(tp.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(tp):
+    for s in range(6):
+        assert tp.status_string(s)
+    assert tp.status_string(0) == "ok"
+    assert tp.status_string(99) == "unknown status"
+
+
+def test_size_queries(tp):
+    s = tp.make_shape(4096, 8192, 32768, 8, tp.BF16)
+    assert tp.saved_bytes(s) == 2 * 4096 * 32768 * 2
+    ws = tp.workspace_bytes(s)
+    off = tp.workspace_offset(s, tp.WS_DY)
+    assert off % 1024 == 0 and off >= 1024
+    assert ws >= off + 4096 * 32768 * 2
+    assert tp.workspace_offset(s, tp.WS_STATUS) == 0
+    assert tp.workspace_offset(s, 7) == ctypes.c_size_t(-1).value
+    f32 = tp.make_shape(128, 256, 1024, 2, tp.F32)
+    assert tp.saved_bytes(f32) == 2 * 128 * 1024 * 4
+    # invalid shapes: 0
+    for bad in (tp.make_shape(128, 256, 1000, 3, tp.BF16),   # F % t != 0
+                tp.make_shape(128, 0, 1024, 2, tp.BF16),     # h = 0
+                tp.make_shape(-1, 256, 1024, 2, tp.BF16),    # T < 0
+                tp.make_shape(128, 256, 1024, 17, tp.BF16),  # t > 16
+                tp.make_shape(128, 256, 1024, 0, tp.BF16),   # t < 1
+                tp.Shape(128, 256, 1024, 2, 7, 0, 0),        # dtype
+                tp.Shape(128, 256, 1024, 2, 1, 5, 0),        # algo
+                tp.Shape(128, 256, 1024, 2, 1, 0, 1)):       # reserved
+        assert tp.saved_bytes(bad) == 0
+        assert tp.workspace_bytes(bad) == 0
+    # an empty batch is valid
+    assert tp.workspace_bytes(tp.make_shape(0, 256, 1024, 2, tp.BF16)) > 0
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def _fwd(tp, shape, ptrs=None, saved=None, ws=FAKE):
+    p = ptrs or [FAKE] * 6
+    sv = saved if saved is not None else tp.Saved(None, None, None, FAKE, FAKE)
+    return tp.lib.tpmlp_forward(ctypes.byref(shape) if shape is not None else None, *p,
+                                ctypes.byref(sv), ws, None)
+
+
+def _bwd(tp, shape, ptrs=None, saved=None, ws=FAKE):
+    p = ptrs or [FAKE] * 6
+    sv = saved if saved is not None else tp.Saved(FAKE, FAKE, FAKE, FAKE, FAKE)
+    return tp.lib.tpmlp_backward(ctypes.byref(shape), p[0], ctypes.byref(sv), *p[1:], ws, None)
+
+
+def test_forward_invalid_arguments(tp):
+    good = tp.make_shape(256, 256, 1024, 2, tp.BF16)
+    assert _fwd(tp, None) == tp.ERR_INVALID_ARG
+    assert _fwd(tp, tp.make_shape(256, 256, 1000, 3, tp.BF16)) == tp.ERR_INVALID_ARG
+    assert _fwd(tp, tp.make_shape(256, 256, 1024, 17, tp.BF16)) == tp.ERR_INVALID_ARG
+    for i in range(6):  # each required pointer NULL in turn
+        p = [FAKE] * 6
+        p[i] = None
+        assert _fwd(tp, good, ptrs=p) == tp.ERR_INVALID_ARG
+    assert _fwd(tp, good, saved=tp.Saved(None, None, None, FAKE, None)) == tp.ERR_INVALID_ARG
+    assert _fwd(tp, good, ws=None) == tp.ERR_INVALID_ARG
+
+
+def test_forward_unsupported(tp):
+    good = tp.make_shape(256, 256, 1024, 2, tp.BF16)
+    p = [FAKE] * 6
+    p[1] = FAKE + 2  # bf16-aligned but not 16-byte aligned: TMA cannot take it
+    assert _fwd(tp, good, ptrs=p) == tp.ERR_UNSUPPORTED
+    p = [FAKE] * 6
+    p[0] = FAKE + 1  # not even element-aligned
+    assert _fwd(tp, good, ptrs=p) == tp.ERR_UNSUPPORTED
+    # shard size F/t = 96 is not a multiple of the 64-wide k-block
+    assert _fwd(tp, tp.make_shape(256, 256, 192, 2, tp.BF16)) == tp.ERR_UNSUPPORTED
+    # hidden size whose row pitch is not 16-byte aligned
+    assert _fwd(tp, tp.make_shape(256, 260, 1024, 2, tp.BF16)) == tp.ERR_UNSUPPORTED
+    # optional H misaligned
+    assert _fwd(tp, good, saved=tp.Saved(None, None, None, FAKE + 2, FAKE)) == tp.ERR_UNSUPPORTED
+    assert _fwd(tp, good, ws=FAKE + 8) == tp.ERR_UNSUPPORTED
+
+
+def test_backward_invalid_arguments(tp):
+    good = tp.make_shape(256, 256, 1024, 2, tp.BF16)
+    for i in range(6):
+        p = [FAKE] * 6
+        p[i] = None
+        assert _bwd(tp, good, ptrs=p) == tp.ERR_INVALID_ARG
+    for field in ("X", "A", "B", "H", "Y"):
+        sv = tp.Saved(FAKE, FAKE, FAKE, FAKE, FAKE)
+        setattr(sv, field, None)
+        assert _bwd(tp, good, saved=sv) == tp.ERR_INVALID_ARG
+    assert _bwd(tp, tp.make_shape(256, 256, 192, 2, tp.BF16)) == tp.ERR_UNSUPPORTED
+
+
+def test_debug_probe_rejects_bad_arguments(tp):
+    assert tp.lib.tpmlp_debug_timeout_probe(None, 1000, None) == tp.ERR_INVALID_ARG
+    assert tp.lib.tpmlp_debug_timeout_probe(FAKE, 20_000_000_000, None) == tp.ERR_INVALID_ARG
+
+
+def test_profile_table_starts_empty(tp):
+    tp.profile_reset()
+    assert tp.lib.tpmlp_profile_count() == 0
+    assert tp.lib.tpmlp_profile_entry(0, None, 0, None, None) == -1
