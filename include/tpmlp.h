@@ -100,6 +100,10 @@ const char *tpmlp_status_string(tpmlp_status s);
 /* Library version, major*10000 + minor*100 + patch. */
 int tpmlp_version(void);
 
+/* Description of the most recent failure of a call made from this host thread
+ * (empty after a call that succeeded from the start).  Static, per-thread storage. */
+const char *tpmlp_last_error(void);
+
 /* Bytes the caller must allocate for H and Y together (2*T*F elements); 0 when
  * the shape is invalid. */
 size_t tpmlp_saved_bytes(const tpmlp_shape *shape);

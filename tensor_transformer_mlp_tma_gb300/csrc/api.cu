@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdarg>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -14,6 +15,19 @@
 
 #include "kernels.h"
 #include "tpmlp.h"
+
+namespace tpmlp {
+
+thread_local char g_last_error[512] = "";
+
+void set_last_error(const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+}
+
+}  // namespace tpmlp
 
 namespace {
 
@@ -146,7 +160,16 @@ tpmlp_status check_ptrs(const tpmlp_shape *s, std::initializer_list<const void *
     return TPMLP_OK;
 }
 
-tpmlp_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TPMLP_OK : TPMLP_ERR_CUDA; }
+tpmlp_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return TPMLP_OK;
+    if (tpmlp::g_last_error[0] == '\0') tpmlp::set_last_error("%s", cudaGetErrorString(e));
+    return TPMLP_ERR_CUDA;
+}
+
+tpmlp_status invalid(const char *why) {
+    tpmlp::set_last_error("%s", why);
+    return TPMLP_ERR_INVALID_ARG;
+}
 
 // One GEMM launch on the selected path.
 cudaError_t gemm(const tpmlp_shape *s, const char *name, Epi epi, const GemmArgs &g, int sms,
@@ -206,6 +229,8 @@ const char *tpmlp_status_string(tpmlp_status s) {
 
 int tpmlp_version(void) { return 100; }
 
+const char *tpmlp_last_error(void) { return tpmlp::g_last_error; }
+
 size_t tpmlp_saved_bytes(const tpmlp_shape *s) {
     if (!shape_valid(s)) return 0;
     return 2 * static_cast<size_t>(s->tokens) * static_cast<size_t>(s->ffn) * elt(s);
@@ -229,9 +254,13 @@ size_t tpmlp_workspace_offset(const tpmlp_shape *s, int region) {
 tpmlp_status tpmlp_forward(const tpmlp_shape *s, const void *X, const void *A, const void *a,
                            const void *B, const void *b, void *Z, tpmlp_saved *saved,
                            void *workspace, void *stream) {
-    if (!shape_valid(s) || !saved || !workspace) return TPMLP_ERR_INVALID_ARG;
+    tpmlp::g_last_error[0] = '\0';
+    if (!shape_valid(s)) return invalid("tpmlp_forward: invalid shape");
+    if (!saved || !workspace) return invalid("tpmlp_forward: saved or workspace is NULL");
     if (!aligned16(workspace)) return TPMLP_ERR_UNSUPPORTED;
-    tpmlp_status rc = check_ptrs(s, {X, A, a, B, b, Z, saved->Y}, {saved->H});
+    // With no tokens the [T, .] tensors are empty and may have NULL data pointers.
+    tpmlp_status rc = s->tokens > 0 ? check_ptrs(s, {X, A, a, B, b, Z, saved->Y}, {saved->H})
+                                    : check_ptrs(s, {A, a, B, b}, {X, Z, saved->Y, saved->H});
     if (rc != TPMLP_OK) return rc;
     saved->X = X;
     saved->A = A;
@@ -268,10 +297,14 @@ tpmlp_status tpmlp_forward(const tpmlp_shape *s, const void *X, const void *A, c
 
 tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_saved *saved, void *dX,
                             void *dA, void *da, void *dB, void *db, void *workspace, void *stream) {
-    if (!shape_valid(s) || !saved || !workspace) return TPMLP_ERR_INVALID_ARG;
+    tpmlp::g_last_error[0] = '\0';
+    if (!shape_valid(s)) return invalid("tpmlp_backward: invalid shape");
+    if (!saved || !workspace) return invalid("tpmlp_backward: saved or workspace is NULL");
     if (!aligned16(workspace)) return TPMLP_ERR_UNSUPPORTED;
     tpmlp_status rc =
-        check_ptrs(s, {dZ, saved->X, saved->A, saved->B, saved->H, saved->Y, dX, dA, da, dB, db}, {});
+        s->tokens > 0
+            ? check_ptrs(s, {dZ, saved->X, saved->A, saved->B, saved->H, saved->Y, dX, dA, da, dB, db}, {})
+            : check_ptrs(s, {saved->A, saved->B, dA, da, dB, db}, {dZ, saved->X, saved->H, saved->Y, dX});
     if (rc != TPMLP_OK) return rc;
     const int64_t T = s->tokens, h = s->hidden, F = s->ffn;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -53,4 +53,8 @@ cudaError_t launch_colsum(bool is_bf16, const void *x, int64_t rows, int64_t col
 // A kernel that waits on a barrier nothing arrives on and reports the timeout.
 cudaError_t launch_timeout_probe(uint32_t *status, uint64_t wait_ns, cudaStream_t st);
 
+// Records a description of the last failure of this host thread (read back by
+// tpmlp_last_error()).
+void set_last_error(const char *fmt, ...);
+
 }  // namespace tpmlp

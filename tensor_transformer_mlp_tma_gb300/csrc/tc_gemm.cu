@@ -28,6 +28,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "kernels.h"
@@ -156,7 +157,7 @@ __device__ __forceinline__ void epi8(const Params &p, int64_t row, int col, floa
 }
 
 template <int EPI, bool A_MN, bool B_MN>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const Params p) {
     constexpr bool FOLD = (EPI == EPI_FOLD_BIAS || EPI == EPI_FOLD);
@@ -398,10 +399,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     std::call_once(once, [] {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e == cudaSuccess && q == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        else
+            set_last_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled): %s, query %d",
+                           cudaGetErrorString(e), static_cast<int>(q));
     });
     return fn;
 }
@@ -410,7 +414,10 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 static bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, uint32_t box_cols,
                      uint32_t box_rows) {
     auto fn = encode_fn();
-    if (!fn) return false;
+    if (!fn) {
+        set_last_error("cuTensorMapEncodeTiled is not available from the driver");
+        return false;
+    }
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
     cuuint32_t box[2] = {box_cols, box_rows};
@@ -418,6 +425,10 @@ static bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        set_last_error("cuTensorMapEncodeTiled failed (CUresult %d) for a [%lld, %lld] bf16 matrix, box %u x %u",
+                       static_cast<int>(r), static_cast<long long>(rows), static_cast<long long>(cols), box_cols,
+                       box_rows);
     return r == CUDA_SUCCESS;
 }
 
@@ -435,7 +446,11 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
         std::lock_guard<std::mutex> lk(mu);
         if (!attr_set[dev]) {
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN);
-            if (e != cudaSuccess) return e;
+            if (e != cudaSuccess) {
+                set_last_error("cudaFuncSetAttribute(%d bytes of shared memory): %s", SMEM_DYN,
+                               cudaGetErrorString(e));
+                return e;
+            }
             attr_set[dev] = true;
         }
     }
@@ -463,7 +478,17 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = tiles < num_sms ? tiles : num_sms;
     kern<<<grid, NUM_THREADS, SMEM_DYN, st>>>(ma, mb, p);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        cudaFuncAttributes fa;
+        std::memset(&fa, 0, sizeof(fa));
+        cudaFuncGetAttributes(&fa, kern);
+        set_last_error("tensor-core GEMM launch (grid %d, %d threads, %d bytes shared): %s "
+                       "[kernel: %d regs, max %d threads, %zu static + max %d dynamic shared bytes]",
+                       grid, NUM_THREADS, SMEM_DYN, cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock,
+                       fa.sharedSizeBytes, fa.maxDynamicSharedSizeBytes);
+    }
+    return e;
 }
 
 }  // namespace tc

@@ -37,7 +37,9 @@ class Saved(ctypes.Structure):
 class TpmlpError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__("%s: %s (status %d)" % (what, status_string(status), status))
+        detail = last_error()
+        super().__init__("%s: %s (status %d)%s" % (what, status_string(status), status,
+                                                    (": " + detail) if detail else ""))
 
 
 def _load():
@@ -50,6 +52,7 @@ def _load():
     decl = {
         "tpmlp_status_string": (ctypes.c_char_p, [i32]),
         "tpmlp_version": (i32, []),
+        "tpmlp_last_error": (ctypes.c_char_p, []),
         "tpmlp_saved_bytes": (sz, [SP]),
         "tpmlp_workspace_bytes": (sz, [SP]),
         "tpmlp_workspace_offset": (sz, [SP, i32]),
@@ -78,6 +81,10 @@ lib = _load()
 
 def status_string(status: int) -> str:
     return lib.tpmlp_status_string(int(status)).decode()
+
+
+def last_error() -> str:
+    return lib.tpmlp_last_error().decode(errors="replace")
 
 
 def make_shape(tokens: int, hidden: int, ffn: int, t: int, dtype, algo: int = ALGO_DEFAULT) -> Shape:
