@@ -161,6 +161,34 @@ void tpmlp_set_wait_limit_ns(uint64_t ns);
  * error path of the bounded waits without faulting or hanging the GPU. */
 tpmlp_status tpmlp_debug_timeout_probe(void *workspace, uint64_t wait_ns, void *stream);
 
+/* Column sums out[c] = sum_r x[r, c] of a row-major [rows, cols] device matrix
+ * of the given dtype -- the kernel behind the bias gradients db = 1^T dZ and
+ * da = 1^T dY of tpmlp_backward, same summation order, same results -- for callers
+ * that cannot allocate device memory.  The pages have no counterpart to this
+ * entry point; it exists for the caller, not the method.
+ *
+ * Who needs it: code that must not call cudaMalloc, e.g. a runtime whose device
+ * memory is one pre-reserved arena owned by another component, or a caller on a
+ * latency-critical path where cudaMalloc's implicit synchronisation or its
+ * failure under memory pressure is not acceptable.  tpmlp_backward needs a
+ * caller workspace; this entry point takes only the input and the output.
+ *
+ * Scratch: the fp32 partial sums go to a fixed 4 MiB array inside the library
+ * (1,048,576 floats), which every GPU that loads the library holds until the
+ * process exits.  A call needs chunks*cols floats, where chunks depends only on
+ * (rows, cols) and is at most ceil(1024 / ceil(cols/256)); requests that need
+ * more (for instance cols > 1,048,576) return TPMLP_ERR_UNSUPPORTED with the
+ * reason in tpmlp_last_error().  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) for that device; make that first call
+ * before any stream capture.  Every call uses the same array and leaves its
+ * partials there; nothing in it needs to start at zero.  Calls that can overlap
+ * on the GPU (other streams, other host threads) race on the array: serialise
+ * them.  rows = 0 writes zeros.
+ * Errors: INVALID_ARG for an unknown dtype, rows < 0, cols <= 0 or a NULL
+ * pointer; UNSUPPORTED beyond the scratch limit; CUDA when a launch fails. */
+tpmlp_status tpmlp_colsum_noalloc(int32_t dtype, const void *x, int64_t rows, int64_t cols, void *out,
+                                  void *stream);
+
 /* Number of kernels this library has launched since it was loaded. */
 uint64_t tpmlp_launch_count(void);
 

@@ -30,11 +30,16 @@ void set_last_error(const char *fmt, ...) {
 }  // namespace tpmlp
 
 namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+
+void tpmlp::add_launches(uint64_t n) { g_launches.fetch_add(n); }
+
+namespace {
 
 using tpmlp::Epi;
 using tpmlp::GemmArgs;
 
-std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_wait_ns{2000000000ull};
 
 // ---- per-kernel timing --------------------------------------------------------

@@ -14,8 +14,11 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tpmlp.h"
 
 namespace tpmlp {
 namespace colsum {
@@ -201,3 +204,78 @@ cudaError_t launch_timeout_probe(uint32_t *status, uint64_t wait_ns, cudaStream_
 }
 
 }  // namespace tpmlp
+
+// ---------------------------------------------------------------- no-allocation variant
+// Column sums whose fp32 partials live in a fixed device array of this library
+// instead of a caller workspace, for callers that cannot allocate device memory.
+// The array is part of the module image: every GPU that loads the library holds
+// it (4 MiB) until the process exits.  Pass 1 writes every partial that pass 2
+// reads, so nothing in it has to start at zero; a call simply overwrites what the
+// previous call left there.
+namespace tpmlp {
+namespace noalloc {
+
+constexpr int64_t SCRATCH_FLOATS = int64_t(1) << 20;  // 4 MiB of fp32 partials
+static __device__ __align__(256) float g_scratch[SCRATCH_FLOATS];
+
+// Device address of g_scratch on the current device, looked up once per device.
+// Host code must not use the symbol itself: on the host it is only a stand-in.
+static cudaError_t scratch_ptr(float **out) {
+    static std::mutex mu;
+    static float *ptrs[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_scratch);
+        if (e != cudaSuccess) return e;
+        ptrs[dev] = static_cast<float *>(p);
+    }
+    *out = ptrs[dev];
+    return cudaSuccess;
+}
+
+}  // namespace noalloc
+}  // namespace tpmlp
+
+extern "C" tpmlp_status tpmlp_colsum_noalloc(int32_t dtype, const void *x, int64_t rows, int64_t cols,
+                                             void *out, void *stream) {
+    using namespace tpmlp;
+    set_last_error("%s", "");
+    if (dtype != TPMLP_F32 && dtype != TPMLP_BF16) {
+        set_last_error("tpmlp_colsum_noalloc: unknown dtype %d", dtype);
+        return TPMLP_ERR_INVALID_ARG;
+    }
+    if (rows < 0 || cols <= 0 || !out || (rows > 0 && !x)) {
+        set_last_error("tpmlp_colsum_noalloc: invalid sizes or NULL pointer");
+        return TPMLP_ERR_INVALID_ARG;
+    }
+    const int64_t need = colsum_chunks(rows, cols) * cols;
+    if (need > noalloc::SCRATCH_FLOATS) {
+        set_last_error("tpmlp_colsum_noalloc: %lld columns need %lld fp32 partials, more than the %lld "
+                       "of the library's fixed scratch array",
+                       static_cast<long long>(cols), static_cast<long long>(need),
+                       static_cast<long long>(noalloc::SCRATCH_FLOATS));
+        return TPMLP_ERR_UNSUPPORTED;
+    }
+    float *scratch = nullptr;
+    cudaError_t e = noalloc::scratch_ptr(&scratch);
+    if (e != cudaSuccess) {
+        set_last_error("tpmlp_colsum_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        return TPMLP_ERR_CUDA;
+    }
+    // rows == 0 needs no special case: pass 1 then sums over no rows and writes zeros.
+    int launches = 0;
+    e = launch_colsum(dtype == TPMLP_BF16, x, rows, cols, scratch, out, static_cast<cudaStream_t>(stream),
+                      &launches);
+    add_launches(static_cast<uint64_t>(launches));
+    if (e != cudaSuccess) {
+        set_last_error("tpmlp_colsum_noalloc: launch failed: %s", cudaGetErrorString(e));
+        return TPMLP_ERR_CUDA;
+    }
+    return TPMLP_OK;
+}
+

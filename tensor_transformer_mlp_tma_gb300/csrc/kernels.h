@@ -57,4 +57,7 @@ cudaError_t launch_timeout_probe(uint32_t *status, uint64_t wait_ns, cudaStream_
 // tpmlp_last_error()).
 void set_last_error(const char *fmt, ...);
 
+// Adds to the count reported by tpmlp_launch_count().
+void add_launches(uint64_t n);
+
 }  // namespace tpmlp
