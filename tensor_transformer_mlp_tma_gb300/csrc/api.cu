@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -204,16 +205,43 @@ GemmArgs base_args(uint32_t *status) {
     g.nshards = 1;
     g.status = status;
     g.wait_ns = g_wait_ns.load();
-    g.group_m = 1;
+    g.group = 1;
+    g.raster_n = false;
     return g;
 }
 
-// Raster order: the operand with fewer bytes is the one re-read across the N
-// (or M) tiles that run together, the other one streams through once.
-int pick_group(const GemmArgs &g) {
-    const int64_t m_tiles = (g.M + 127) / 128;
-    const double a_bytes = static_cast<double>(g.M) * g.K, b_bytes = static_cast<double>(g.N) * g.K;
-    return a_bytes <= b_bytes ? static_cast<int>(m_tiles) : 1;
+// Raster order of the tensor-core GEMM tiles (128 x 256).  Tiles are walked in
+// super-rows of G tiles along M (or N); the G operand panels of the grouped
+// dimension (each spans all of K) are re-read while the super-row lasts, so
+// they should stay in L2, and each panel of the other operand is read once per
+// super-row.  DRAM traffic is about  A + B * ceil(m_tiles / G)  (groups along M)
+// or  B + A * ceil(n_tiles / G)  (along N); G is the largest group whose panels
+// fit in the L2 budget, and the cheaper direction wins.
+// TPMLP_RASTER=m:G or n:G overrides the choice (a tuning knob, read per call).
+void pick_raster(GemmArgs &g) {
+    const int64_t m_tiles = (g.M + 127) / 128, n_tiles = (g.N + 255) / 256;
+    const char *env = std::getenv("TPMLP_RASTER");
+    if (env && (env[0] == 'm' || env[0] == 'n') && env[1] == ':') {
+        g.raster_n = env[0] == 'n';
+        g.group = std::atoi(env + 2);
+        return;
+    }
+    const char *bud = std::getenv("TPMLP_L2_PANEL_MB");
+    const double budget = (bud ? std::atof(bud) : 24.0) * 1048576.0;
+    const double a_panel = 128.0 * g.K * 2, b_panel = 256.0 * g.K * 2;
+    const double a_total = static_cast<double>(g.M) * g.K * 2, b_total = static_cast<double>(g.N) * g.K * 2;
+    int64_t gm = static_cast<int64_t>(budget / a_panel), gn = static_cast<int64_t>(budget / b_panel);
+    // Very long K makes panels too big for the budget; tiles that run in the same
+    // wave still share panels while they walk K together, so keep the wave
+    // roughly square: G between 8 and 24 tiles (measured best on GB300).
+    gm = gm < 8 ? 8 : (gm > 24 ? 24 : gm);
+    gn = gn < 8 ? 8 : (gn > 24 ? 24 : gn);
+    gm = gm > m_tiles ? m_tiles : gm;
+    gn = gn > n_tiles ? n_tiles : gn;
+    const double tm = a_total + b_total * static_cast<double>((m_tiles + gm - 1) / gm);
+    const double tn = b_total + a_total * static_cast<double>((n_tiles + gn - 1) / gn);
+    g.raster_n = tn < tm;
+    g.group = static_cast<int>(g.raster_n ? gn : gm);
 }
 
 }  // namespace
@@ -284,7 +312,7 @@ tpmlp_status tpmlp_forward(const tpmlp_shape *s, const void *X, const void *A, c
     g1.b = A, g1.b_mn = true;   // A[h,F]: N contiguous, MN-major
     g1.M = T, g1.N = F, g1.K = h, g1.kshard = h;
     g1.out0 = saved->H, g1.out1 = saved->Y, g1.bias = a;
-    g1.group_m = pick_group(g1);
+    pick_raster(g1);
     cudaError_t e = gemm(s, "fc1_bias_gelu", tpmlp::EPI_BIAS_GELU, g1, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
@@ -295,7 +323,7 @@ tpmlp_status tpmlp_forward(const tpmlp_shape *s, const void *X, const void *A, c
     g2.M = T, g2.N = h, g2.K = F;
     g2.nshards = s->t, g2.kshard = F / s->t;
     g2.out0 = Z, g2.bias = b;
-    g2.group_m = pick_group(g2);
+    pick_raster(g2);
     e = gemm(s, "fc2_shard_fold", tpmlp::EPI_FOLD_BIAS, g2, sms, st);
     return from_cuda(e);
 }
@@ -339,7 +367,7 @@ tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_sa
     g3.b = saved->B, g3.b_mn = false;  // B[F,h] as [N=F, K=h]: K-major
     g3.M = T, g3.N = F, g3.K = h, g3.kshard = h;
     g3.out0 = dY, g3.aux = saved->H;
-    g3.group_m = pick_group(g3);
+    pick_raster(g3);
     e = gemm(s, "bwd_dY_dgelu", tpmlp::EPI_DGELU, g3, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
@@ -353,7 +381,7 @@ tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_sa
     g4.b = dZ, g4.b_mn = true;        // dZ[T,h] as [K=T, N=h]: MN-major
     g4.M = F, g4.N = h, g4.K = T, g4.kshard = T;
     g4.out0 = dB;
-    g4.group_m = pick_group(g4);
+    pick_raster(g4);
     e = gemm(s, "bwd_dB", tpmlp::EPI_STORE, g4, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
@@ -363,7 +391,7 @@ tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_sa
     g5.b = dY, g5.b_mn = true;        // dY[T,F] as [K=T, N=F]: MN-major
     g5.M = h, g5.N = F, g5.K = T, g5.kshard = T;
     g5.out0 = dA;
-    g5.group_m = pick_group(g5);
+    pick_raster(g5);
     e = gemm(s, "bwd_dA", tpmlp::EPI_STORE, g5, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
@@ -374,7 +402,7 @@ tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_sa
     g6.M = T, g6.N = h, g6.K = F;
     g6.nshards = s->t, g6.kshard = F / s->t;
     g6.out0 = dX;
-    g6.group_m = pick_group(g6);
+    pick_raster(g6);
     e = gemm(s, "bwd_dX_shard_fold", tpmlp::EPI_FOLD, g6, sms, st);
     return from_cuda(e);
 }

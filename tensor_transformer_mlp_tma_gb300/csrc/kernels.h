@@ -35,7 +35,8 @@ struct GemmArgs {
     const void *bias;  // a for EPI_BIAS_GELU, b for EPI_FOLD_BIAS
     uint32_t *status;  // device status word
     uint64_t wait_ns;
-    int group_m;       // raster: tiles walk `group_m` M-tiles fastest, then N
+    int group;         // raster: tiles walk `group` M-tiles (N-tiles if raster_n) fastest
+    bool raster_n;
 };
 
 // Tensor-core path: bf16 operands, fp32 accumulation in TMEM (tcgen05).

@@ -47,14 +47,20 @@ constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int NUM_THREADS = 320;
 constexpr int EPI_THREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int SMEM_DYN = STAGES * STAGE_BYTES + 1024;  // + slack to align to 1024
 constexpr int MN_BLOCK_BYTES = 64 * BK * 2;             // one 64(MN) x 64(K) TMA box
+// Epilogue staging: each epilogue warp owns two 32 x 32 bf16 boxes (2 KB each,
+// 64-byte swizzled) that it fills from registers and writes out with TMA stores.
+constexpr int STG_BOX = 32 * 32 * 2;
+constexpr int STG_PER_WARP = 2 * STG_BOX;
+constexpr int SMEM_DYN = STAGES * STAGE_BYTES + (EPI_THREADS / 32) * STG_PER_WARP + 1024;  // + align slack
 
 constexpr uint32_t STATUS_TIMEOUT = 4;  // TPMLP_ERR_TIMEOUT
 
 struct Params {
     int M, N;
-    int m_tiles, n_tiles, group_m;
+    int m_tiles, n_tiles;
+    int group;     // tiles walk `group` M-tiles (or N-tiles if raster_n) fastest
+    int raster_n;  // 0: groups along M; 1: groups along N
     int nshards, kb_per_shard;
     void *out0;
     void *out1;
@@ -64,14 +70,21 @@ struct Params {
     unsigned long long wait_ns;
 };
 
+// Tile order: super-rows of `group` tiles along one dimension; inside a
+// super-row the grouped index runs fastest, so the CTAs resident at one time
+// share `group` panels of one operand and a few of the other.
 __device__ __forceinline__ void tile_coords(int tile, const Params &p, int &mb, int &nb) {
-    const int per_group = p.group_m * p.n_tiles;
+    const int fast_tiles = p.raster_n ? p.n_tiles : p.m_tiles;
+    const int slow_tiles = p.raster_n ? p.m_tiles : p.n_tiles;
+    const int per_group = p.group * slow_tiles;
     const int g = tile / per_group;
-    const int first_m = g * p.group_m;
-    const int gsize = min(p.m_tiles - first_m, p.group_m);
+    const int first = g * p.group;
+    const int gsize = min(fast_tiles - first, p.group);
     const int local = tile - g * per_group;
-    mb = first_m + local % gsize;
-    nb = local / gsize;
+    const int fast = first + local % gsize;
+    const int slow = local / gsize;
+    mb = p.raster_n ? slow : fast;
+    nb = p.raster_n ? fast : slow;
 }
 
 // Records a timeout once in the status word (detail = which role gave up).
@@ -124,41 +137,94 @@ __device__ __forceinline__ void load8(const void *in, int64_t off, float *v) {
     unpack_bf16(w.w, v[6], v[7]);
 }
 
-// Epilogue of one group of 8 columns for the non-fold kinds.
-template <int EPI>
-__device__ __forceinline__ void epi8(const Params &p, int64_t row, int col, float *acc) {
-    const int64_t off = row * p.N + col;
-    if constexpr (EPI == EPI_BIAS_GELU) {
-        float bias[8];
-        load8(p.bias, col, bias);
-        float y[8];
+// Row r of a 32 x 32 bf16 box staged for a 64-byte-swizzled TMA store: 16-byte
+// chunk j of the 64-byte row sits at chunk j ^ ((r >> 1) & 3).
+__device__ __forceinline__ void stage_row(uint32_t box, int r, const uint32_t (&w)[16]) {
+    const uint32_t row = box + static_cast<uint32_t>(r) * 64u;
+    const int x = (r >> 1) & 3;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            acc[i] += bias[i];
-            y[i] = gelu_f(acc[i]);
+    for (int j = 0; j < 4; ++j)
+        ptx::st_shared_v4(row + (static_cast<uint32_t>(j ^ x) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2],
+                          w[4 * j + 3]);
+}
+
+__device__ __forceinline__ void pack32(const float (&v)[32], uint32_t (&w)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
+}
+
+// Loads 32 consecutive bf16 values of a row-major [rows, N] matrix; entries past
+// the end of the row (ragged N) or of the matrix (ok = false) read as zero.
+__device__ __forceinline__ void load32(const void *in, int64_t off, int col, int N, bool ok, float (&v)[32]) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if (ok && col + 8 * g < N) {
+            load8(in, off + 8 * g, &v[8 * g]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[8 * g + i] = 0.0f;
         }
-        if (p.out0) store8(p.out0, off, acc);
-        store8(p.out1, off, y);
+    }
+}
+
+// Finishes one 32-column chunk of this thread's row: applies the epilogue
+// operation to the fp32 accumulator values and writes the result (two results
+// for bias + GeLU) through the warp's staging boxes with TMA stores.  Rows and
+// columns outside the output are clipped by the TMA unit.
+template <int EPI>
+__device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap *tm0, const CUtensorMap *tm1,
+                                             float (&v)[32], int64_t row, int row0, int col, int lane,
+                                             uint32_t stg) {
+    const bool row_ok = row < p.M;
+    uint32_t w0[16], w1[16];
+    bool two = false, store0 = true;
+    if constexpr (EPI == EPI_BIAS_GELU) {
+        float bias[32];
+        load32(p.bias, col, col, p.N, true, bias);
+        float y[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            v[i] += bias[i];
+            y[i] = gelu_f(v[i]);
+        }
+        pack32(v, w0);
+        pack32(y, w1);
+        two = true;
+        store0 = p.out0 != nullptr;
     } else if constexpr (EPI == EPI_DGELU) {
-        float hv[8];
-        load8(p.aux, off, hv);
+        float hv[32];
+        load32(p.aux, row * p.N + col, col, p.N, row_ok, hv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] *= gelu_prime_f(hv[i]);
-        store8(p.out0, off, acc);
+        for (int i = 0; i < 32; ++i) v[i] *= gelu_prime_f(hv[i]);
+        pack32(v, w0);
     } else if constexpr (EPI == EPI_FOLD_BIAS) {
-        float bias[8];
-        load8(p.bias, col, bias);
+        float bias[32];
+        load32(p.bias, col, col, p.N, true, bias);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += bias[i];
-        store8(p.out0, off, acc);
+        for (int i = 0; i < 32; ++i) v[i] += bias[i];
+        pack32(v, w0);
     } else {  // EPI_STORE, EPI_FOLD
-        store8(p.out0, off, acc);
+        pack32(v, w0);
+    }
+    // The previous chunk's stores must have finished reading the staging boxes.
+    if (lane == 0) ptx::bulk_wait_read0();
+    __syncwarp();
+    stage_row(stg, lane, w0);
+    if (two) stage_row(stg + STG_BOX, lane, w1);
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    // A box that lies wholly outside the output (ragged last tile) is not stored.
+    if (lane == 0 && row0 < p.M && col < p.N) {
+        if (store0) ptx::tma_store_2d(tm0, stg, col, row0);
+        if (two) ptx::tma_store_2d(tm1, stg + STG_BOX, col, row0);
+        ptx::bulk_commit();
     }
 }
 
 template <int EPI, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
                 const Params p) {
     constexpr bool FOLD = (EPI == EPI_FOLD_BIAS || EPI == EPI_FOLD);
     constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
@@ -192,6 +258,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB);
+        ptx::prefetch_tensormap(&tmO0);
+        ptx::prefetch_tensormap(&tmO1);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), TMEM_COLS);
@@ -314,6 +382,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int quarter = warp & 3;                    // TMEM lanes this warp may read
         const int half = ew >> 2;                        // column half of the 256-wide tile
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t stg = smem_base + STAGES * STAGE_BYTES + ew * STG_PER_WARP;
         uint32_t unit = 0;
         bool ok = true;
         float sum[FOLD ? 128 : 1];
@@ -321,9 +390,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             int mb, nb;
             tile_coords(tile, p, mb, nb);
-            const int64_t row = static_cast<int64_t>(mb) * BM + quarter * 32 + lane;
+            const int row0 = mb * BM + quarter * 32;
+            const int64_t row = static_cast<int64_t>(row0) + lane;
             const int col0 = nb * BN + half * 128;
-            const bool row_ok = row < p.M;
             for (int s = 0; s < p.nshards; ++s, ++unit) {
                 const uint32_t buf = unit & 1u, use = unit >> 1;
                 bool got = ptx::mbar_wait(ptx::smem_u32(&bar_tfull[buf]), use & 1u, p.wait_ns, &abort_sh);
@@ -348,14 +417,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(ptx::smem_u32(&bar_tempty[buf]));
-                    if (s == p.nshards - 1 && row_ok) {
+                    if (s == p.nshards - 1) {
 #pragma unroll
-                        for (int g = 0; g < 16; ++g) {
-                            const int col = col0 + g * 8;
-                            float v[8];
+                        for (int c = 0; c < 4; ++c) {
+                            float v[32];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) v[i] = sum[g * 8 + i];
-                            if (col < p.N) epi8<EPI>(p, row, col, v);
+                            for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i];
+                            finish_chunk<EPI>(p, &tmO0, &tmO1, v, row, row0, col0 + c * 32, lane, stg);
                         }
                     }
                 } else {
@@ -364,23 +432,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         uint32_t r[32];
                         ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
                         ptx::tmem_ld_wait(r);
-                        if (row_ok) {
-#pragma unroll
-                            for (int g = 0; g < 4; ++g) {
-                                const int col = col0 + c * 32 + g * 8;
-                                float v[8];
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[g * 8 + i]);
-                                if (col < p.N) epi8<EPI>(p, row, col, v);
-                            }
+                        if (c == 3) {
+                            // the whole accumulator slice is in registers: release the buffer
+                            ptx::tc_fence_before();
+                            ptx::mbar_arrive(ptx::smem_u32(&bar_tempty[buf]));
                         }
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                        finish_chunk<EPI>(p, &tmO0, &tmO1, v, row, row0, col0 + c * 32, lane, stg);
                     }
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(ptx::smem_u32(&bar_tempty[buf]));
                 }
             }
         }
         if (!ok) record_timeout(p, &abort_sh, 5);
+        // every TMA store of this warp must be complete before the CTA exits
+        if (lane == 0) ptx::bulk_wait0();
+        __syncwarp();
     }
 
     ptx::tc_fence_before();
@@ -412,7 +480,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // Row-major bf16 matrix [rows, cols] with a box of box_cols (inner) x box_rows.
 static bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, uint32_t box_cols,
-                     uint32_t box_rows) {
+                     uint32_t box_rows, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = encode_fn();
     if (!fn) {
         set_last_error("cuTensorMapEncodeTiled is not available from the driver");
@@ -423,7 +491,7 @@ static bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         set_last_error("cuTensorMapEncodeTiled failed (CUresult %d) for a [%lld, %lld] bf16 matrix, box %u x %u",
@@ -460,13 +528,25 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     const bool oka = A_MN ? make_map(&ma, g.a, g.K, g.M, 64, BK) : make_map(&ma, g.a, g.M, g.K, BK, BM);
     const bool okb = B_MN ? make_map(&mb, g.b, g.K, g.N, 64, BK) : make_map(&mb, g.b, g.N, g.K, BK, BN);
     if (!oka || !okb) return cudaErrorInvalidValue;
+    // Output maps: [M, N] row-major, 32 x 32 boxes, 64-byte swizzle (matches stage_row).
+    // Bias + GeLU writes H (optional) and Y; the others write out0 only.
+    CUtensorMap mo0, mo1;
+    const void *o0 = g.out0 ? g.out0 : g.out1;
+    const void *o1 = (EPI == EPI_BIAS_GELU) ? g.out1 : o0;
+    if (!make_map(&mo0, o0, g.M, g.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map(&mo1, o1, g.M, g.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
 
     Params p;
     p.M = static_cast<int>(g.M);
     p.N = static_cast<int>(g.N);
     p.m_tiles = static_cast<int>((g.M + BM - 1) / BM);
     p.n_tiles = static_cast<int>((g.N + BN - 1) / BN);
-    p.group_m = g.group_m < 1 ? 1 : (g.group_m > p.m_tiles ? p.m_tiles : g.group_m);
+    p.raster_n = g.raster_n ? 1 : 0;
+    {
+        const int fast_tiles = p.raster_n ? p.n_tiles : p.m_tiles;
+        p.group = g.group < 1 ? 1 : (g.group > fast_tiles ? fast_tiles : g.group);
+    }
     p.nshards = g.nshards;
     p.kb_per_shard = static_cast<int>((g.kshard + BK - 1) / BK);
     p.out0 = g.out0;
@@ -477,7 +557,7 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     p.wait_ns = g.wait_ns;
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    kern<<<grid, NUM_THREADS, SMEM_DYN, st>>>(ma, mb, p);
+    kern<<<grid, NUM_THREADS, SMEM_DYN, st>>>(ma, mb, mo0, mo1, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         cudaFuncAttributes fa;
