@@ -148,6 +148,20 @@ __device__ __forceinline__ void stage_row(uint32_t box, int r, const uint32_t (&
                           w[4 * j + 3]);
 }
 
+// Reads row r of a 64-byte-swizzled 32 x 32 bf16 box (the layout a TMA load
+// with SWIZZLE_64B leaves) as 32 floats.
+__device__ __forceinline__ void unstage_row(uint32_t box, int r, float (&v)[32]) {
+    const uint32_t row = box + static_cast<uint32_t>(r) * 64u;
+    const int x = (r >> 1) & 3;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t w[4];
+        ptx::ld_shared_v4(row + (static_cast<uint32_t>(j ^ x) << 4), w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) unpack_bf16(w[i], v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+    }
+}
+
 __device__ __forceinline__ void pack32(const float (&v)[32], uint32_t (&w)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
@@ -171,11 +185,31 @@ __device__ __forceinline__ void load32(const void *in, int64_t off, int col, int
 // operation to the fp32 accumulator values and writes the result (two results
 // for bias + GeLU) through the warp's staging boxes with TMA stores.  Rows and
 // columns outside the output are clipped by the TMA unit.
+// The GeLU' epilogue reads H through the warp's second staging box: a TMA load
+// of the 32 x 32 H chunk is kept one chunk ahead of the chunk being finished.
+struct AuxLoad {
+    uint32_t bar;    // this warp's barrier
+    uint32_t phase;  // parity of the next completion
+    bool pending;    // a load has been issued and not yet consumed
+};
+
+__device__ __forceinline__ void aux_issue(const CUtensorMap *tm, AuxLoad &a, uint32_t box, int col, int row0,
+                                          int lane) {
+    __syncwarp();  // every lane has read the previous chunk out of the box
+    if (lane == 0) {
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive_expect_tx(a.bar, STG_BOX);
+        ptx::tma_load_2d(box, tm, a.bar, col, row0);  // out-of-range parts read as zero
+    }
+    a.pending = true;
+}
+
 template <int EPI>
 __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap *tm0, const CUtensorMap *tm1,
                                              float (&v)[32], int64_t row, int row0, int col, int lane,
-                                             uint32_t stg) {
-    const bool row_ok = row < p.M;
+                                             uint32_t stg, AuxLoad *aux = nullptr, int next_col = -1,
+                                             int next_row0 = 0, volatile int *abort_flag = nullptr) {
+    (void)row;
     uint32_t w0[16], w1[16];
     bool two = false, store0 = true;
     if constexpr (EPI == EPI_BIAS_GELU) {
@@ -193,7 +227,14 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
         store0 = p.out0 != nullptr;
     } else if constexpr (EPI == EPI_DGELU) {
         float hv[32];
-        load32(p.aux, row * p.N + col, col, p.N, row_ok, hv);
+        bool got = ptx::mbar_wait(aux->bar, aux->phase, p.wait_ns, abort_flag);
+        aux->phase ^= 1u;
+        aux->pending = false;
+        if (!__all_sync(0xffffffffu, got)) {
+            if (lane == 0) record_timeout(p, abort_flag, 6);
+        }
+        unstage_row(stg + STG_BOX, lane, hv);
+        if (next_col >= 0) aux_issue(tm1, *aux, stg + STG_BOX, next_col, next_row0, lane);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= gelu_prime_f(hv[i]);
         pack32(v, w0);
@@ -235,6 +276,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __shared__ __align__(8) uint64_t bar_tfull[2];
     __shared__ __align__(8) uint64_t bar_tempty[2];
     __shared__ __align__(8) uint64_t bar_done;
+    __shared__ __align__(8) uint64_t bar_aux[EPI_THREADS / 32];
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
 
@@ -252,6 +294,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(ptx::smem_u32(&bar_tempty[b]), EPI_THREADS);
         }
         ptx::mbar_init(ptx::smem_u32(&bar_done), 1);
+        for (int w = 0; w < EPI_THREADS / 32; ++w) ptx::mbar_init(ptx::smem_u32(&bar_aux[w]), 1);
         abort_sh = 0;
         ptx::fence_mbar_init();
     }
@@ -387,12 +430,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         float sum[FOLD ? 128 : 1];
         (void)sum;
+        AuxLoad aux{ptx::smem_u32(&bar_aux[ew]), 0u, false};
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             int mb, nb;
             tile_coords(tile, p, mb, nb);
             const int row0 = mb * BM + quarter * 32;
             const int64_t row = static_cast<int64_t>(row0) + lane;
             const int col0 = nb * BN + half * 128;
+            if constexpr (EPI == EPI_DGELU) aux_issue(&tmO1, aux, stg + STG_BOX, col0, row0, lane);
             for (int s = 0; s < p.nshards; ++s, ++unit) {
                 const uint32_t buf = unit & 1u, use = unit >> 1;
                 bool got = ptx::mbar_wait(ptx::smem_u32(&bar_tfull[buf]), use & 1u, p.wait_ns, &abort_sh);
@@ -440,12 +485,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         float v[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                        finish_chunk<EPI>(p, &tmO0, &tmO1, v, row, row0, col0 + c * 32, lane, stg);
+                        finish_chunk<EPI>(p, &tmO0, &tmO1, v, row, row0, col0 + c * 32, lane, stg, &aux,
+                                          c < 3 ? col0 + (c + 1) * 32 : -1, row0, &abort_sh);
                     }
                 }
             }
         }
         if (!ok) record_timeout(p, &abort_sh, 5);
+        // an H load still in flight (only after an abort) must land before the CTA exits
+        if (aux.pending && !ptx::mbar_wait(aux.bar, aux.phase, p.wait_ns, nullptr) && lane == 0)
+            record_timeout(p, &abort_sh, 7);
         // every TMA store of this warp must be complete before the CTA exits
         if (lane == 0) ptx::bulk_wait0();
         __syncwarp();
@@ -529,10 +578,11 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     const bool okb = B_MN ? make_map(&mb, g.b, g.K, g.N, 64, BK) : make_map(&mb, g.b, g.N, g.K, BK, BN);
     if (!oka || !okb) return cudaErrorInvalidValue;
     // Output maps: [M, N] row-major, 32 x 32 boxes, 64-byte swizzle (matches stage_row).
-    // Bias + GeLU writes H (optional) and Y; the others write out0 only.
+    // Bias + GeLU writes H (optional) and Y; GeLU' reads H through the second map;
+    // the others write out0 only.
     CUtensorMap mo0, mo1;
     const void *o0 = g.out0 ? g.out0 : g.out1;
-    const void *o1 = (EPI == EPI_BIAS_GELU) ? g.out1 : o0;
+    const void *o1 = (EPI == EPI_BIAS_GELU) ? g.out1 : (EPI == EPI_DGELU ? g.aux : o0);
     if (!make_map(&mo0, o0, g.M, g.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&mo1, o1, g.M, g.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
