@@ -207,6 +207,10 @@ GemmArgs base_args(uint32_t *status) {
     g.wait_ns = g_wait_ns.load();
     g.group = 1;
     g.raster_n = false;
+    // CTA pairs (256 x 256 tiles) by default; TPMLP_CTA_PAIR=0 selects single-CTA
+    // 128 x 256 tiles (a tuning knob, read per call).
+    const char *pair = std::getenv("TPMLP_CTA_PAIR");
+    g.cta_pair = !(pair && pair[0] == '0');
     return g;
 }
 
@@ -219,7 +223,8 @@ GemmArgs base_args(uint32_t *status) {
 // fit in the L2 budget, and the cheaper direction wins.
 // TPMLP_RASTER=m:G or n:G overrides the choice (a tuning knob, read per call).
 void pick_raster(GemmArgs &g) {
-    const int64_t m_tiles = (g.M + 127) / 128, n_tiles = (g.N + 255) / 256;
+    const int64_t tile_m = g.cta_pair ? 256 : 128;
+    const int64_t m_tiles = (g.M + tile_m - 1) / tile_m, n_tiles = (g.N + 255) / 256;
     const char *env = std::getenv("TPMLP_RASTER");
     if (env && (env[0] == 'm' || env[0] == 'n') && env[1] == ':') {
         g.raster_n = env[0] == 'n';
@@ -228,7 +233,7 @@ void pick_raster(GemmArgs &g) {
     }
     const char *bud = std::getenv("TPMLP_L2_PANEL_MB");
     const double budget = (bud ? std::atof(bud) : 24.0) * 1048576.0;
-    const double a_panel = 128.0 * g.K * 2, b_panel = 256.0 * g.K * 2;
+    const double a_panel = static_cast<double>(tile_m) * g.K * 2, b_panel = 256.0 * g.K * 2;
     const double a_total = static_cast<double>(g.M) * g.K * 2, b_total = static_cast<double>(g.N) * g.K * 2;
     int64_t gm = static_cast<int64_t>(budget / a_panel), gn = static_cast<int64_t>(budget / b_panel);
     // Very long K makes panels too big for the budget; tiles that run in the same

@@ -37,6 +37,7 @@ struct GemmArgs {
     uint64_t wait_ns;
     int group;         // raster: tiles walk `group` M-tiles (N-tiles if raster_n) fastest
     bool raster_n;
+    bool cta_pair;     // tensor-core path: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2)
 };
 
 // Tensor-core path: bf16 operands, fp32 accumulation in TMEM (tcgen05).

@@ -2,7 +2,10 @@
 // tcgen05.mma (one thread) -> fp32 accumulators in tensor memory -> epilogue
 // warps (tcgen05.ld) -> fused bias / GeLU / GeLU' / shard fold -> global memory.
 //
-// One persistent CTA per SM, 10 warps:
+// Tiles are 256 x 256 on CTA pairs (a 2-CTA cluster, tcgen05 cta_group::2: each
+// CTA loads its 128 rows of A and 128 of B's 256 columns, the even CTA issues the
+// MMAs, each CTA's TMEM holds its 128 rows of the accumulator) or 128 x 256 on
+// single CTAs.  One persistent CTA per SM, 10 warps:
 //   warp 0      TMA producer (one elected lane): fills a 4-stage ring of
 //               128x64 A tiles and 256x64 B tiles, 128-byte swizzled.
 //   warp 1      MMA issuer (one elected lane) and owner of the 512 TMEM columns:
@@ -28,6 +31,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -37,13 +41,9 @@
 namespace tpmlp {
 namespace tc {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;  // 64 bf16 = one 128-byte swizzle row
-constexpr int STAGES = 4;
-constexpr int A_STAGE = BM * BK * 2;
-constexpr int B_STAGE = BN * BK * 2;
-constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int BM = 128;   // accumulator rows per CTA (TMEM lanes)
+constexpr int BN = 256;   // accumulator columns
+constexpr int BK = 64;    // 64 bf16 = one 128-byte swizzle row
 constexpr int NUM_THREADS = 320;
 constexpr int EPI_THREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;
@@ -52,7 +52,22 @@ constexpr int MN_BLOCK_BYTES = 64 * BK * 2;             // one 64(MN) x 64(K) TM
 // 64-byte swizzled) that it fills from registers and writes out with TMA stores.
 constexpr int STG_BOX = 32 * 32 * 2;
 constexpr int STG_PER_WARP = 2 * STG_BOX;
-constexpr int SMEM_DYN = STAGES * STAGE_BYTES + (EPI_THREADS / 32) * STG_PER_WARP + 1024;  // + align slack
+
+// Per-CTA pipeline geometry.  CG = 1: one CTA computes a 128 x 256 tile and loads
+// all of B's 256 columns.  CG = 2: a CTA pair computes a 256 x 256 tile with
+// CTA-pair MMAs; each CTA loads its own 128 rows of A and 128 of B's columns, so
+// a stage is 32 KB instead of 48 KB and six stages fit.
+template <int CG>
+struct Cfg {
+    static constexpr int TILE_M = BM * CG;
+    static constexpr int B_ROWS = BN / CG;
+    static constexpr int A_STAGE = BM * BK * 2;
+    static constexpr int B_STAGE = B_ROWS * BK * 2;
+    static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+    static constexpr int STAGES = CG == 1 ? 4 : 6;
+    static constexpr int SMEM_DYN = STAGES * STAGE_BYTES + (EPI_THREADS / 32) * STG_PER_WARP + 1024;
+};
+constexpr int MAX_STAGES = 6;
 
 constexpr uint32_t STATUS_TIMEOUT = 4;  // TPMLP_ERR_TIMEOUT
 
@@ -262,17 +277,20 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
     }
 }
 
-template <int EPI, bool A_MN, bool B_MN>
+template <int EPI, bool A_MN, bool B_MN, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
                 const Params p) {
+    using C = Cfg<CG>;
+    constexpr bool PAIR = CG == 2;
     constexpr bool FOLD = (EPI == EPI_FOLD_BIAS || EPI == EPI_FOLD);
-    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(C::TILE_M, BN, A_MN, B_MN);
+    constexpr int STAGES = C::STAGES;
 
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_full[STAGES];
-    __shared__ __align__(8) uint64_t bar_empty[STAGES];
+    __shared__ __align__(8) uint64_t bar_full[MAX_STAGES];
+    __shared__ __align__(8) uint64_t bar_empty[MAX_STAGES];
     __shared__ __align__(8) uint64_t bar_tfull[2];
     __shared__ __align__(8) uint64_t bar_tempty[2];
     __shared__ __align__(8) uint64_t bar_done;
@@ -283,15 +301,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t smem_base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // In a pair the even CTA (rank 0) issues the MMAs and owns the barriers both
+    // CTAs feed: the stage-full barriers (loads of both CTAs) and the
+    // accumulator-empty barriers (epilogues of both CTAs).
+    const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int unit_id = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int num_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
+            // one arrival (the leader's expect-tx for the stage bytes of the whole
+            // pair) plus the transaction bytes of every copy into the stage
             ptx::mbar_init(ptx::smem_u32(&bar_full[s]), 1);
             ptx::mbar_init(ptx::smem_u32(&bar_empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(ptx::smem_u32(&bar_tfull[b]), 1);
-            ptx::mbar_init(ptx::smem_u32(&bar_tempty[b]), EPI_THREADS);
+            // one arrival per epilogue warp of every CTA of the pair
+            ptx::mbar_init(ptx::smem_u32(&bar_tempty[b]), (EPI_THREADS / 32) * CG);
         }
         ptx::mbar_init(ptx::smem_u32(&bar_done), 1);
         for (int w = 0; w < EPI_THREADS / 32; ++w) ptx::mbar_init(ptx::smem_u32(&bar_aux[w]), 1);
@@ -305,11 +333,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::prefetch_tensormap(&tmO1);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), TMEM_COLS);
-        ptx::tmem_relinquish();
+        if constexpr (PAIR) {
+            ptx::tmem_alloc_pair(ptx::smem_u32(&tmem_base_sh), TMEM_COLS);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), TMEM_COLS);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        ptx::cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+    else
+        __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = tmem_base_sh;
 
@@ -323,34 +359,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
                 int mb, nb;
                 tile_coords(tile, p, mb, nb);
-                const int m0 = mb * BM, n0 = nb * BN;
+                const int m0 = mb * C::TILE_M + BM * static_cast<int>(rank);
+                const int n0 = nb * BN + C::B_ROWS * static_cast<int>(rank);
                 for (int kb = 0; kb < kb_total; ++kb) {
-                    if (!ptx::mbar_wait(ptx::smem_u32(&bar_empty[stage]), phase ^ 1u, p.wait_ns,
-                                        &abort_sh)) {
+                    if (!ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_empty[stage]), phase ^ 1u, p.wait_ns,
+                                                     &abort_sh)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t full = ptx::smem_u32(&bar_full[stage]);
-                    const uint32_t sa = smem_base + stage * STAGE_BYTES;
-                    const uint32_t sb = sa + A_STAGE;
+                    const uint32_t full_local = ptx::smem_u32(&bar_full[stage]);
+                    const uint32_t full = PAIR ? ptx::mapa_shared(full_local, 0) : full_local;
+                    const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
+                    const uint32_t sb = sa + C::A_STAGE;
                     const int k0 = kb * BK;
-                    ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
+                    auto load = [&](uint32_t dst, const CUtensorMap *map, int x, int y) {
+                        if constexpr (PAIR)
+                            ptx::tma_load_2d_pair(dst, map, full, x, y);
+                        else
+                            ptx::tma_load_2d(dst, map, full, x, y);
+                    };
+                    // The leader announces the bytes of both CTAs' copies; the peer's
+                    // copies only complete bytes on the leader's barrier (they can land
+                    // before the announcement: the phase still needs the arrival).
+                    if (leader) ptx::mbar_arrive_expect_tx(full_local, CG * C::STAGE_BYTES);
                     if constexpr (!A_MN) {
-                        ptx::tma_load_2d(sa, &tmA, full, k0, m0);
+                        load(sa, &tmA, k0, m0);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BM / 64; ++j)
-                            ptx::tma_load_2d(sa + j * MN_BLOCK_BYTES, &tmA, full, m0 + 64 * j, k0);
+                        for (int j = 0; j < BM / 64; ++j) load(sa + j * MN_BLOCK_BYTES, &tmA, m0 + 64 * j, k0);
                     }
                     if constexpr (!B_MN) {
-                        ptx::tma_load_2d(sb, &tmB, full, k0, n0);
+                        load(sb, &tmB, k0, n0);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)
-                            ptx::tma_load_2d(sb + j * MN_BLOCK_BYTES, &tmB, full, n0 + 64 * j, k0);
+                        for (int j = 0; j < C::B_ROWS / 64; ++j)
+                            load(sb + j * MN_BLOCK_BYTES, &tmB, n0 + 64 * j, k0);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -360,64 +406,79 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (!ok) record_timeout(p, &abort_sh, 1);
-            // Let every copy this thread started land before the CTA can exit.
-            const int64_t tail = issued < STAGES ? issued : STAGES;
-            for (int64_t i = issued - tail; i < issued; ++i) {
-                const int s = static_cast<int>(i % STAGES);
-                const uint32_t ph = static_cast<uint32_t>((i / STAGES) & 1);
-                if (!ptx::mbar_wait(ptx::smem_u32(&bar_full[s]), ph, p.wait_ns, nullptr))
-                    record_timeout(p, &abort_sh, 2);
+            // Let every copy started for this CTA's stages land before the CTA can
+            // exit.  In a pair the stage-full barriers live in the leader and count
+            // both CTAs' copies; the peer is held by the closing cluster barrier.
+            if (leader) {
+                const int64_t tail = issued < STAGES ? issued : STAGES;
+                for (int64_t i = issued - tail; i < issued; ++i) {
+                    const int s = static_cast<int>(i % STAGES);
+                    const uint32_t ph = static_cast<uint32_t>((i / STAGES) & 1);
+                    if (!ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_full[s]), ph, p.wait_ns, nullptr))
+                        record_timeout(p, &abort_sh, 2);
+                }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t unit = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
                 for (int s = 0; s < p.nshards && ok; ++s, ++unit) {
                     const uint32_t buf = unit & 1u, use = unit >> 1;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&bar_tempty[buf]), (use & 1u) ^ 1u, p.wait_ns,
-                                        &abort_sh)) {
+                    if (!ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_tempty[buf]), (use & 1u) ^ 1u, p.wait_ns,
+                                                     &abort_sh)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BN;
                     for (int kb = 0; kb < p.kb_per_shard; ++kb) {
-                        if (!ptx::mbar_wait(ptx::smem_u32(&bar_full[stage]), phase, p.wait_ns,
-                                            &abort_sh)) {
+                        if (!ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_full[stage]), phase, p.wait_ns,
+                                                         &abort_sh)) {
                             ok = false;
                             break;
                         }
                         ptx::tc_fence_after();
-                        const uint32_t sa = smem_base + stage * STAGE_BYTES;
-                        const uint32_t sb = sa + A_STAGE;
+                        const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
+                        const uint32_t sb = sa + C::A_STAGE;
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k) {
                             const uint64_t ad = A_MN ? ptx::sdesc_sw128(sa + k * 2048, MN_BLOCK_BYTES, 1024)
                                                      : ptx::sdesc_sw128(sa + k * 32, 16, 1024);
                             const uint64_t bd = B_MN ? ptx::sdesc_sw128(sb + k * 2048, MN_BLOCK_BYTES, 1024)
                                                      : ptx::sdesc_sw128(sb + k * 32, 16, 1024);
-                            ptx::umma_f16_ss(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                            if constexpr (PAIR)
+                                ptx::umma_f16_ss_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                            else
+                                ptx::umma_f16_ss(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
                         }
-                        ptx::umma_commit(ptx::smem_u32(&bar_empty[stage]));
+                        if constexpr (PAIR)
+                            ptx::umma_commit_pair_multicast(ptx::smem_u32(&bar_empty[stage]), 0x3);
+                        else
+                            ptx::umma_commit(ptx::smem_u32(&bar_empty[stage]));
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
                     if (!ok) break;
-                    ptx::umma_commit(ptx::smem_u32(&bar_tfull[buf]));
+                    if constexpr (PAIR)
+                        ptx::umma_commit_pair_multicast(ptx::smem_u32(&bar_tfull[buf]), 0x3);
+                    else
+                        ptx::umma_commit(ptx::smem_u32(&bar_tfull[buf]));
                 }
             }
             if (!ok) record_timeout(p, &abort_sh, 3);
             // Retire every MMA this thread issued before TMEM can be freed.
-            ptx::umma_commit(ptx::smem_u32(&bar_done));
-            if (!ptx::mbar_wait(ptx::smem_u32(&bar_done), 0, p.wait_ns, nullptr))
-                record_timeout(p, &abort_sh, 4);
+            if constexpr (PAIR)
+                ptx::umma_commit_pair(ptx::smem_u32(&bar_done));
+            else
+                ptx::umma_commit(ptx::smem_u32(&bar_done));
+            if (!ptx::mbar_wait(ptx::smem_u32(&bar_done), 0, p.wait_ns, nullptr)) record_timeout(p, &abort_sh, 4);
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -425,22 +486,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int quarter = warp & 3;                    // TMEM lanes this warp may read
         const int half = ew >> 2;                        // column half of the 256-wide tile
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t stg = smem_base + STAGES * STAGE_BYTES + ew * STG_PER_WARP;
+        const uint32_t stg = smem_base + STAGES * C::STAGE_BYTES + ew * STG_PER_WARP;
         uint32_t unit = 0;
         bool ok = true;
         float sum[FOLD ? 128 : 1];
         (void)sum;
         AuxLoad aux{ptx::smem_u32(&bar_aux[ew]), 0u, false};
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        // After every lane's tcgen05.ld of the buffer has completed, one arrival
+        // per warp on the leader's accumulator-empty barrier.
+        auto release = [&](uint32_t buf) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t a = ptx::smem_u32(&bar_tempty[buf]);
+                if constexpr (PAIR)
+                    ptx::mbar_arrive_remote(ptx::mapa_shared(a, 0));
+                else
+                    ptx::mbar_arrive(a);
+            }
+        };
+        for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
             int mb, nb;
             tile_coords(tile, p, mb, nb);
-            const int row0 = mb * BM + quarter * 32;
+            const int row0 = mb * C::TILE_M + BM * static_cast<int>(rank) + quarter * 32;
             const int64_t row = static_cast<int64_t>(row0) + lane;
             const int col0 = nb * BN + half * 128;
             if constexpr (EPI == EPI_DGELU) aux_issue(&tmO1, aux, stg + STG_BOX, col0, row0, lane);
             for (int s = 0; s < p.nshards; ++s, ++unit) {
                 const uint32_t buf = unit & 1u, use = unit >> 1;
-                bool got = ptx::mbar_wait(ptx::smem_u32(&bar_tfull[buf]), use & 1u, p.wait_ns, &abort_sh);
+                bool got = ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_tfull[buf]), use & 1u, p.wait_ns,
+                                                       &abort_sh);
                 got = __all_sync(0xffffffffu, got);
                 if (!got) {
                     ok = false;
@@ -460,8 +535,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             sum[c * 32 + i] = (s == 0) ? v : sum[c * 32 + i] + v;
                         }
                     }
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(ptx::smem_u32(&bar_tempty[buf]));
+                    release(buf);
                     if (s == p.nshards - 1) {
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
@@ -477,11 +551,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         uint32_t r[32];
                         ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
                         ptx::tmem_ld_wait(r);
-                        if (c == 3) {
-                            // the whole accumulator slice is in registers: release the buffer
-                            ptx::tc_fence_before();
-                            ptx::mbar_arrive(ptx::smem_u32(&bar_tempty[buf]));
-                        }
+                        // the whole accumulator slice is in registers: release the buffer
+                        if (c == 3) release(buf);
                         float v[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
@@ -502,10 +573,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
+    // In a pair, neither CTA leaves (or frees TMEM) while the leader's MMAs may
+    // still read the peer's shared memory or write its TMEM.
+    if constexpr (PAIR) ptx::cluster_sync();
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (PAIR)
+            ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            ptx::tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -549,24 +626,50 @@ static bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols
     return r == CUDA_SUCCESS;
 }
 
-template <int EPI, bool A_MN, bool B_MN>
+template <int EPI, bool A_MN, bool B_MN, int CG>
 static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
-    auto kern = gemm_kernel<EPI, A_MN, B_MN>;
-    // The shared-memory opt-in is a per-device function attribute: set it once per device.
+    using C = Cfg<CG>;
+    auto kern = gemm_kernel<EPI, A_MN, B_MN, CG>;
+    // Per-device, once: the shared-memory opt-in, and for CTA pairs the number of
+    // 2-CTA clusters that can be resident at once (the persistent grid size).
     static std::mutex mu;
     static bool attr_set[64] = {};
+    static int max_clusters[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_DYN;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = CG > 1 ? 1 : 0;  // single CTAs launch without a cluster
     {
         std::lock_guard<std::mutex> lk(mu);
         if (!attr_set[dev]) {
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN);
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_DYN);
             if (e != cudaSuccess) {
-                set_last_error("cudaFuncSetAttribute(%d bytes of shared memory): %s", SMEM_DYN,
+                set_last_error("cudaFuncSetAttribute(%d bytes of shared memory): %s", C::SMEM_DYN,
                                cudaGetErrorString(e));
                 return e;
+            }
+            if (CG > 1) {
+                cfg.gridDim = dim3(static_cast<unsigned>(num_sms / CG * CG), 1, 1);
+                int n = 0;
+                e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+                if (e != cudaSuccess || n < 1) {
+                    set_last_error("cudaOccupancyMaxActiveClusters: %s (%d)", cudaGetErrorString(e), n);
+                    return e != cudaSuccess ? e : cudaErrorLaunchOutOfResources;
+                }
+                max_clusters[dev] = n;
+            } else {
+                max_clusters[dev] = num_sms;
             }
             attr_set[dev] = true;
         }
@@ -574,8 +677,9 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
 
     CUtensorMap ma, mb;
     // A operand: K-major [M,K] with a 64 x 128 box, or MN-major [K,M] with 64 x 64 boxes.
+    // B operand: this CTA's B_ROWS columns, K-major in one box or MN-major in 64-wide boxes.
     const bool oka = A_MN ? make_map(&ma, g.a, g.K, g.M, 64, BK) : make_map(&ma, g.a, g.M, g.K, BK, BM);
-    const bool okb = B_MN ? make_map(&mb, g.b, g.K, g.N, 64, BK) : make_map(&mb, g.b, g.N, g.K, BK, BN);
+    const bool okb = B_MN ? make_map(&mb, g.b, g.K, g.N, 64, BK) : make_map(&mb, g.b, g.N, g.K, BK, C::B_ROWS);
     if (!oka || !okb) return cudaErrorInvalidValue;
     // Output maps: [M, N] row-major, 32 x 32 boxes, 64-byte swizzle (matches stage_row).
     // Bias + GeLU writes H (optional) and Y; GeLU' reads H through the second map;
@@ -590,7 +694,7 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     Params p;
     p.M = static_cast<int>(g.M);
     p.N = static_cast<int>(g.N);
-    p.m_tiles = static_cast<int>((g.M + BM - 1) / BM);
+    p.m_tiles = static_cast<int>((g.M + C::TILE_M - 1) / C::TILE_M);
     p.n_tiles = static_cast<int>((g.N + BN - 1) / BN);
     p.raster_n = g.raster_n ? 1 : 0;
     {
@@ -606,19 +710,31 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     p.status = g.status;
     p.wait_ns = g.wait_ns;
     const int tiles = p.m_tiles * p.n_tiles;
-    const int grid = tiles < num_sms ? tiles : num_sms;
-    kern<<<grid, NUM_THREADS, SMEM_DYN, st>>>(ma, mb, mo0, mo1, p);
-    e = cudaGetLastError();
+    int resident = max_clusters[dev];
+    if (const char *o = std::getenv("TPMLP_MAX_UNITS")) resident = std::atoi(o) > 0 ? std::atoi(o) : resident;
+    const int units = tiles < resident ? tiles : resident;
+    if (std::getenv("TPMLP_DEBUG_LAUNCH"))
+        std::fprintf(stderr, "tpmlp gemm epi=%d cg=%d M=%lld N=%lld K=%lld tiles=%d resident=%d grid=%d group=%d%c\n",
+                     EPI, CG, static_cast<long long>(g.M), static_cast<long long>(g.N), static_cast<long long>(g.K),
+                     tiles, max_clusters[dev], units * CG, p.group, p.raster_n ? 'n' : 'm');
+    cfg.gridDim = dim3(static_cast<unsigned>(units * CG), 1, 1);
+    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo0, mo1, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         cudaFuncAttributes fa;
         std::memset(&fa, 0, sizeof(fa));
         cudaFuncGetAttributes(&fa, kern);
-        set_last_error("tensor-core GEMM launch (grid %d, %d threads, %d bytes shared): %s "
+        set_last_error("tensor-core GEMM launch (grid %d x cluster %d, %d threads, %d bytes shared): %s "
                        "[kernel: %d regs, max %d threads, %zu static + max %d dynamic shared bytes]",
-                       grid, NUM_THREADS, SMEM_DYN, cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock,
-                       fa.sharedSizeBytes, fa.maxDynamicSharedSizeBytes);
+                       units, CG, NUM_THREADS, C::SMEM_DYN, cudaGetErrorString(e), fa.numRegs,
+                       fa.maxThreadsPerBlock, fa.sharedSizeBytes, fa.maxDynamicSharedSizeBytes);
     }
     return e;
+}
+
+template <int EPI, bool A_MN, bool B_MN>
+static cudaError_t launch_cg(const GemmArgs &g, int num_sms, cudaStream_t st) {
+    return g.cta_pair ? launch_t<EPI, A_MN, B_MN, 2>(g, num_sms, st) : launch_t<EPI, A_MN, B_MN, 1>(g, num_sms, st);
 }
 
 }  // namespace tc
@@ -628,19 +744,19 @@ cudaError_t launch_tc_gemm(Epi epi, const GemmArgs &g, int num_sms, cudaStream_t
     if (g.M <= 0 || g.N <= 0 || g.K <= 0) return cudaSuccess;
     switch (epi) {
         case EPI_BIAS_GELU:  // X[T,h] (K-major) . A[h,F] (MN-major)
-            if (!g.a_mn && g.b_mn) return launch_t<EPI_BIAS_GELU, false, true>(g, num_sms, st);
+            if (!g.a_mn && g.b_mn) return launch_cg<EPI_BIAS_GELU, false, true>(g, num_sms, st);
             break;
         case EPI_FOLD_BIAS:  // Y[T,F] (K-major) . B[F,h] (MN-major)
-            if (!g.a_mn && g.b_mn) return launch_t<EPI_FOLD_BIAS, false, true>(g, num_sms, st);
+            if (!g.a_mn && g.b_mn) return launch_cg<EPI_FOLD_BIAS, false, true>(g, num_sms, st);
             break;
         case EPI_DGELU:  // dZ[T,h] (K-major) . B[F,h]^T (K-major)
-            if (!g.a_mn && !g.b_mn) return launch_t<EPI_DGELU, false, false>(g, num_sms, st);
+            if (!g.a_mn && !g.b_mn) return launch_cg<EPI_DGELU, false, false>(g, num_sms, st);
             break;
         case EPI_STORE:  // Y^T . dZ and X^T . dY: both operands MN-major
-            if (g.a_mn && g.b_mn) return launch_t<EPI_STORE, true, true>(g, num_sms, st);
+            if (g.a_mn && g.b_mn) return launch_cg<EPI_STORE, true, true>(g, num_sms, st);
             break;
         case EPI_FOLD:  // dY[T,F] (K-major) . A[h,F]^T (K-major)
-            if (!g.a_mn && !g.b_mn) return launch_t<EPI_FOLD, false, false>(g, num_sms, st);
+            if (!g.a_mn && !g.b_mn) return launch_cg<EPI_FOLD, false, false>(g, num_sms, st);
             break;
     }
     return cudaErrorNotSupported;
