@@ -34,6 +34,7 @@ from tensor_transformer_mlp_tma_gb300.workloads import HEADLINE, WORKLOADS  # no
 
 METRIC = "TP-MLP fwd+bwd TFLOP/s (bf16, 1×GB300) and % of dense BF16 peak"
 UNIT = "TFLOP/s"
+REF_BUDGET_S = 150.0  # wall-time target of the reference arm's warm-up + timed steps
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes (read + write) per launch of each tensor-core GEMM, from one ncu
@@ -180,10 +181,22 @@ def run_reference(args, rank, world):
         return
     w = WORKLOADS[args.workload]
     import oracle
-    inp = inputs.for_workload(w, tokens=args.oracle_tokens)
     lib = oracle.load()
-    f64 = {k: oracle._f64(v) for k, v in inp.items()}
     t = w.shards[-1]
+    # Size the per-step token sample so that warm-up + timed steps take about
+    # REF_BUDGET_S seconds: one calibration step on the requested sample first.
+    tokens = args.oracle_tokens
+    inp = inputs.for_workload(w, tokens=tokens)
+    f64 = {k: oracle._f64(v) for k, v in inp.items()}
+    c0 = time.perf_counter()
+    oracle.forward_backward(f64["X"], f64["A"], f64["a"], f64["B"], f64["b"], f64["dZ"], t, lib=lib)
+    per_step = time.perf_counter() - c0
+    n = args.steps + args.warmup
+    if n * per_step > REF_BUDGET_S and tokens > 1:
+        tokens = max(1, int(tokens * REF_BUDGET_S / (n * per_step)))
+        inp = inputs.for_workload(w, tokens=tokens)
+        f64 = {k: oracle._f64(v) for k, v in inp.items()}
+    args.oracle_tokens = tokens
 
     def step():
         oracle.forward_backward(f64["X"], f64["A"], f64["a"], f64["B"], f64["b"], f64["dZ"], t, lib=lib)
@@ -207,8 +220,10 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def config_of(w, t, world):
+def config_of(w, t, world, fwd_only=False, recompute=False):
     return {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden, "ffn": w.ffn, "t": t,
+            "pass": "forward" if fwd_only else "forward+backward",
+            "activations_kept": "H only (recompute Y)" if recompute else "H and Y",
             "dtype": w.dtype, "parallelism": "replicas x%d" % world if world > 1 else "single GPU",
             "l2": "inputs larger than L2 (A, B 537 MB each; ~3.2 GB touched per step)"
             if w.name == "h8192" else "per-step working set larger than L2"}
@@ -225,7 +240,7 @@ def run_ours(args, rank, world, local, w=None, quiet=False):
     host = inputs.for_workload(w, seed=args.seed + rank)
     d = {k: v.to(dev) for k, v in host.items()}
     T, h, F = w.tokens, w.hidden, w.ffn
-    ctx = tpmlp.Context(T, h, F, t, dt, device=dev)
+    ctx = tpmlp.Context(T, h, F, t, dt, device=dev, recompute=args.recompute)
     Z = torch.empty((T, h), dtype=dt, device=dev)
     g = {"dX": torch.empty((T, h), dtype=dt, device=dev), "dA": torch.empty((h, F), dtype=dt, device=dev),
          "da": torch.empty((F,), dtype=dt, device=dev), "dB": torch.empty((F, h), dtype=dt, device=dev),
@@ -234,7 +249,8 @@ def run_ours(args, rank, world, local, w=None, quiet=False):
 
     def step():
         tpmlp.forward(ctx, d["X"], d["A"], d["a"], d["B"], d["b"], Z=Z, stream=stream)
-        tpmlp.backward(ctx, d["dZ"], stream=stream, **g)
+        if not args.fwd_only:
+            tpmlp.backward(ctx, d["dZ"], stream=stream, **g)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -267,7 +283,7 @@ def run_ours(args, rank, world, local, w=None, quiet=False):
     if st != tpmlp.OK:
         raise RuntimeError("device status after timed region: %s" % tpmlp.status_string(st))
     ms_max = max_over_ranks(ms, world)
-    flops = 12.0 * T * h * F
+    flops = (4.0 if args.fwd_only else 12.0) * T * h * F
     value = flops * world / (ms_max * 1e-3) / 1e12
 
     peaks, peak_src = load_peaks()
@@ -303,13 +319,15 @@ def run_ours(args, rank, world, local, w=None, quiet=False):
 
         def e2e_step():
             dX_in.copy_(hX, non_blocking=True)
-            dZ_in.copy_(hdZ, non_blocking=True)
+            if not args.fwd_only:
+                dZ_in.copy_(hdZ, non_blocking=True)
             tpmlp.forward(ctx, dX_in, d["A"], d["a"], d["B"], d["b"], Z=Z, stream=stream)
-            tpmlp.backward(ctx, dZ_in, stream=stream, **g)
             oZ.copy_(Z, non_blocking=True)
-            odX.copy_(g["dX"], non_blocking=True)
-            oda.copy_(g["da"], non_blocking=True)
-            odb.copy_(g["db"], non_blocking=True)
+            if not args.fwd_only:
+                tpmlp.backward(ctx, dZ_in, stream=stream, **g)
+                odX.copy_(g["dX"], non_blocking=True)
+                oda.copy_(g["da"], non_blocking=True)
+                odb.copy_(g["db"], non_blocking=True)
 
         with torch.cuda.stream(stream):
             for _ in range(max(1, args.warmup)):
@@ -326,16 +344,17 @@ def run_ours(args, rank, world, local, w=None, quiet=False):
         barrier(world)
         ems = max_over_ranks(f0.elapsed_time(f1) / args.steps, world)
         esz = hX.element_size()
+        h2d = hX.numel() + (0 if args.fwd_only else hdZ.numel())
+        d2h = oZ.numel() + (0 if args.fwd_only else odX.numel() + oda.numel() + odb.numel())
         e2e = {"value": flops * world / (ems * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ems,
-               "h2d_bytes_per_step": (hX.numel() + hdZ.numel()) * esz,
-               "d2h_bytes_per_step": (oZ.numel() + odX.numel() + oda.numel() + odb.numel()) * esz,
+               "h2d_bytes_per_step": h2d * esz, "d2h_bytes_per_step": d2h * esz,
                "what": "X and dZ copied in from pinned host memory, Z, dX, da, db copied out, every "
                        "step; weights and weight gradients stay resident"}
 
     clk = clocks.summary()
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": config_of(w, t, world),
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": config_of(w, t, world, args.fwd_only, args.recompute),
             "frac_of_peak": value / world / peaks["bf16_tflops_sustained"],
             "peak_tflops": peaks["bf16_tflops_sustained"], "peak_source": peak_src,
             "roofline": roof, "e2e": e2e, "gpu_launches": int(sum_over_ranks(launches, world)),
@@ -355,6 +374,10 @@ def main():
     ap.add_argument("--t", type=int, default=0, help="shard count (default: the workload's)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--sweep", action="store_true", help="microbatch sweep h12288-b{1,2,4,8}")
+    ap.add_argument("--fwd-only", action="store_true",
+                    help="time tpmlp_forward alone (4*T*h*F FLOP per step)")
+    ap.add_argument("--recompute", action="store_true",
+                    help="activation recomputation: keep only H between forward and backward")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-tokens", type=int, default=32,

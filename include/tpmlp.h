@@ -71,8 +71,18 @@ typedef struct {
     int32_t t;      /* number of tensor-parallel shards, 1..16 */
     int32_t dtype;  /* tpmlp_dtype */
     int32_t algo;   /* tpmlp_algo */
-    int32_t reserved; /* must be 0 */
+    int32_t flags;  /* tpmlp_flags, 0 for the plain pass */
 } tpmlp_shape;
+
+/* TPMLP_FLAG_RECOMPUTE: activation recomputation (the "activation checkpointing"
+ * of the oreateai page, section 2.2; "selective recomputation" in the report's
+ * section 6.4).  The forward pass keeps only the pre-activation H for the
+ * backward pass; Y = GeLU(H) goes to the workspace (TPMLP_WS_Y) for the
+ * row-parallel GEMM and is rebuilt from H by the backward pass's GeLU'
+ * epilogue, which reads H anyway.  Activation memory kept between the passes is
+ * T*F elements instead of 2*T*F.  saved->Y may then be NULL; saved->H is
+ * required. */
+typedef enum { TPMLP_FLAG_RECOMPUTE = 1 } tpmlp_flags;
 
 /* What the forward pass keeps for the backward pass.  The caller allocates H and
  * Y (T*F elements each, tpmlp_saved_bytes() in total); tpmlp_forward() fills in
@@ -91,7 +101,8 @@ typedef struct {
 typedef enum {
     TPMLP_WS_STATUS = 0,  /* uint32 status word (tpmlp_status), then a uint32 detail word */
     TPMLP_WS_PARTIALS = 1, /* fp32 column-sum partials */
-    TPMLP_WS_DY = 2        /* dY = (dZ B^T) * GeLU'(H), [T,F] in the shape's dtype */
+    TPMLP_WS_DY = 2,       /* dY = (dZ B^T) * GeLU'(H), [T,F] in the shape's dtype */
+    TPMLP_WS_Y = 3         /* Y under TPMLP_FLAG_RECOMPUTE, [T,F]; absent (size 0) otherwise */
 } tpmlp_ws_region;
 
 /* Human-readable name of a status code (static storage). */
@@ -104,8 +115,9 @@ int tpmlp_version(void);
  * (empty after a call that succeeded from the start).  Static, per-thread storage. */
 const char *tpmlp_last_error(void);
 
-/* Bytes the caller must allocate for H and Y together (2*T*F elements); 0 when
- * the shape is invalid. */
+/* Bytes the caller must allocate for the saved activations: H and Y together
+ * (2*T*F elements), or H alone (T*F) under TPMLP_FLAG_RECOMPUTE; 0 when the shape
+ * is invalid. */
 size_t tpmlp_saved_bytes(const tpmlp_shape *shape);
 
 /* Bytes of device workspace forward and backward need: the status word, the

@@ -114,7 +114,7 @@ bool shape_valid(const tpmlp_shape *s) {
     if (s->t < 1 || s->t > 16 || s->ffn % s->t != 0) return false;
     if (s->dtype != TPMLP_F32 && s->dtype != TPMLP_BF16) return false;
     if (s->algo != TPMLP_ALGO_DEFAULT && s->algo != TPMLP_ALGO_SIMT) return false;
-    if (s->reserved != 0) return false;
+    if ((s->flags & ~TPMLP_FLAG_RECOMPUTE) != 0) return false;
     // int32 tile and grid arithmetic inside the kernels
     if (s->tokens > (1LL << 30) || s->hidden > (1LL << 30) || s->ffn > (1LL << 30)) return false;
     return true;
@@ -128,11 +128,17 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr size_t STATUS_BYTES = 1024;
 
+// fp32 column-sum partials: the two-pass column sums of db (and of da on the
+// FFMA path), or the per-32-row-block da partials written by the tensor-core
+// GeLU' epilogue.  They are used one after the other, so they share one region.
 size_t partials_bytes(const tpmlp_shape *s) {
     const int64_t T = s->tokens, h = s->hidden, F = s->ffn;
-    const int64_t p1 = tpmlp::colsum_chunks(T, h) * h;
+    int64_t n = tpmlp::colsum_chunks(T, h) * h;
     const int64_t p2 = tpmlp::colsum_chunks(T, F) * F;
-    return align_up(static_cast<size_t>(p1 > p2 ? p1 : p2) * sizeof(float), 1024);
+    const int64_t p3 = (T + 31) / 32 * F;
+    n = n > p2 ? n : p2;
+    n = n > p3 ? n : p3;
+    return align_up(static_cast<size_t>(n) * sizeof(float), 1024);
 }
 
 size_t dy_offset(const tpmlp_shape *s) { return STATUS_BYTES + partials_bytes(s); }
@@ -140,6 +146,12 @@ size_t dy_offset(const tpmlp_shape *s) { return STATUS_BYTES + partials_bytes(s)
 size_t dy_bytes(const tpmlp_shape *s) {
     return align_up(static_cast<size_t>(s->tokens) * static_cast<size_t>(s->ffn) * elt(s), 1024);
 }
+
+bool recompute(const tpmlp_shape *s) { return (s->flags & TPMLP_FLAG_RECOMPUTE) != 0; }
+
+size_t y_offset(const tpmlp_shape *s) { return dy_offset(s) + dy_bytes(s); }
+
+size_t y_bytes(const tpmlp_shape *s) { return recompute(s) ? dy_bytes(s) : 0; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned_elt(const void *p, size_t e) { return (reinterpret_cast<uintptr_t>(p) % e) == 0; }
@@ -271,12 +283,12 @@ const char *tpmlp_last_error(void) { return tpmlp::g_last_error; }
 
 size_t tpmlp_saved_bytes(const tpmlp_shape *s) {
     if (!shape_valid(s)) return 0;
-    return 2 * static_cast<size_t>(s->tokens) * static_cast<size_t>(s->ffn) * elt(s);
+    return (recompute(s) ? 1 : 2) * static_cast<size_t>(s->tokens) * static_cast<size_t>(s->ffn) * elt(s);
 }
 
 size_t tpmlp_workspace_bytes(const tpmlp_shape *s) {
     if (!shape_valid(s)) return 0;
-    return dy_offset(s) + dy_bytes(s);
+    return y_offset(s) + y_bytes(s);
 }
 
 size_t tpmlp_workspace_offset(const tpmlp_shape *s, int region) {
@@ -285,6 +297,7 @@ size_t tpmlp_workspace_offset(const tpmlp_shape *s, int region) {
         case TPMLP_WS_STATUS: return 0;
         case TPMLP_WS_PARTIALS: return STATUS_BYTES;
         case TPMLP_WS_DY: return dy_offset(s);
+        case TPMLP_WS_Y: return y_offset(s);
     }
     return static_cast<size_t>(-1);
 }
@@ -297,8 +310,11 @@ tpmlp_status tpmlp_forward(const tpmlp_shape *s, const void *X, const void *A, c
     if (!saved || !workspace) return invalid("tpmlp_forward: saved or workspace is NULL");
     if (!aligned16(workspace)) return TPMLP_ERR_UNSUPPORTED;
     // With no tokens the [T, .] tensors are empty and may have NULL data pointers.
-    tpmlp_status rc = s->tokens > 0 ? check_ptrs(s, {X, A, a, B, b, Z, saved->Y}, {saved->H})
-                                    : check_ptrs(s, {A, a, B, b}, {X, Z, saved->Y, saved->H});
+    // Under recomputation H is the saved activation and Y lives in the workspace.
+    const bool rec = recompute(s);
+    tpmlp_status rc = s->tokens == 0 ? check_ptrs(s, {A, a, B, b}, {X, Z, saved->Y, saved->H})
+                      : rec          ? check_ptrs(s, {X, A, a, B, b, Z, saved->H}, {saved->Y})
+                                     : check_ptrs(s, {X, A, a, B, b, Z, saved->Y}, {saved->H});
     if (rc != TPMLP_OK) return rc;
     saved->X = X;
     saved->A = A;
@@ -310,20 +326,21 @@ tpmlp_status tpmlp_forward(const tpmlp_shape *s, const void *X, const void *A, c
     if (use_tc(s) && sms < 0) return TPMLP_ERR_DEVICE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint32_t *status = static_cast<uint32_t *>(workspace);
+    void *Y = rec ? static_cast<void *>(static_cast<uint8_t *>(workspace) + y_offset(s)) : saved->Y;
 
     // Column-parallel GEMM of all shards, bias and GeLU fused: H = X A + a, Y = GeLU(H).
     GemmArgs g1 = base_args(status);
     g1.a = X, g1.a_mn = false;  // X[T,h]: K-major
     g1.b = A, g1.b_mn = true;   // A[h,F]: N contiguous, MN-major
     g1.M = T, g1.N = F, g1.K = h, g1.kshard = h;
-    g1.out0 = saved->H, g1.out1 = saved->Y, g1.bias = a;
+    g1.out0 = saved->H, g1.out1 = Y, g1.bias = a;
     pick_raster(g1);
     cudaError_t e = gemm(s, "fc1_bias_gelu", tpmlp::EPI_BIAS_GELU, g1, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
     // Row-parallel GEMM, one accumulation per shard, shard partials folded in order, + b.
     GemmArgs g2 = base_args(status);
-    g2.a = saved->Y, g2.a_mn = false;  // Y[T,F]: K-major
+    g2.a = Y, g2.a_mn = false;  // Y[T,F]: K-major
     g2.b = B, g2.b_mn = true;          // B[F,h]: MN-major
     g2.M = T, g2.N = h, g2.K = F;
     g2.nshards = s->t, g2.kshard = F / s->t;
@@ -339,10 +356,11 @@ tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_sa
     if (!shape_valid(s)) return invalid("tpmlp_backward: invalid shape");
     if (!saved || !workspace) return invalid("tpmlp_backward: saved or workspace is NULL");
     if (!aligned16(workspace)) return TPMLP_ERR_UNSUPPORTED;
+    const bool rec = recompute(s);
     tpmlp_status rc =
-        s->tokens > 0
-            ? check_ptrs(s, {dZ, saved->X, saved->A, saved->B, saved->H, saved->Y, dX, dA, da, dB, db}, {})
-            : check_ptrs(s, {saved->A, saved->B, dA, da, dB, db}, {dZ, saved->X, saved->H, saved->Y, dX});
+        s->tokens == 0 ? check_ptrs(s, {saved->A, saved->B, dA, da, dB, db}, {dZ, saved->X, saved->H, saved->Y, dX})
+        : rec ? check_ptrs(s, {dZ, saved->X, saved->A, saved->B, saved->H, dX, dA, da, dB, db}, {saved->Y})
+              : check_ptrs(s, {dZ, saved->X, saved->A, saved->B, saved->H, saved->Y, dX, dA, da, dB, db}, {});
     if (rc != TPMLP_OK) return rc;
     const int64_t T = s->tokens, h = s->hidden, F = s->ffn;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -361,6 +379,8 @@ tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_sa
     uint32_t *status = reinterpret_cast<uint32_t *>(ws);
     float *partials = reinterpret_cast<float *>(ws + STATUS_BYTES);
     void *dY = ws + dy_offset(s);
+    // Under recomputation the GeLU' epilogue rebuilds Y = GeLU(H) into the workspace.
+    void *Y = rec ? static_cast<void *>(ws + y_offset(s)) : saved->Y;
 
     // db = column sums of dZ
     cudaError_t e = colsum(s, "colsum_db", dZ, T, h, partials, db, st);
@@ -372,17 +392,27 @@ tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_sa
     g3.b = saved->B, g3.b_mn = false;  // B[F,h] as [N=F, K=h]: K-major
     g3.M = T, g3.N = F, g3.K = h, g3.kshard = h;
     g3.out0 = dY, g3.aux = saved->H;
+    g3.out1 = rec ? Y : nullptr;
+    // On tensor cores the epilogue also sums dY's columns per 32-row block.
+    g3.colsum_part = use_tc(s) ? partials : nullptr;
     pick_raster(g3);
     e = gemm(s, "bwd_dY_dgelu", tpmlp::EPI_DGELU, g3, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
-    // da = column sums of dY
-    e = colsum(s, "colsum_da", dY, T, F, partials, da, st);
+    // da = column sums of dY: the in-order sum of those block partials, or a
+    // two-pass column sum of dY on the FFMA path.
+    if (use_tc(s)) {
+        Timed timed("da_block_sum", st);
+        e = tpmlp::launch_colsum_final(true, partials, (T + 31) / 32, F, da, st);
+        if (e == cudaSuccess) g_launches.fetch_add(1);
+    } else {
+        e = colsum(s, "colsum_da", dY, T, F, partials, da, st);
+    }
     if (e != cudaSuccess) return from_cuda(e);
 
     // dB = Y^T dZ
     GemmArgs g4 = base_args(status);
-    g4.a = saved->Y, g4.a_mn = true;  // Y[T,F] as [K=T, M=F]: MN-major
+    g4.a = Y, g4.a_mn = true;  // Y[T,F] as [K=T, M=F]: MN-major
     g4.b = dZ, g4.b_mn = true;        // dZ[T,h] as [K=T, N=h]: MN-major
     g4.M = F, g4.N = h, g4.K = T, g4.kshard = T;
     g4.out0 = dB;

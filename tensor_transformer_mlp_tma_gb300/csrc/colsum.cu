@@ -172,6 +172,18 @@ cudaError_t launch_colsum(bool is_bf16, const void *x, int64_t rows, int64_t col
                                    static_cast<float *>(out), st, launches);
 }
 
+cudaError_t launch_colsum_final(bool is_bf16, const float *partials, int64_t chunks, int64_t cols, void *out,
+                                cudaStream_t st) {
+    if (cols <= 0) return cudaSuccess;
+    const unsigned grid = static_cast<unsigned>((cols + 255) / 256);
+    if (is_bf16)
+        colsum::final_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(partials, chunks, cols,
+                                                                  static_cast<__nv_bfloat16 *>(out));
+    else
+        colsum::final_kernel<float><<<grid, 256, 0, st>>>(partials, chunks, cols, static_cast<float *>(out));
+    return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- timeout probe
 // One warp allocates 32 TMEM columns (so the release path is exercised too),
 // waits on a barrier that never completes for at most wait_ns, records the

@@ -30,7 +30,7 @@ struct GemmArgs {
     int nshards;
     int64_t kshard;
     void *out0;        // H / Z / dY / dB / dA / dX
-    void *out1;        // Y for EPI_BIAS_GELU
+    void *out1;        // Y for EPI_BIAS_GELU; Y rebuilt from H for EPI_DGELU (optional)
     const void *aux;   // H for EPI_DGELU
     const void *bias;  // a for EPI_BIAS_GELU, b for EPI_FOLD_BIAS
     uint32_t *status;  // device status word
@@ -38,6 +38,7 @@ struct GemmArgs {
     int group;         // raster: tiles walk `group` M-tiles (N-tiles if raster_n) fastest
     bool raster_n;
     bool cta_pair;     // tensor-core path: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2)
+    float *colsum_part;  // EPI_DGELU on tensor cores: fp32 column sums per 32-row block [ceil(M/32), N]
 };
 
 // Tensor-core path: bf16 operands, fp32 accumulation in TMEM (tcgen05).
@@ -51,6 +52,10 @@ cudaError_t launch_simt_gemm(Epi epi, bool is_bf16, const GemmArgs &g, cudaStrea
 int64_t colsum_chunks(int64_t rows, int64_t cols);
 cudaError_t launch_colsum(bool is_bf16, const void *x, int64_t rows, int64_t cols, float *partials,
                           void *out, cudaStream_t st, int *launches);
+
+// Second pass alone: out[c] = sum over `chunks` rows of partials[k, c], in order.
+cudaError_t launch_colsum_final(bool is_bf16, const float *partials, int64_t chunks, int64_t cols, void *out,
+                                cudaStream_t st);
 
 // A kernel that waits on a barrier nothing arrives on and reports the timeout.
 cudaError_t launch_timeout_probe(uint32_t *status, uint64_t wait_ns, cudaStream_t st);

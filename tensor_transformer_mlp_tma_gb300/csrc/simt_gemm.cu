@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(256) gemm_kernel(const Params p) {
             } else if constexpr (EPI == EPI_DGELU) {
                 const float hv = ld<T>(static_cast<const T *>(p.aux), o);
                 st<T>(static_cast<T *>(p.out0), o, v * gelu_prime_exact_tanh(hv));
+                if (p.out1) st<T>(static_cast<T *>(p.out1), o, gelu_exact_tanh(hv));  // Y rebuilt from H
             } else {
                 st<T>(static_cast<T *>(p.out0), o, v);
             }

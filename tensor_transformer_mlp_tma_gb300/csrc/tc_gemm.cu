@@ -83,6 +83,7 @@ struct Params {
     const void *bias;
     uint32_t *status;
     unsigned long long wait_ns;
+    float *colsum_part;  // GeLU' epilogue: fp32 column sums of dY per 32-row block, or null
 };
 
 // Tile order: super-rows of `group` tiles along one dimension; inside a
@@ -196,6 +197,48 @@ __device__ __forceinline__ void load32(const void *in, int64_t off, int col, int
     }
 }
 
+// Column sums of a warp's 32 x 32 chunk (row = lane, column j = x[j]) by a
+// fixed butterfly: after five exchange-and-add steps lane L holds the sum over
+// the 32 rows of column L.  The summation tree is the same on every run.
+__device__ __forceinline__ float warp_colsum32(const float (&x)[32], int lane) {
+    float a[16];
+    const bool h16 = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float send = h16 ? x[i] : x[i + 16];
+        const float keep = h16 ? x[i + 16] : x[i];
+        a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+    float b[8];
+    const bool h8 = lane & 8;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float send = h8 ? a[i] : a[i + 8];
+        const float keep = h8 ? a[i + 8] : a[i];
+        b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    float c[4];
+    const bool h4 = lane & 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = h4 ? b[i] : b[i + 4];
+        const float keep = h4 ? b[i + 4] : b[i];
+        c[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    float d[2];
+    const bool h2 = lane & 2;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = h2 ? c[i] : c[i + 2];
+        const float keep = h2 ? c[i + 2] : c[i];
+        d[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    const bool h1 = lane & 1;
+    const float send = h1 ? d[0] : d[1];
+    const float keep = h1 ? d[1] : d[0];
+    return keep + __shfl_xor_sync(0xffffffffu, send, 1);
+}
+
 // Finishes one 32-column chunk of this thread's row: applies the epilogue
 // operation to the fp32 accumulator values and writes the result (two results
 // for bias + GeLU) through the warp's staging boxes with TMA stores.  Rows and
@@ -212,6 +255,7 @@ __device__ __forceinline__ void aux_issue(const CUtensorMap *tm, AuxLoad &a, uin
                                           int lane) {
     __syncwarp();  // every lane has read the previous chunk out of the box
     if (lane == 0) {
+        ptx::bulk_wait_read0();  // a store staged in this box (rebuilt Y) has been read
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive_expect_tx(a.bar, STG_BOX);
         ptx::tma_load_2d(box, tm, a.bar, col, row0);  // out-of-range parts read as zero
@@ -221,12 +265,14 @@ __device__ __forceinline__ void aux_issue(const CUtensorMap *tm, AuxLoad &a, uin
 
 template <int EPI>
 __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap *tm0, const CUtensorMap *tm1,
-                                             float (&v)[32], int64_t row, int row0, int col, int lane,
-                                             uint32_t stg, AuxLoad *aux = nullptr, int next_col = -1,
-                                             int next_row0 = 0, volatile int *abort_flag = nullptr) {
+                                             const CUtensorMap *tm2, float (&v)[32], int64_t row, int row0,
+                                             int col, int lane, uint32_t stg, AuxLoad *aux = nullptr,
+                                             int next_col = -1, int next_row0 = 0,
+                                             volatile int *abort_flag = nullptr) {
     (void)row;
     uint32_t w0[16], w1[16];
     bool two = false, store0 = true;
+    const CUtensorMap *tm_second = tm1;  // map of the second staged box
     if constexpr (EPI == EPI_BIAS_GELU) {
         float bias[32];
         load32(p.bias, col, col, p.N, true, bias);
@@ -249,10 +295,31 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
             if (lane == 0) record_timeout(p, abort_flag, 6);
         }
         unstage_row(stg + STG_BOX, lane, hv);
-        if (next_col >= 0) aux_issue(tm1, *aux, stg + STG_BOX, next_col, next_row0, lane);
+        // With activation recomputation the H box is reused to stage the rebuilt
+        // Y, so the next H load waits until that store has left the box.
+        const bool rebuild_y = p.out1 != nullptr;
+        if (!rebuild_y && next_col >= 0) aux_issue(tm1, *aux, stg + STG_BOX, next_col, next_row0, lane);
+        if (rebuild_y) {
+            float y[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) y[i] = gelu_f(hv[i]);
+            pack32(y, w1);
+            two = true;
+            tm_second = tm2;
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= gelu_prime_f(hv[i]);
         pack32(v, w0);
+        if (p.colsum_part) {
+            // da = 1^T dY: column sums of the stored (bf16-rounded) dY of this
+            // warp's 32 rows.  Rows past M hold exact zeros (zero-filled operands).
+            float q[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) unpack_bf16(w0[i], q[2 * i], q[2 * i + 1]);
+            const float cs = warp_colsum32(q, lane);
+            if (row0 < p.M && col + lane < p.N)
+                p.colsum_part[static_cast<int64_t>(row0 >> 5) * p.N + col + lane] = cs;
+        }
     } else if constexpr (EPI == EPI_FOLD_BIAS) {
         float bias[32];
         load32(p.bias, col, col, p.N, true, bias);
@@ -272,8 +339,11 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
     // A box that lies wholly outside the output (ragged last tile) is not stored.
     if (lane == 0 && row0 < p.M && col < p.N) {
         if (store0) ptx::tma_store_2d(tm0, stg, col, row0);
-        if (two) ptx::tma_store_2d(tm1, stg + STG_BOX, col, row0);
+        if (two) ptx::tma_store_2d(tm_second, stg + STG_BOX, col, row0);
         ptx::bulk_commit();
+    }
+    if constexpr (EPI == EPI_DGELU) {
+        if (p.out1 != nullptr && next_col >= 0) aux_issue(tm1, *aux, stg + STG_BOX, next_col, next_row0, lane);
     }
 }
 
@@ -281,7 +351,7 @@ template <int EPI, bool A_MN, bool B_MN, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
-                const Params p) {
+                const __grid_constant__ CUtensorMap tmO2, const Params p) {
     using C = Cfg<CG>;
     constexpr bool PAIR = CG == 2;
     constexpr bool FOLD = (EPI == EPI_FOLD_BIAS || EPI == EPI_FOLD);
@@ -331,6 +401,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::prefetch_tensormap(&tmB);
         ptx::prefetch_tensormap(&tmO0);
         ptx::prefetch_tensormap(&tmO1);
+        ptx::prefetch_tensormap(&tmO2);
     }
     if (warp == 1) {
         if constexpr (PAIR) {
@@ -542,7 +613,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             float v[32];
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i];
-                            finish_chunk<EPI>(p, &tmO0, &tmO1, v, row, row0, col0 + c * 32, lane, stg);
+                            finish_chunk<EPI>(p, &tmO0, &tmO1, &tmO2, v, row, row0, col0 + c * 32, lane, stg);
                         }
                     }
                 } else {
@@ -556,7 +627,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         float v[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                        finish_chunk<EPI>(p, &tmO0, &tmO1, v, row, row0, col0 + c * 32, lane, stg, &aux,
+                        finish_chunk<EPI>(p, &tmO0, &tmO1, &tmO2, v, row, row0, col0 + c * 32, lane, stg, &aux,
                                           c < 3 ? col0 + (c + 1) * 32 : -1, row0, &abort_sh);
                     }
                 }
@@ -684,11 +755,14 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     // Output maps: [M, N] row-major, 32 x 32 boxes, 64-byte swizzle (matches stage_row).
     // Bias + GeLU writes H (optional) and Y; GeLU' reads H through the second map;
     // the others write out0 only.
-    CUtensorMap mo0, mo1;
+    // The GeLU' epilogue can also write Y rebuilt from H (third map).
+    CUtensorMap mo0, mo1, mo2;
     const void *o0 = g.out0 ? g.out0 : g.out1;
     const void *o1 = (EPI == EPI_BIAS_GELU) ? g.out1 : (EPI == EPI_DGELU ? g.aux : o0);
+    const void *o2 = (EPI == EPI_DGELU && g.out1) ? g.out1 : o0;
     if (!make_map(&mo0, o0, g.M, g.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&mo1, o1, g.M, g.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+        !make_map(&mo1, o1, g.M, g.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map(&mo2, o2, g.M, g.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
 
     Params p;
@@ -709,6 +783,7 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     p.bias = g.bias;
     p.status = g.status;
     p.wait_ns = g.wait_ns;
+    p.colsum_part = g.colsum_part;
     const int tiles = p.m_tiles * p.n_tiles;
     int resident = max_clusters[dev];
     if (const char *o = std::getenv("TPMLP_MAX_UNITS")) resident = std::atoi(o) > 0 ? std::atoi(o) : resident;
@@ -718,7 +793,7 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
                      EPI, CG, static_cast<long long>(g.M), static_cast<long long>(g.N), static_cast<long long>(g.K),
                      tiles, max_clusters[dev], units * CG, p.group, p.raster_n ? 'n' : 'm');
     cfg.gridDim = dim3(static_cast<unsigned>(units * CG), 1, 1);
-    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo0, mo1, p);
+    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo0, mo1, mo2, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         cudaFuncAttributes fa;

@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(_HERE, "libtpmlp.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(6)
 F32, BF16 = 0, 1
 ALGO_DEFAULT, ALGO_SIMT = 0, 1
-WS_STATUS, WS_PARTIALS, WS_DY = 0, 1, 2
+WS_STATUS, WS_PARTIALS, WS_DY, WS_Y = 0, 1, 2, 3
+FLAG_RECOMPUTE = 1
 
 _DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -26,7 +27,7 @@ _DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
 class Shape(ctypes.Structure):
     _fields_ = [("tokens", ctypes.c_int64), ("hidden", ctypes.c_int64), ("ffn", ctypes.c_int64),
                 ("t", ctypes.c_int32), ("dtype", ctypes.c_int32), ("algo", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("flags", ctypes.c_int32)]
 
 
 class Saved(ctypes.Structure):
@@ -87,10 +88,11 @@ def last_error() -> str:
     return lib.tpmlp_last_error().decode(errors="replace")
 
 
-def make_shape(tokens: int, hidden: int, ffn: int, t: int, dtype, algo: int = ALGO_DEFAULT) -> Shape:
+def make_shape(tokens: int, hidden: int, ffn: int, t: int, dtype, algo: int = ALGO_DEFAULT,
+               flags: int = 0) -> Shape:
     if isinstance(dtype, torch.dtype):
         dtype = _DTYPES[dtype]
-    return Shape(int(tokens), int(hidden), int(ffn), int(t), int(dtype), int(algo), 0)
+    return Shape(int(tokens), int(hidden), int(ffn), int(t), int(dtype), int(algo), int(flags))
 
 
 def saved_bytes(shape: Shape) -> int:
@@ -145,25 +147,38 @@ class Context:
     """The buffers one layer needs between forward and backward: H, Y and the
     workspace, plus the ctypes shape and saved-activation records."""
 
-    def __init__(self, tokens, hidden, ffn, t, dtype, algo=ALGO_DEFAULT, device=None, keep_H=True):
-        self.shape = make_shape(tokens, hidden, ffn, t, dtype, algo)
+    def __init__(self, tokens, hidden, ffn, t, dtype, algo=ALGO_DEFAULT, device=None, keep_H=True,
+                 recompute=False):
+        """recompute=True keeps only H between the passes (TPMLP_FLAG_RECOMPUTE):
+        Y then lives in the workspace and is rebuilt by the backward pass."""
+        self.shape = make_shape(tokens, hidden, ffn, t, dtype, algo, FLAG_RECOMPUTE if recompute else 0)
         if saved_bytes(self.shape) == 0 and tokens > 0:
             raise ValueError("invalid shape (tokens=%d hidden=%d ffn=%d t=%d)" % (tokens, hidden, ffn, t))
         self.dtype = dtype
+        self.recompute = recompute
         dev = device or "cuda"
-        self.H = torch.empty((tokens, ffn), dtype=dtype, device=dev) if keep_H else None
-        self.Y = torch.empty((tokens, ffn), dtype=dtype, device=dev)
+        self.H = torch.empty((tokens, ffn), dtype=dtype, device=dev) if (keep_H or recompute) else None
+        self._Y = None if recompute else torch.empty((tokens, ffn), dtype=dtype, device=dev)
         self.workspace = new_workspace(self.shape, dev)
-        self.saved = Saved(None, None, None, _ptr(self.H), _ptr(self.Y))
+        self.saved = Saved(None, None, None, _ptr(self.H), _ptr(self._Y))
         self._keep = []
+
+    def _ws_view(self, region):
+        T, F = self.shape.tokens, self.shape.ffn
+        off = workspace_offset(self.shape, region)
+        esz = 2 if self.dtype == torch.bfloat16 else 4
+        return self.workspace[off:off + T * F * esz].view(self.dtype).view(T, F)
+
+    @property
+    def Y(self) -> torch.Tensor:
+        """GeLU(H): the caller-owned buffer, or under recomputation the workspace
+        copy (written by forward, rebuilt by backward)."""
+        return self._ws_view(WS_Y) if self.recompute else self._Y
 
     @property
     def dY(self) -> torch.Tensor:
         """The dY intermediate of the last backward (a view into the workspace)."""
-        T, F = self.shape.tokens, self.shape.ffn
-        off = workspace_offset(self.shape, WS_DY)
-        esz = 2 if self.dtype == torch.bfloat16 else 4
-        return self.workspace[off:off + T * F * esz].view(self.dtype).view(T, F)
+        return self._ws_view(WS_DY)
 
 
 def forward(ctx: Context, X, A, a, B, b, Z=None, stream=None):

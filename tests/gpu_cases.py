@@ -25,20 +25,20 @@ def to_np(x: torch.Tensor) -> np.ndarray:
     return x.detach().double().cpu().numpy()
 
 
-def run_gpu(inp: dict, t: int, algo=None, device="cuda", keep=False):
+def run_gpu(inp: dict, t: int, algo=None, device="cuda", keep=False, recompute=False):
     """Forward + backward on the GPU; returns (outputs as GPU tensors, context)."""
     from tensor_transformer_mlp_tma_gb300 import tpmlp
     algo = tpmlp.ALGO_DEFAULT if algo is None else algo
     d = {k: v.to(device) for k, v in inp.items()}
     T, h = d["X"].shape
     F = d["A"].shape[1]
-    ctx = tpmlp.Context(T, h, F, t, d["X"].dtype, algo, device)
+    ctx = tpmlp.Context(T, h, F, t, d["X"].dtype, algo, device, recompute=recompute)
     Z = tpmlp.forward(ctx, d["X"], d["A"], d["a"], d["B"], d["b"])
     g = tpmlp.backward(ctx, d["dZ"])
     torch.cuda.synchronize()
     st = tpmlp.check_device_status(ctx)
     assert st == tpmlp.OK, "device status: %s" % tpmlp.status_string(st)
-    out = {"H": ctx.H, "Y": ctx.Y, "Z": Z, "dY": ctx.dY.clone()}
+    out = {"H": ctx.H, "Y": ctx.Y.clone(), "Z": Z, "dY": ctx.dY.clone()}
     out.update(g)
     if keep:
         out["_dev_inputs"] = d

@@ -64,9 +64,14 @@ def test_size_queries(tp):
                 tp.make_shape(128, 256, 1024, 0, tp.BF16),   # t < 1
                 tp.Shape(128, 256, 1024, 2, 7, 0, 0),        # dtype
                 tp.Shape(128, 256, 1024, 2, 1, 5, 0),        # algo
-                tp.Shape(128, 256, 1024, 2, 1, 0, 1)):       # reserved
+                tp.Shape(128, 256, 1024, 2, 1, 0, 2)):       # unknown flag
         assert tp.saved_bytes(bad) == 0
         assert tp.workspace_bytes(bad) == 0
+    # recomputation keeps H only and moves Y into the workspace
+    rec = tp.make_shape(4096, 8192, 32768, 8, tp.BF16, flags=tp.FLAG_RECOMPUTE)
+    assert tp.saved_bytes(rec) == 4096 * 32768 * 2
+    assert tp.workspace_offset(rec, tp.WS_Y) == tp.workspace_bytes(s)
+    assert tp.workspace_bytes(rec) == tp.workspace_bytes(s) + 4096 * 32768 * 2
     # an empty batch is valid
     assert tp.workspace_bytes(tp.make_shape(0, 256, 1024, 2, tp.BF16)) > 0
 
@@ -98,6 +103,9 @@ def test_forward_invalid_arguments(tp):
         assert _fwd(tp, good, ptrs=p) == tp.ERR_INVALID_ARG
     assert _fwd(tp, good, saved=tp.Saved(None, None, None, FAKE, None)) == tp.ERR_INVALID_ARG
     assert _fwd(tp, good, ws=None) == tp.ERR_INVALID_ARG
+    # under recomputation H is required (it is the saved activation)
+    rec = tp.make_shape(256, 256, 1024, 2, tp.BF16, flags=tp.FLAG_RECOMPUTE)
+    assert _fwd(tp, rec, saved=tp.Saved(None, None, None, None, FAKE)) == tp.ERR_INVALID_ARG
 
 
 def test_forward_unsupported(tp):

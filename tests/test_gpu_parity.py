@@ -138,7 +138,40 @@ def test_inference_forward_without_H():
     compare_full({"Z": Z, "Y": ctx.Y}, ref, {"Z": 1e-2, "Y": 1e-2})
 
 
+@pytest.mark.parametrize("algo", ["tc", "simt"])
+@pytest.mark.parametrize("T,h,F,t", [(300, 384, 1280, 2), (257, 512, 1024, 4)])
+def test_recompute_matches_oracle_and_plain_mode(T, h, F, t, algo):
+    """Activation recomputation (only H kept between the passes, Y rebuilt from H
+    in the backward GeLU' epilogue) against the oracle, and against the plain
+    mode: Z, dY, dX, dA, da, db come out of identical arithmetic and must be
+    bit-identical; dB uses the rebuilt Y (GeLU of the stored bf16 H instead of
+    the fp32 pre-activation) and is compared within tolerance."""
+    from tensor_transformer_mlp_tma_gb300 import tpmlp
+    a = tpmlp.ALGO_SIMT if algo == "simt" else tpmlp.ALGO_DEFAULT
+    inp = inputs.make(T, h, F, "bf16", seed=T * 3 + t, std=STD)
+    rec, ctx = run_gpu(inp, t, algo=a, recompute=True)
+    assert tpmlp.saved_bytes(ctx.shape) == T * F * 2
+    ref = oracle.forward_backward(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], inp["dZ"], t)
+    compare_full(rec, ref, TOL_BF16)
+    plain, _ = run_gpu(inp, t, algo=a)
+    for k in ("Z", "H", "dY", "dX", "dA", "da", "db"):
+        assert torch.equal(rec[k].view(torch.int16), plain[k].view(torch.int16)), k
+    compare_full({"dB": rec["dB"]}, {"dB": to_np(plain["dB"])}, {"dB": 2e-2})
+
+
 FULL = [("h2048", 1), ("h2048", 2), ("h2048", 4), ("h4096", 8), ("h8192", 8), ("h12288-b1", 8)]
+
+
+@pytest.mark.parametrize("name,t", [("h8192", 8)])
+def test_full_size_recompute_slices(name, t):
+    w = WORKLOADS[name]
+    inp = inputs.for_workload(w)
+    out, _ = run_gpu(inp, t, recompute=True)
+    T, F = w.tokens, w.ffn
+    R = sample_indices(T, 32, seed=3, must=(0, T - 1))
+    J = sample_indices(F, 96, seed=4, must=[0, F - 1] + [i * (F // t) for i in range(t)])
+    ref = oracle.slice_(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], inp["dZ"], t, R, J)
+    compare_slices(out, ref, R, J, TOL_BF16)
 
 
 @pytest.mark.parametrize("name,t", FULL)
