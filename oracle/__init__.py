@@ -70,6 +70,10 @@ def load(path: str | None = None):
         lib.oracle_slice.restype = ctypes.c_int
         lib.oracle_slice.argtypes = ([_I64, _I64, _I64, _I32] + [_DP] * 6 +
                                      [_I64, _LP, _I64, _LP] + [_DP] * 12)
+        lib.oracle_layernorm_forward.restype = None
+        lib.oracle_layernorm_forward.argtypes = [_I64, _I64, _DP, _DP, _DP, ctypes.c_double, _DP, _DP, _DP]
+        lib.oracle_layernorm_backward.restype = ctypes.c_int
+        lib.oracle_layernorm_backward.argtypes = [_I64, _I64, _DP, _DP, _DP, ctypes.c_double, _DP, _DP, _DP]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         if path is None:
@@ -181,6 +185,46 @@ def slice_(X, A, a, B, b, dZ, t: int, rows, cols, lib=None) -> dict:
                                                  "dYc", "dAc", "daJ", "dBr", "db")))
     if rc != 0:
         raise ValueError("oracle_slice rejected the arguments (rc=%d)" % rc)
+    return out
+
+
+def layernorm_forward(X, gamma, beta, eps: float, lib=None) -> dict:
+    """LayerNorm of every row: Y, and the row mean and 1/std (fp64)."""
+    lib = lib or load()
+    X, gamma, beta = (_f64(v) for v in (X, gamma, beta))
+    T, h = X.shape
+    Y = np.empty((T, h))
+    mean = np.empty(T)
+    rstd = np.empty(T)
+    lib.oracle_layernorm_forward(T, h, _p(X), _p(gamma), _p(beta), float(eps), _p(Y), _p(mean), _p(rstd))
+    return {"Y": Y, "mean": mean, "rstd": rstd}
+
+
+def layernorm_backward(dY, X, gamma, eps: float, lib=None) -> dict:
+    """dX, dgamma, dbeta of LayerNorm for the upstream gradient dY (fp64)."""
+    lib = lib or load()
+    dY, X, gamma = (_f64(v) for v in (dY, X, gamma))
+    T, h = X.shape
+    dX = np.empty((T, h))
+    dg = np.empty(h)
+    db = np.empty(h)
+    rc = lib.oracle_layernorm_backward(T, h, _p(dY), _p(X), _p(gamma), float(eps), _p(dX), _p(dg), _p(db))
+    if rc != 0:
+        raise MemoryError("oracle_layernorm_backward")
+    return {"dX": dX, "dgamma": dg, "dbeta": db}
+
+
+def sp_forward_backward(X_in, gamma, beta, eps, A, a, B, b, dZ, t: int, lib=None) -> dict:
+    """The sequence-parallel MLP block: LayerNorm of the input rows, then the
+    tensor-parallel MLP, and the backward pass through both.  Token shards only
+    change where rows live, not any value, so the whole batch is processed at
+    once.  Returns the MLP outputs plus Xn (normalised input), mean, rstd,
+    dX_in, dgamma, dbeta."""
+    ln = layernorm_forward(X_in, gamma, beta, eps, lib=lib)
+    out = forward_backward(ln["Y"], A, a, B, b, dZ, t, lib=lib)
+    lb = layernorm_backward(out["dX"], X_in, gamma, eps, lib=lib)
+    out.update({"Xn": ln["Y"], "mean": ln["mean"], "rstd": ln["rstd"], "dX_in": lb["dX"],
+                "dgamma": lb["dgamma"], "dbeta": lb["dbeta"]})
     return out
 
 

@@ -368,6 +368,87 @@ int oracle_slice(int64_t T, int64_t h, int64_t F, int32_t t,
     return 0;
 }
 
+/* ---- LayerNorm (sequence-parallel MLP) ----------------------------------------
+ * The report's section 4.3 runs LayerNorm locally on each token shard in front
+ * of the tensor-parallel MLP (sequence parallelism); LayerNorm itself is the
+ * textbook per-row normalisation (Ba, Kiros & Hinton, 2016):
+ *   mu_r = mean_j x[r,j],  var_r = mean_j (x[r,j] - mu_r)^2,  rstd_r = 1/sqrt(var_r + eps),
+ *   y[r,j] = (x[r,j] - mu_r) * rstd_r * gamma[j] + beta[j].
+ * Rows are independent, so token shards need no exchange. */
+void oracle_layernorm_forward(int64_t T, int64_t h, const double *X, const double *gamma,
+                              const double *beta, double eps, double *Y, double *mean,
+                              double *rstd) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T; ++r) {
+        const double *x = X + r * h;
+        double s = 0.0;
+        for (int64_t j = 0; j < h; ++j) s += x[j];
+        const double mu = s / (double)h;
+        double v = 0.0;
+        for (int64_t j = 0; j < h; ++j) v += (x[j] - mu) * (x[j] - mu);
+        v /= (double)h;
+        const double rs = 1.0 / sqrt(v + eps);
+        for (int64_t j = 0; j < h; ++j) Y[r * h + j] = (x[j] - mu) * rs * gamma[j] + beta[j];
+        if (mean) mean[r] = mu;
+        if (rstd) rstd[r] = rs;
+    }
+}
+
+/* Backward of the above for an upstream gradient dY (chain rule through mu and
+ * var):  xhat = (x - mu) rstd,  g = dY * gamma,
+ *   dX[r,j] = rstd_r (g[r,j] - mean_j g[r,.] - xhat[r,j] mean_j (g[r,.] xhat[r,.])),
+ *   dgamma = sum_r dY * xhat,  dbeta = sum_r dY.  mean and rstd are recomputed. */
+int oracle_layernorm_backward(int64_t T, int64_t h, const double *dY, const double *X,
+                              const double *gamma, double eps, double *dX, double *dgamma,
+                              double *dbeta) {
+    double *mu = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    double *rs = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    if (!mu || !rs) {
+        free(mu);
+        free(rs);
+        return -2;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T; ++r) {
+        const double *x = X + r * h;
+        const double *dy = dY + r * h;
+        double s = 0.0;
+        for (int64_t j = 0; j < h; ++j) s += x[j];
+        const double m = s / (double)h;
+        double v = 0.0;
+        for (int64_t j = 0; j < h; ++j) v += (x[j] - m) * (x[j] - m);
+        v /= (double)h;
+        const double rstd = 1.0 / sqrt(v + eps);
+        mu[r] = m;
+        rs[r] = rstd;
+        double mg = 0.0, mgx = 0.0;
+        for (int64_t j = 0; j < h; ++j) {
+            const double g = dy[j] * gamma[j];
+            mg += g;
+            mgx += g * (x[j] - m) * rstd;
+        }
+        mg /= (double)h;
+        mgx /= (double)h;
+        for (int64_t j = 0; j < h; ++j) {
+            const double xh = (x[j] - m) * rstd;
+            dX[r * h + j] = rstd * (dy[j] * gamma[j] - mg - xh * mgx);
+        }
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < h; ++j) {
+        double sg = 0.0, sb = 0.0;
+        for (int64_t r = 0; r < T; ++r) {
+            sg += dY[r * h + j] * (X[r * h + j] - mu[r]) * rs[r];
+            sb += dY[r * h + j];
+        }
+        dgamma[j] = sg;
+        dbeta[j] = sb;
+    }
+    free(mu);
+    free(rs);
+    return 0;
+}
+
 /* Number of OpenMP threads a parallel region of this library will use. */
 int oracle_num_threads(void) {
 #ifdef _OPENMP

@@ -21,6 +21,11 @@ What pins what:
   * closed forms -- X = 0 gives Z = gelu(a) B + b and dA = 0; A = 0, a = 0 give
                  Z = b, dY = dZ B^T / 2, dX = 0; db is the column sum of dZ.
   * slices    -- the exact row/column slices equal the full result.
+  * LayerNorm -- numpy's population mean/variance definition; normalised rows
+                 have mean 0 and variance 1; invariance to a positive scale and a
+                 shift of a row; dX orthogonal to 1 and xhat; central finite
+                 differences for dX, dgamma, dbeta, and for the whole
+                 sequence-parallel block (LayerNorm, then the sharded MLP).
 """
 from __future__ import annotations
 
@@ -233,9 +238,115 @@ def check_slice_vs_full(lib):
     return f
 
 
+def check_layernorm_numpy(lib):
+    """LayerNorm against numpy's population mean and variance (the textbook
+    definition, Ba et al. 2016)."""
+    f = []
+    rng = np.random.default_rng(500)
+    for T, h, eps in ((4, 16, 1e-5), (7, 33, 1e-6), (1, 8192, 1e-5)):
+        X = rng.standard_normal((T, h)) * 3 + 1.5
+        g = rng.standard_normal(h)
+        b = rng.standard_normal(h)
+        out = oracle.layernorm_forward(X, g, b, eps, lib=lib)
+        mu = X.mean(axis=1, keepdims=True)
+        var = X.var(axis=1, keepdims=True)
+        ref = (X - mu) / np.sqrt(var + eps) * g + b
+        if _rel(out["Y"], ref) > 1e-12:
+            f.append("layernorm h=%d differs from numpy (%.3e)" % (h, _rel(out["Y"], ref)))
+        if _rel(out["mean"], mu[:, 0]) > 1e-14 or _rel(out["rstd"], 1 / np.sqrt(var[:, 0] + eps)) > 1e-12:
+            f.append("layernorm statistics differ from numpy")
+    return f
+
+
+def check_layernorm_invariants(lib):
+    f = []
+    rng = np.random.default_rng(501)
+    T, h = 5, 64
+    X = rng.standard_normal((T, h))
+    one, zero = np.ones(h), np.zeros(h)
+    y = oracle.layernorm_forward(X, one, zero, 0.0, lib=lib)["Y"]
+    if np.max(np.abs(y.mean(axis=1))) > 1e-14 or np.max(np.abs(y.var(axis=1) - 1)) > 1e-13:
+        f.append("normalised rows do not have mean 0 and variance 1")
+    y2 = oracle.layernorm_forward(3.7 * X - 2.0, one, zero, 0.0, lib=lib)["Y"]
+    if _rel(y2, y) > 1e-12:
+        f.append("layernorm is not invariant to a positive scale and a shift of the row")
+    # dX is orthogonal to the all-ones and to xhat directions (LN is invariant to both)
+    dY = rng.standard_normal((T, h))
+    bw = oracle.layernorm_backward(dY, X, one, 0.0, lib=lib)
+    xh = y
+    if np.max(np.abs(bw["dX"].sum(axis=1))) > 1e-12 or np.max(np.abs((bw["dX"] * xh).sum(axis=1))) > 1e-11:
+        f.append("layernorm dX is not orthogonal to 1 and xhat")
+    if _rel(bw["dbeta"], dY.sum(axis=0)) > 1e-13:
+        f.append("dbeta != column sum of dY")
+    return f
+
+
+def check_layernorm_backward_fd(lib, eps_fd=1e-6, tol=1e-6):
+    f = []
+    rng = np.random.default_rng(502)
+    T, h, eps = 3, 5, 1e-5
+    X = rng.standard_normal((T, h)) * 2
+    g = rng.standard_normal(h)
+    b = rng.standard_normal(h)
+    dY = rng.standard_normal((T, h))
+
+    def loss():
+        return float(np.sum(dY * oracle.layernorm_forward(X, g, b, eps, lib=lib)["Y"]))
+
+    bw = oracle.layernorm_backward(dY, X, g, eps, lib=lib)
+    for name, p, grad in (("X", X, bw["dX"]), ("gamma", g, bw["dgamma"]), ("beta", b, bw["dbeta"])):
+        fd = np.empty_like(p)
+        flat = p.reshape(-1)
+        for i in range(flat.size):
+            old = flat[i]
+            flat[i] = old + eps_fd
+            lp = loss()
+            flat[i] = old - eps_fd
+            lm = loss()
+            flat[i] = old
+            fd.reshape(-1)[i] = (lp - lm) / (2 * eps_fd)
+        if _rel(grad, fd) > tol:
+            f.append("layernorm d%s vs finite differences: rel %.3e" % (name, _rel(grad, fd)))
+    return f
+
+
+def check_sp_composition_fd(lib, eps_fd=1e-6, tol=1e-6):
+    """The sequence-parallel block (LayerNorm, then the sharded MLP) as one
+    function: finite differences of L = sum(dZ * Z) w.r.t. its input rows and the
+    LayerNorm parameters."""
+    f = []
+    rng = np.random.default_rng(503)
+    T, h, F, t, eps = 3, 4, 8, 2, 1e-5
+    Xi = rng.standard_normal((T, h)) * 2
+    g = rng.standard_normal(h)
+    be = rng.standard_normal(h)
+    _, A, a, B, b, dZ = _case(T, h, F, 504)
+
+    def loss():
+        xn = oracle.layernorm_forward(Xi, g, be, eps, lib=lib)["Y"]
+        return float(np.sum(dZ * oracle.forward(xn, A, a, B, b, t, lib=lib)["Z"]))
+
+    out = oracle.sp_forward_backward(Xi, g, be, eps, A, a, B, b, dZ, t, lib=lib)
+    for name, p, grad in (("X_in", Xi, out["dX_in"]), ("gamma", g, out["dgamma"]), ("beta", be, out["dbeta"])):
+        fd = np.empty_like(p)
+        flat = p.reshape(-1)
+        for i in range(flat.size):
+            old = flat[i]
+            flat[i] = old + eps_fd
+            lp = loss()
+            flat[i] = old - eps_fd
+            lm = loss()
+            flat[i] = old
+            fd.reshape(-1)[i] = (lp - lm) / (2 * eps_fd)
+        if _rel(grad, fd) > tol:
+            f.append("sequence-parallel block d%s vs finite differences: rel %.3e" % (name, _rel(grad, fd)))
+    return f
+
+
 ALL = [check_gelu_vs_erf, check_gelu_identities, check_gelu_prime_fd, check_forward_numpy,
        check_worked_example_t2, check_backward_fd, check_backward_partials,
-       check_closed_forms, check_slice_vs_full]
+       check_closed_forms, check_slice_vs_full, check_layernorm_numpy, check_layernorm_invariants,
+       check_layernorm_backward_fd, check_sp_composition_fd]
 
 
 def run_all(lib) -> list:

@@ -39,6 +39,14 @@ MUTANTS = {
                     "for (int64_t f = i * Fs; f < (i + 1) * Fs - 1; ++f) {\n                    const double yf = Yr[f];"),
     # the slice oracle reads the wrong token row
     "slice_row": ("const int64_t r = R[q];", "const int64_t r = (R[q] + 1) % T;"),
+    # LayerNorm with the sample variance (h - 1) instead of the population variance
+    "ln_sample_var": ("        v /= (double)h;\n        const double rs = 1.0 / sqrt(v + eps);\n        for (int64_t j = 0; j < h; ++j) Y[",
+                      "        v /= (double)(h - 1);\n        const double rs = 1.0 / sqrt(v + eps);\n        for (int64_t j = 0; j < h; ++j) Y["),
+    # LayerNorm backward without the projection onto xhat
+    "ln_bwd_drop_term": ("dX[r * h + j] = rstd * (dy[j] * gamma[j] - mg - xh * mgx);",
+                         "dX[r * h + j] = rstd * (dy[j] * gamma[j] - mg);"),
+    # dgamma without xhat
+    "ln_dgamma": ("sg += dY[r * h + j] * (X[r * h + j] - mu[r]) * rs[r];", "sg += dY[r * h + j];"),
 }
 
 
