@@ -220,10 +220,11 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def config_of(w, t, world, fwd_only=False, recompute=False):
+def config_of(w, t, world, fwd_only=False, recompute=False, sp=False):
     return {"workload": w.name, "tokens": w.tokens, "hidden": w.hidden, "ffn": w.ffn, "t": t,
             "pass": "forward" if fwd_only else "forward+backward",
             "activations_kept": "H only (recompute Y)" if recompute else "H and Y",
+            "layernorm_in_front": bool(sp),
             "dtype": w.dtype, "parallelism": "replicas x%d" % world if world > 1 else "single GPU",
             "l2": "inputs larger than L2 (A, B 537 MB each; ~3.2 GB touched per step)"
             if w.name == "h8192" else "per-step working set larger than L2"}
@@ -240,7 +241,10 @@ def run_ours(args, rank, world, local, w=None, quiet=False):
     host = inputs.for_workload(w, seed=args.seed + rank)
     d = {k: v.to(dev) for k, v in host.items()}
     T, h, F = w.tokens, w.hidden, w.ffn
-    ctx = tpmlp.Context(T, h, F, t, dt, device=dev, recompute=args.recompute)
+    ctx = tpmlp.Context(T, h, F, t, dt, device=dev, recompute=args.recompute, layernorm=args.sp)
+    if args.sp:  # LayerNorm parameters of the sequence-parallel block
+        gamma = torch.ones((h,), dtype=dt, device=dev)
+        beta = torch.zeros((h,), dtype=dt, device=dev)
     Z = torch.empty((T, h), dtype=dt, device=dev)
     g = {"dX": torch.empty((T, h), dtype=dt, device=dev), "dA": torch.empty((h, F), dtype=dt, device=dev),
          "da": torch.empty((F,), dtype=dt, device=dev), "dB": torch.empty((F, h), dtype=dt, device=dev),
@@ -248,9 +252,19 @@ def run_ours(args, rank, world, local, w=None, quiet=False):
     stream = torch.cuda.Stream(device=dev)
 
     def step():
+        if args.sp:
+            tpmlp.sp_forward(ctx, d["X"], gamma, beta, d["A"], d["a"], d["B"], d["b"], Z=Z, stream=stream)
+            if not args.fwd_only:
+                tpmlp.sp_backward(ctx, d["dZ"], stream=stream, dX_in=g["dX"], dgamma=sp_dg, dbeta=sp_db,
+                                  dA=g["dA"], da=g["da"], dB=g["dB"], db=g["db"])
+            return
         tpmlp.forward(ctx, d["X"], d["A"], d["a"], d["B"], d["b"], Z=Z, stream=stream)
         if not args.fwd_only:
             tpmlp.backward(ctx, d["dZ"], stream=stream, **g)
+
+    if args.sp:
+        sp_dg = torch.empty((h,), dtype=dt, device=dev)
+        sp_db = torch.empty((h,), dtype=dt, device=dev)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -321,10 +335,17 @@ def run_ours(args, rank, world, local, w=None, quiet=False):
             dX_in.copy_(hX, non_blocking=True)
             if not args.fwd_only:
                 dZ_in.copy_(hdZ, non_blocking=True)
-            tpmlp.forward(ctx, dX_in, d["A"], d["a"], d["B"], d["b"], Z=Z, stream=stream)
+            if args.sp:
+                tpmlp.sp_forward(ctx, dX_in, gamma, beta, d["A"], d["a"], d["B"], d["b"], Z=Z, stream=stream)
+            else:
+                tpmlp.forward(ctx, dX_in, d["A"], d["a"], d["B"], d["b"], Z=Z, stream=stream)
             oZ.copy_(Z, non_blocking=True)
             if not args.fwd_only:
-                tpmlp.backward(ctx, dZ_in, stream=stream, **g)
+                if args.sp:
+                    tpmlp.sp_backward(ctx, dZ_in, stream=stream, dX_in=g["dX"], dgamma=sp_dg, dbeta=sp_db,
+                                      dA=g["dA"], da=g["da"], dB=g["dB"], db=g["db"])
+                else:
+                    tpmlp.backward(ctx, dZ_in, stream=stream, **g)
                 odX.copy_(g["dX"], non_blocking=True)
                 oda.copy_(g["da"], non_blocking=True)
                 odb.copy_(g["db"], non_blocking=True)
@@ -354,7 +375,7 @@ def run_ours(args, rank, world, local, w=None, quiet=False):
     clk = clocks.summary()
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": config_of(w, t, world, args.fwd_only, args.recompute),
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": config_of(w, t, world, args.fwd_only, args.recompute, args.sp),
             "frac_of_peak": value / world / peaks["bf16_tflops_sustained"],
             "peak_tflops": peaks["bf16_tflops_sustained"], "peak_source": peak_src,
             "roofline": roof, "e2e": e2e, "gpu_launches": int(sum_over_ranks(launches, world)),
@@ -378,6 +399,8 @@ def main():
                     help="time tpmlp_forward alone (4*T*h*F FLOP per step)")
     ap.add_argument("--recompute", action="store_true",
                     help="activation recomputation: keep only H between forward and backward")
+    ap.add_argument("--sp", action="store_true",
+                    help="sequence-parallel block: LayerNorm in front of the MLP")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-tokens", type=int, default=32,

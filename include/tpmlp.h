@@ -82,7 +82,24 @@ typedef struct {
  * epilogue, which reads H anyway.  Activation memory kept between the passes is
  * T*F elements instead of 2*T*F.  saved->Y may then be NULL; saved->H is
  * required. */
-typedef enum { TPMLP_FLAG_RECOMPUTE = 1 } tpmlp_flags;
+/* TPMLP_FLAG_LAYERNORM: the block has LayerNorm in front, the sequence-parallel
+ * MLP of the report's section 4.3 (see tpmlp_sp_forward).  The workspace then
+ * also holds the MLP's input gradient (TPMLP_WS_DXN) for the LayerNorm backward. */
+typedef enum { TPMLP_FLAG_RECOMPUTE = 1, TPMLP_FLAG_LAYERNORM = 2 } tpmlp_flags;
+
+/* The LayerNorm in front of the sequence-parallel block.  All buffers are the
+ * caller's: X_in [T,h] (the token shards' rows side by side), gamma and beta [h],
+ * Xn [T,h] (the normalised rows, which the MLP takes as its X), mean and rstd [T]
+ * in fp32 (row statistics kept for the backward pass). */
+typedef struct {
+    const void *X_in;
+    const void *gamma;
+    const void *beta;
+    void *Xn;
+    float *mean;
+    float *rstd;
+    float eps;
+} tpmlp_layernorm;
 
 /* What the forward pass keeps for the backward pass.  The caller allocates H and
  * Y (T*F elements each, tpmlp_saved_bytes() in total); tpmlp_forward() fills in
@@ -102,7 +119,8 @@ typedef enum {
     TPMLP_WS_STATUS = 0,  /* uint32 status word (tpmlp_status), then a uint32 detail word */
     TPMLP_WS_PARTIALS = 1, /* fp32 column-sum partials */
     TPMLP_WS_DY = 2,       /* dY = (dZ B^T) * GeLU'(H), [T,F] in the shape's dtype */
-    TPMLP_WS_Y = 3         /* Y under TPMLP_FLAG_RECOMPUTE, [T,F]; absent (size 0) otherwise */
+    TPMLP_WS_Y = 3,        /* Y under TPMLP_FLAG_RECOMPUTE, [T,F]; absent (size 0) otherwise */
+    TPMLP_WS_DXN = 4       /* dXn, the MLP's input gradient, under TPMLP_FLAG_LAYERNORM, [T,h] */
 } tpmlp_ws_region;
 
 /* Human-readable name of a status code (static storage). */
@@ -157,6 +175,41 @@ tpmlp_status tpmlp_forward(const tpmlp_shape *shape, const void *X, const void *
 tpmlp_status tpmlp_backward(const tpmlp_shape *shape, const void *dZ, const tpmlp_saved *saved,
                             void *dX, void *dA, void *da, void *dB, void *db,
                             void *workspace, void *stream);
+
+/* LayerNorm of every row of ln->X_in into ln->Xn, keeping ln->mean and ln->rstd
+ * (the per-token-shard LayerNorm of the report's section 4.3; rows are
+ * independent, so all shards are one launch):
+ *   mu = mean_j x, var = mean_j (x - mu)^2, rstd = 1/sqrt(var + eps),
+ *   xn = (x - mu) * rstd * gamma + beta.
+ * Uses shape->tokens, hidden and dtype.  Errors: INVALID_ARG for a bad shape or
+ * a NULL pointer, or eps < 0; CUDA when a launch fails. */
+tpmlp_status tpmlp_ln_forward(const tpmlp_shape *shape, tpmlp_layernorm *ln, void *stream);
+
+/* Backward of tpmlp_ln_forward for the gradient dXn of its output:
+ *   dX_in = rstd * (g - mean_j g - xhat * mean_j(g * xhat)),  g = dXn * gamma,
+ *   dgamma = sum_rows dXn * xhat,  dbeta = sum_rows dXn   (fixed-order sums).
+ * The workspace is a tpmlp_workspace_bytes() buffer of a shape with
+ * TPMLP_FLAG_LAYERNORM (its column-sum partials are used). */
+tpmlp_status tpmlp_ln_backward(const tpmlp_shape *shape, const tpmlp_layernorm *ln, const void *dXn, void *dX_in,
+                               void *dgamma, void *dbeta, void *workspace, void *stream);
+
+/* The sequence-parallel MLP block (report section 4.3): LayerNorm of the input
+ * rows, then tpmlp_forward on the normalised rows.  Across t GPUs the
+ * normalised token shards would be all-gathered before the column-parallel GEMM
+ * and the output partials reduce-scattered back to token shards; with every
+ * shard on one GPU the gathered input is the Xn buffer itself and the shard fold
+ * already produces every output row.  shape->flags must include
+ * TPMLP_FLAG_LAYERNORM.  saved->X is set to ln->Xn. */
+tpmlp_status tpmlp_sp_forward(const tpmlp_shape *shape, tpmlp_layernorm *ln, const void *A, const void *a,
+                              const void *B, const void *b, void *Z, tpmlp_saved *saved, void *workspace,
+                              void *stream);
+
+/* Backward of tpmlp_sp_forward: tpmlp_backward into the workspace's dXn, then
+ * tpmlp_ln_backward.  Outputs dX_in [T,h], dgamma, dbeta [h] and the MLP's
+ * weight and bias gradients. */
+tpmlp_status tpmlp_sp_backward(const tpmlp_shape *shape, const tpmlp_layernorm *ln, const void *dZ,
+                               const tpmlp_saved *saved, void *dX_in, void *dgamma, void *dbeta, void *dA,
+                               void *da, void *dB, void *db, void *workspace, void *stream);
 
 /* Synchronises the stream, reads the workspace status word, clears it and
  * returns it (TPMLP_OK when no device-side error was recorded). */

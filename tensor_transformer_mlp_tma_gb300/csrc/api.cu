@@ -114,7 +114,7 @@ bool shape_valid(const tpmlp_shape *s) {
     if (s->t < 1 || s->t > 16 || s->ffn % s->t != 0) return false;
     if (s->dtype != TPMLP_F32 && s->dtype != TPMLP_BF16) return false;
     if (s->algo != TPMLP_ALGO_DEFAULT && s->algo != TPMLP_ALGO_SIMT) return false;
-    if ((s->flags & ~TPMLP_FLAG_RECOMPUTE) != 0) return false;
+    if ((s->flags & ~(TPMLP_FLAG_RECOMPUTE | TPMLP_FLAG_LAYERNORM)) != 0) return false;
     // int32 tile and grid arithmetic inside the kernels
     if (s->tokens > (1LL << 30) || s->hidden > (1LL << 30) || s->ffn > (1LL << 30)) return false;
     return true;
@@ -136,8 +136,10 @@ size_t partials_bytes(const tpmlp_shape *s) {
     int64_t n = tpmlp::colsum_chunks(T, h) * h;
     const int64_t p2 = tpmlp::colsum_chunks(T, F) * F;
     const int64_t p3 = (T + 31) / 32 * F;
+    const int64_t p4 = (s->flags & TPMLP_FLAG_LAYERNORM) ? tpmlp::ln_partial_floats(T, h) : 0;
     n = n > p2 ? n : p2;
     n = n > p3 ? n : p3;
+    n = n > p4 ? n : p4;
     return align_up(static_cast<size_t>(n) * sizeof(float), 1024);
 }
 
@@ -152,6 +154,15 @@ bool recompute(const tpmlp_shape *s) { return (s->flags & TPMLP_FLAG_RECOMPUTE) 
 size_t y_offset(const tpmlp_shape *s) { return dy_offset(s) + dy_bytes(s); }
 
 size_t y_bytes(const tpmlp_shape *s) { return recompute(s) ? dy_bytes(s) : 0; }
+
+bool layernorm(const tpmlp_shape *s) { return (s->flags & TPMLP_FLAG_LAYERNORM) != 0; }
+
+size_t dxn_offset(const tpmlp_shape *s) { return y_offset(s) + y_bytes(s); }
+
+size_t dxn_bytes(const tpmlp_shape *s) {
+    return layernorm(s) ? align_up(static_cast<size_t>(s->tokens) * static_cast<size_t>(s->hidden) * elt(s), 1024)
+                        : 0;
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned_elt(const void *p, size_t e) { return (reinterpret_cast<uintptr_t>(p) % e) == 0; }
@@ -288,7 +299,7 @@ size_t tpmlp_saved_bytes(const tpmlp_shape *s) {
 
 size_t tpmlp_workspace_bytes(const tpmlp_shape *s) {
     if (!shape_valid(s)) return 0;
-    return y_offset(s) + y_bytes(s);
+    return dxn_offset(s) + dxn_bytes(s);
 }
 
 size_t tpmlp_workspace_offset(const tpmlp_shape *s, int region) {
@@ -298,24 +309,52 @@ size_t tpmlp_workspace_offset(const tpmlp_shape *s, int region) {
         case TPMLP_WS_PARTIALS: return STATUS_BYTES;
         case TPMLP_WS_DY: return dy_offset(s);
         case TPMLP_WS_Y: return y_offset(s);
+        case TPMLP_WS_DXN: return dxn_offset(s);
     }
     return static_cast<size_t>(-1);
 }
 
-tpmlp_status tpmlp_forward(const tpmlp_shape *s, const void *X, const void *A, const void *a,
-                           const void *B, const void *b, void *Z, tpmlp_saved *saved,
-                           void *workspace, void *stream) {
-    tpmlp::g_last_error[0] = '\0';
+}  // extern "C"
+
+namespace {
+
+tpmlp_status validate_forward(const tpmlp_shape *s, const void *X, const void *A, const void *a, const void *B,
+                              const void *b, const void *Z, const tpmlp_saved *saved, const void *workspace) {
     if (!shape_valid(s)) return invalid("tpmlp_forward: invalid shape");
     if (!saved || !workspace) return invalid("tpmlp_forward: saved or workspace is NULL");
     if (!aligned16(workspace)) return TPMLP_ERR_UNSUPPORTED;
     // With no tokens the [T, .] tensors are empty and may have NULL data pointers.
     // Under recomputation H is the saved activation and Y lives in the workspace.
     const bool rec = recompute(s);
-    tpmlp_status rc = s->tokens == 0 ? check_ptrs(s, {A, a, B, b}, {X, Z, saved->Y, saved->H})
-                      : rec          ? check_ptrs(s, {X, A, a, B, b, Z, saved->H}, {saved->Y})
-                                     : check_ptrs(s, {X, A, a, B, b, Z, saved->Y}, {saved->H});
+    return s->tokens == 0 ? check_ptrs(s, {A, a, B, b}, {X, Z, saved->Y, saved->H})
+           : rec          ? check_ptrs(s, {X, A, a, B, b, Z, saved->H}, {saved->Y})
+                          : check_ptrs(s, {X, A, a, B, b, Z, saved->Y}, {saved->H});
+}
+
+tpmlp_status validate_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_saved *saved, const void *dX,
+                               const void *dA, const void *da, const void *dB, const void *db,
+                               const void *workspace) {
+    if (!shape_valid(s)) return invalid("tpmlp_backward: invalid shape");
+    if (!saved || !workspace) return invalid("tpmlp_backward: saved or workspace is NULL");
+    if (!aligned16(workspace)) return TPMLP_ERR_UNSUPPORTED;
+    const bool rec = recompute(s);
+    return s->tokens == 0
+               ? check_ptrs(s, {saved->A, saved->B, dA, da, dB, db}, {dZ, saved->X, saved->H, saved->Y, dX})
+           : rec ? check_ptrs(s, {dZ, saved->X, saved->A, saved->B, saved->H, dX, dA, da, dB, db}, {saved->Y})
+                 : check_ptrs(s, {dZ, saved->X, saved->A, saved->B, saved->H, saved->Y, dX, dA, da, dB, db}, {});
+}
+
+}  // namespace
+
+extern "C" {
+
+tpmlp_status tpmlp_forward(const tpmlp_shape *s, const void *X, const void *A, const void *a,
+                           const void *B, const void *b, void *Z, tpmlp_saved *saved,
+                           void *workspace, void *stream) {
+    tpmlp::g_last_error[0] = '\0';
+    tpmlp_status rc = validate_forward(s, X, A, a, B, b, Z, saved, workspace);
     if (rc != TPMLP_OK) return rc;
+    const bool rec = recompute(s);
     saved->X = X;
     saved->A = A;
     saved->B = B;
@@ -353,15 +392,9 @@ tpmlp_status tpmlp_forward(const tpmlp_shape *s, const void *X, const void *A, c
 tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_saved *saved, void *dX,
                             void *dA, void *da, void *dB, void *db, void *workspace, void *stream) {
     tpmlp::g_last_error[0] = '\0';
-    if (!shape_valid(s)) return invalid("tpmlp_backward: invalid shape");
-    if (!saved || !workspace) return invalid("tpmlp_backward: saved or workspace is NULL");
-    if (!aligned16(workspace)) return TPMLP_ERR_UNSUPPORTED;
-    const bool rec = recompute(s);
-    tpmlp_status rc =
-        s->tokens == 0 ? check_ptrs(s, {saved->A, saved->B, dA, da, dB, db}, {dZ, saved->X, saved->H, saved->Y, dX})
-        : rec ? check_ptrs(s, {dZ, saved->X, saved->A, saved->B, saved->H, dX, dA, da, dB, db}, {saved->Y})
-              : check_ptrs(s, {dZ, saved->X, saved->A, saved->B, saved->H, saved->Y, dX, dA, da, dB, db}, {});
+    tpmlp_status rc = validate_backward(s, dZ, saved, dX, dA, da, dB, db, workspace);
     if (rc != TPMLP_OK) return rc;
+    const bool rec = recompute(s);
     const int64_t T = s->tokens, h = s->hidden, F = s->ffn;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (T == 0) {
@@ -440,6 +473,84 @@ tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_sa
     pick_raster(g6);
     e = gemm(s, "bwd_dX_shard_fold", tpmlp::EPI_FOLD, g6, sms, st);
     return from_cuda(e);
+}
+
+tpmlp_status tpmlp_ln_forward(const tpmlp_shape *s, tpmlp_layernorm *ln, void *stream) {
+    tpmlp::g_last_error[0] = '\0';
+    if (!shape_valid(s) || !ln) return invalid("tpmlp_ln_forward: invalid shape or NULL layernorm");
+    if (!(ln->eps >= 0.0f)) return invalid("tpmlp_ln_forward: eps must be >= 0");
+    const int64_t T = s->tokens;
+    tpmlp_status rc = T > 0 ? check_ptrs(s, {ln->X_in, ln->gamma, ln->beta, ln->Xn}, {})
+                            : check_ptrs(s, {ln->gamma, ln->beta}, {ln->X_in, ln->Xn});
+    if (rc != TPMLP_OK) return rc;
+    if (T > 0 && (!ln->mean || !ln->rstd)) return invalid("tpmlp_ln_forward: NULL mean or rstd");
+    if (T == 0) return TPMLP_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    tpmlp::LnArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.rows = T, a.h = s->hidden, a.eps = ln->eps;
+    a.x = ln->X_in, a.gamma = ln->gamma, a.beta = ln->beta, a.y = ln->Xn, a.mean = ln->mean, a.rstd = ln->rstd;
+    Timed timed("ln_forward", st);
+    cudaError_t e = tpmlp::launch_ln_forward(s->dtype == TPMLP_BF16, a, st);
+    if (e == cudaSuccess) g_launches.fetch_add(1);
+    return from_cuda(e);
+}
+
+tpmlp_status tpmlp_ln_backward(const tpmlp_shape *s, const tpmlp_layernorm *ln, const void *dXn, void *dX_in,
+                               void *dgamma, void *dbeta, void *workspace, void *stream) {
+    tpmlp::g_last_error[0] = '\0';
+    if (!shape_valid(s) || !ln || !workspace) return invalid("tpmlp_ln_backward: invalid shape or NULL argument");
+    if (!layernorm(s)) return invalid("tpmlp_ln_backward: the shape needs TPMLP_FLAG_LAYERNORM (workspace size)");
+    const int64_t T = s->tokens;
+    tpmlp_status rc = T > 0 ? check_ptrs(s, {dXn, ln->X_in, ln->gamma, dX_in, dgamma, dbeta}, {})
+                            : check_ptrs(s, {ln->gamma, dgamma, dbeta}, {dXn, ln->X_in, dX_in});
+    if (rc != TPMLP_OK) return rc;
+    if (T > 0 && (!ln->mean || !ln->rstd)) return invalid("tpmlp_ln_backward: NULL mean or rstd");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    tpmlp::LnArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.rows = T, a.h = s->hidden, a.eps = ln->eps;
+    a.x = ln->X_in, a.gamma = ln->gamma, a.mean = ln->mean, a.rstd = ln->rstd;
+    a.dy = dXn, a.dx = dX_in, a.dgamma = dgamma, a.dbeta = dbeta;
+    a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + STATUS_BYTES);
+    Timed timed("ln_backward", st);
+    int n = 0;
+    cudaError_t e = tpmlp::launch_ln_backward(s->dtype == TPMLP_BF16, a, st, &n);
+    g_launches.fetch_add(static_cast<uint64_t>(n));
+    return from_cuda(e);
+}
+
+tpmlp_status tpmlp_sp_forward(const tpmlp_shape *s, tpmlp_layernorm *ln, const void *A, const void *a,
+                              const void *B, const void *b, void *Z, tpmlp_saved *saved, void *workspace,
+                              void *stream) {
+    if (!shape_valid(s) || !ln) return invalid("tpmlp_sp_forward: invalid shape or NULL layernorm");
+    if (!layernorm(s)) return invalid("tpmlp_sp_forward: the shape needs TPMLP_FLAG_LAYERNORM");
+    // Validate the whole call before the first launch.
+    tpmlp_status rc = validate_forward(s, ln->Xn, A, a, B, b, Z, saved, workspace);
+    if (rc != TPMLP_OK) return rc;
+    if (s->tokens > 0 && (!ln->X_in || !ln->mean || !ln->rstd)) return invalid("tpmlp_sp_forward: NULL layernorm buffer");
+    rc = tpmlp_ln_forward(s, ln, stream);
+    if (rc != TPMLP_OK) return rc;
+    return tpmlp_forward(s, ln->Xn, A, a, B, b, Z, saved, workspace, stream);
+}
+
+tpmlp_status tpmlp_sp_backward(const tpmlp_shape *s, const tpmlp_layernorm *ln, const void *dZ,
+                               const tpmlp_saved *saved, void *dX_in, void *dgamma, void *dbeta, void *dA,
+                               void *da, void *dB, void *db, void *workspace, void *stream) {
+    if (!shape_valid(s) || !ln || !workspace) return invalid("tpmlp_sp_backward: invalid shape or NULL argument");
+    if (!layernorm(s)) return invalid("tpmlp_sp_backward: the shape needs TPMLP_FLAG_LAYERNORM");
+    void *dXn = static_cast<uint8_t *>(workspace) + dxn_offset(s);
+    void *dXn_or_null = s->tokens > 0 ? dXn : nullptr;
+    // Validate the whole call before the first launch.
+    tpmlp_status rc = validate_backward(s, dZ, saved, dXn_or_null, dA, da, dB, db, workspace);
+    if (rc != TPMLP_OK) return rc;
+    rc = s->tokens > 0 ? check_ptrs(s, {ln->X_in, ln->gamma, dX_in, dgamma, dbeta}, {})
+                       : check_ptrs(s, {ln->gamma, dgamma, dbeta}, {ln->X_in, dX_in});
+    if (rc != TPMLP_OK) return rc;
+    if (s->tokens > 0 && (!ln->mean || !ln->rstd)) return invalid("tpmlp_sp_backward: NULL mean or rstd");
+    rc = tpmlp_backward(s, dZ, saved, dXn_or_null, dA, da, dB, db, workspace, stream);
+    if (rc != TPMLP_OK) return rc;
+    return tpmlp_ln_backward(s, ln, dXn, dX_in, dgamma, dbeta, workspace, stream);
 }
 
 tpmlp_status tpmlp_check_device_status(void *workspace, void *stream) {

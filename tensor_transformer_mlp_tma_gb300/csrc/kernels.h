@@ -60,6 +60,26 @@ cudaError_t launch_colsum_final(bool is_bf16, const float *partials, int64_t chu
 // A kernel that waits on a barrier nothing arrives on and reports the timeout.
 cudaError_t launch_timeout_probe(uint32_t *status, uint64_t wait_ns, cudaStream_t st);
 
+// LayerNorm over the rows of a row-major [rows, h] matrix (fp32 statistics).
+struct LnArgs {
+    int64_t rows, h;
+    float eps;
+    const void *x;      // input rows
+    const void *gamma;  // [h]
+    const void *beta;   // [h] (forward)
+    void *y;            // forward output
+    float *mean;        // [rows]
+    float *rstd;        // [rows]
+    const void *dy;     // backward: gradient w.r.t. the output
+    void *dx;           // backward: gradient w.r.t. the input
+    void *dgamma;       // [h]
+    void *dbeta;        // [h]
+    float *partials;    // backward: ln_partial_floats(rows, h) floats of scratch
+};
+int64_t ln_partial_floats(int64_t rows, int64_t h);
+cudaError_t launch_ln_forward(bool is_bf16, const LnArgs &a, cudaStream_t st);
+cudaError_t launch_ln_backward(bool is_bf16, const LnArgs &a, cudaStream_t st, int *launches);
+
 // Records a description of the last failure of this host thread (read back by
 // tpmlp_last_error()).
 void set_last_error(const char *fmt, ...);

@@ -18,8 +18,8 @@ LIB_PATH = os.path.join(_HERE, "libtpmlp.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(6)
 F32, BF16 = 0, 1
 ALGO_DEFAULT, ALGO_SIMT = 0, 1
-WS_STATUS, WS_PARTIALS, WS_DY, WS_Y = 0, 1, 2, 3
-FLAG_RECOMPUTE = 1
+WS_STATUS, WS_PARTIALS, WS_DY, WS_Y, WS_DXN = 0, 1, 2, 3, 4
+FLAG_RECOMPUTE, FLAG_LAYERNORM = 1, 2
 
 _DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -33,6 +33,12 @@ class Shape(ctypes.Structure):
 class Saved(ctypes.Structure):
     _fields_ = [("X", ctypes.c_void_p), ("A", ctypes.c_void_p), ("B", ctypes.c_void_p),
                 ("H", ctypes.c_void_p), ("Y", ctypes.c_void_p)]
+
+
+class LayerNorm(ctypes.Structure):
+    _fields_ = [("X_in", ctypes.c_void_p), ("gamma", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+                ("Xn", ctypes.c_void_p), ("mean", ctypes.c_void_p), ("rstd", ctypes.c_void_p),
+                ("eps", ctypes.c_float)]
 
 
 class TpmlpError(RuntimeError):
@@ -59,6 +65,11 @@ def _load():
         "tpmlp_workspace_offset": (sz, [SP, i32]),
         "tpmlp_forward": (i32, [SP, vp, vp, vp, vp, vp, vp, ctypes.POINTER(Saved), vp, vp]),
         "tpmlp_backward": (i32, [SP, vp, ctypes.POINTER(Saved), vp, vp, vp, vp, vp, vp, vp]),
+        "tpmlp_ln_forward": (i32, [SP, ctypes.POINTER(LayerNorm), vp]),
+        "tpmlp_ln_backward": (i32, [SP, ctypes.POINTER(LayerNorm), vp, vp, vp, vp, vp, vp]),
+        "tpmlp_sp_forward": (i32, [SP, ctypes.POINTER(LayerNorm), vp, vp, vp, vp, vp, ctypes.POINTER(Saved),
+                                   vp, vp]),
+        "tpmlp_sp_backward": (i32, [SP, ctypes.POINTER(LayerNorm), vp, ctypes.POINTER(Saved)] + [vp] * 9),
         "tpmlp_check_device_status": (i32, [vp, vp]),
         "tpmlp_set_wait_limit_ns": (None, [u64]),
         "tpmlp_debug_timeout_probe": (i32, [vp, u64, vp]),
@@ -148,10 +159,13 @@ class Context:
     workspace, plus the ctypes shape and saved-activation records."""
 
     def __init__(self, tokens, hidden, ffn, t, dtype, algo=ALGO_DEFAULT, device=None, keep_H=True,
-                 recompute=False):
+                 recompute=False, layernorm=False, eps=1e-5):
         """recompute=True keeps only H between the passes (TPMLP_FLAG_RECOMPUTE):
-        Y then lives in the workspace and is rebuilt by the backward pass."""
-        self.shape = make_shape(tokens, hidden, ffn, t, dtype, algo, FLAG_RECOMPUTE if recompute else 0)
+        Y then lives in the workspace and is rebuilt by the backward pass.
+        layernorm=True adds the LayerNorm in front (the sequence-parallel block,
+        TPMLP_FLAG_LAYERNORM): Xn, mean and rstd buffers are allocated here."""
+        flags = (FLAG_RECOMPUTE if recompute else 0) | (FLAG_LAYERNORM if layernorm else 0)
+        self.shape = make_shape(tokens, hidden, ffn, t, dtype, algo, flags)
         if saved_bytes(self.shape) == 0 and tokens > 0:
             raise ValueError("invalid shape (tokens=%d hidden=%d ffn=%d t=%d)" % (tokens, hidden, ffn, t))
         self.dtype = dtype
@@ -162,12 +176,24 @@ class Context:
         self.workspace = new_workspace(self.shape, dev)
         self.saved = Saved(None, None, None, _ptr(self.H), _ptr(self._Y))
         self._keep = []
+        if layernorm:
+            self.Xn = torch.empty((tokens, hidden), dtype=dtype, device=dev)
+            self.mean = torch.empty((tokens,), dtype=torch.float32, device=dev)
+            self.rstd = torch.empty((tokens,), dtype=torch.float32, device=dev)
+            self.ln = LayerNorm(None, None, None, _ptr(self.Xn), _ptr(self.mean), _ptr(self.rstd), float(eps))
 
-    def _ws_view(self, region):
-        T, F = self.shape.tokens, self.shape.ffn
+    def _ws_view(self, region, cols=None):
+        T = self.shape.tokens
+        C = self.shape.ffn if cols is None else cols
         off = workspace_offset(self.shape, region)
         esz = 2 if self.dtype == torch.bfloat16 else 4
-        return self.workspace[off:off + T * F * esz].view(self.dtype).view(T, F)
+        return self.workspace[off:off + T * C * esz].view(self.dtype).view(T, C)
+
+    @property
+    def dXn(self) -> torch.Tensor:
+        """The MLP's input gradient of the last sequence-parallel backward (the
+        LayerNorm's output gradient; a view into the workspace)."""
+        return self._ws_view(WS_DXN, self.shape.hidden)
 
     @property
     def Y(self) -> torch.Tensor:
@@ -215,6 +241,65 @@ def backward(ctx: Context, dZ, dX=None, dA=None, da=None, dB=None, db=None, stre
                             _ptr(ctx.workspace), _stream(stream))
     _check(st, "tpmlp_backward")
     return out
+
+
+def sp_forward(ctx: Context, X_in, gamma, beta, A, a, B, b, Z=None, stream=None):
+    """Sequence-parallel block forward: Xn = LayerNorm(X_in), then the MLP on Xn."""
+    s = ctx.shape
+    T, h, F = s.tokens, s.hidden, s.ffn
+    for x, n, shp in ((X_in, "X_in", (T, h)), (gamma, "gamma", (h,)), (beta, "beta", (h,)), (A, "A", (h, F)),
+                      (a, "a", (F,)), (B, "B", (F, h)), (b, "b", (h,))):
+        _need(x, n, ctx.dtype, shp)
+    if Z is None:
+        Z = torch.empty((T, h), dtype=ctx.dtype, device=X_in.device)
+    _need(Z, "Z", ctx.dtype, (T, h))
+    ctx.ln.X_in, ctx.ln.gamma, ctx.ln.beta = _ptr(X_in), _ptr(gamma), _ptr(beta)
+    ctx._keep = [X_in, gamma, beta, A, B]
+    st = lib.tpmlp_sp_forward(ctypes.byref(s), ctypes.byref(ctx.ln), _ptr(A), _ptr(a), _ptr(B), _ptr(b), _ptr(Z),
+                              ctypes.byref(ctx.saved), _ptr(ctx.workspace), _stream(stream))
+    _check(st, "tpmlp_sp_forward")
+    return Z
+
+
+def sp_backward(ctx: Context, dZ, stream=None, **outs):
+    """Sequence-parallel block backward: dX_in, dgamma, dbeta and the MLP's
+    weight and bias gradients."""
+    s = ctx.shape
+    T, h, F = s.tokens, s.hidden, s.ffn
+    _need(dZ, "dZ", ctx.dtype, (T, h))
+    out = {}
+    for name, shp in (("dX_in", (T, h)), ("dgamma", (h,)), ("dbeta", (h,)), ("dA", (h, F)), ("da", (F,)),
+                      ("dB", (F, h)), ("db", (h,))):
+        val = outs.get(name)
+        if val is None:
+            val = torch.empty(shp, dtype=ctx.dtype, device=dZ.device)
+        _need(val, name, ctx.dtype, shp)
+        out[name] = val
+    st = lib.tpmlp_sp_backward(ctypes.byref(s), ctypes.byref(ctx.ln), _ptr(dZ), ctypes.byref(ctx.saved),
+                               *(_ptr(out[k]) for k in ("dX_in", "dgamma", "dbeta", "dA", "da", "dB", "db")),
+                               _ptr(ctx.workspace), _stream(stream))
+    _check(st, "tpmlp_sp_backward")
+    return out
+
+
+def ln_forward(ctx: Context, X_in, gamma, beta, stream=None):
+    """LayerNorm alone (the block's first step): fills ctx.Xn, ctx.mean, ctx.rstd."""
+    ctx.ln.X_in, ctx.ln.gamma, ctx.ln.beta = _ptr(X_in), _ptr(gamma), _ptr(beta)
+    ctx._keep = [X_in, gamma, beta]
+    _check(lib.tpmlp_ln_forward(ctypes.byref(ctx.shape), ctypes.byref(ctx.ln), _stream(stream)), "tpmlp_ln_forward")
+    return ctx.Xn
+
+
+def ln_backward(ctx: Context, dXn, stream=None):
+    """LayerNorm backward alone for the gradient dXn of its output."""
+    T, h = ctx.shape.tokens, ctx.shape.hidden
+    dX_in = torch.empty((T, h), dtype=ctx.dtype, device=dXn.device)
+    dg = torch.empty((h,), dtype=ctx.dtype, device=dXn.device)
+    dbt = torch.empty((h,), dtype=ctx.dtype, device=dXn.device)
+    st = lib.tpmlp_ln_backward(ctypes.byref(ctx.shape), ctypes.byref(ctx.ln), _ptr(dXn), _ptr(dX_in), _ptr(dg),
+                               _ptr(dbt), _ptr(ctx.workspace), _stream(stream))
+    _check(st, "tpmlp_ln_backward")
+    return {"dX_in": dX_in, "dgamma": dg, "dbeta": dbt}
 
 
 def check_device_status(ctx_or_ws, stream=None) -> int:

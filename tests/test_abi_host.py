@@ -64,7 +64,7 @@ def test_size_queries(tp):
                 tp.make_shape(128, 256, 1024, 0, tp.BF16),   # t < 1
                 tp.Shape(128, 256, 1024, 2, 7, 0, 0),        # dtype
                 tp.Shape(128, 256, 1024, 2, 1, 5, 0),        # algo
-                tp.Shape(128, 256, 1024, 2, 1, 0, 2)):       # unknown flag
+                tp.Shape(128, 256, 1024, 2, 1, 0, 4)):       # unknown flag
         assert tp.saved_bytes(bad) == 0
         assert tp.workspace_bytes(bad) == 0
     # recomputation keeps H only and moves Y into the workspace
