@@ -41,12 +41,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, with the hash of the kernel source they were taken at.  A kernel whose
 # source has changed since reports traffic null.
 NCU_TRAFFIC = {  # profiles/dram_traffic_h8192_gemms.md (h8192 workload)
-    "fc1_bias_gelu": (2.40e9 + 0.51857e9, "6993b5289148"),
-    "fc2_shard_fold": (2.42e9 + 0.07220e9, "6993b5289148"),
-    "bwd_dY_dgelu": (2.93e9 + 0.25805e9, "6993b5289148"),
-    "bwd_dB": (0.94146e9 + 0.51235e9, "6993b5289148"),
-    "bwd_dA": (0.89537e9 + 0.51297e9, "6993b5289148"),
-    "bwd_dX_shard_fold": (2.42e9 + 0.06982e9, "6993b5289148"),
+    "fc1_bias_gelu": (2.02e9 + 0.51988e9, "1f33cdadddf3"),
+    "fc2_shard_fold": (2.58e9 + 0.10298e9, "1f33cdadddf3"),
+    "bwd_dY_dgelu": (2.60e9 + 0.27456e9, "1f33cdadddf3"),
+    "bwd_dB": (1.14e9 + 0.51904e9, "1f33cdadddf3"),
+    "bwd_dA": (1.19e9 + 0.51934e9, "1f33cdadddf3"),
+    "bwd_dX_shard_fold": (2.55e9 + 0.09327e9, "1f33cdadddf3"),
 }
 
 
