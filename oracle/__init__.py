@@ -74,6 +74,10 @@ def load(path: str | None = None):
         lib.oracle_layernorm_forward.argtypes = [_I64, _I64, _DP, _DP, _DP, ctypes.c_double, _DP, _DP, _DP]
         lib.oracle_layernorm_backward.restype = ctypes.c_int
         lib.oracle_layernorm_backward.argtypes = [_I64, _I64, _DP, _DP, _DP, ctypes.c_double, _DP, _DP, _DP]
+        lib.oracle_attn_forward.restype = ctypes.c_int
+        lib.oracle_attn_forward.argtypes = [_I64, _I64, _I64, _I64, _I32] + [_DP] * 9
+        lib.oracle_attn_backward.restype = ctypes.c_int
+        lib.oracle_attn_backward.argtypes = [_I64, _I64, _I64, _I64, _I32] + [_DP] * 12
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         if path is None:
@@ -226,6 +230,45 @@ def sp_forward_backward(X_in, gamma, beta, eps, A, a, B, b, dZ, t: int, lib=None
     out.update({"Xn": ln["Y"], "mean": ln["mean"], "rstd": ln["rstd"], "dX_in": lb["dX"],
                 "dgamma": lb["dgamma"], "dbeta": lb["dbeta"]})
     return out
+
+
+def attn_forward(X, Wqkv, bqkv, Wo, bo, nb: int, heads: int, t: int, lib=None) -> dict:
+    """Tensor-parallel causal self-attention forward in fp64: QKV [T,3h] (shard-
+    major columns [Q_i | K_i | V_i]), P [nb, heads, S, S], O [T,h], Z [T,h]."""
+    lib = lib or load()
+    X, Wqkv, bqkv, Wo, bo = (_f64(v) for v in (X, Wqkv, bqkv, Wo, bo))
+    T, h = X.shape
+    S = T // nb
+    QKV = np.empty((T, 3 * h))
+    P = np.empty((nb, heads, S, S))
+    O = np.empty((T, h))
+    Z = np.empty((T, h))
+    rc = lib.oracle_attn_forward(nb, S, h, heads, t, _p(X), _p(Wqkv), _p(bqkv), _p(Wo), _p(bo),
+                                 _p(QKV), _p(P), _p(O), _p(Z))
+    if rc != 0:
+        raise ValueError("oracle_attn_forward rejected the shape (rc=%d)" % rc)
+    return {"QKV": QKV, "P": P, "O": O, "Z": Z}
+
+
+def attn_backward(X, Wqkv, Wo, QKV, P, O, dZ, nb: int, heads: int, t: int, lib=None) -> dict:
+    """dX, dWqkv, dbqkv, dWo, dbo of the attention block in fp64."""
+    lib = lib or load()
+    X, Wqkv, Wo, QKV, P, O, dZ = (_f64(v) for v in (X, Wqkv, Wo, QKV, P, O, dZ))
+    T, h = X.shape
+    S = T // nb
+    out = {"dX": np.empty((T, h)), "dWqkv": np.empty((h, 3 * h)), "dbqkv": np.empty(3 * h),
+           "dWo": np.empty((h, h)), "dbo": np.empty(h)}
+    rc = lib.oracle_attn_backward(nb, S, h, heads, t, _p(X), _p(Wqkv), _p(Wo), _p(QKV), _p(P), _p(O), _p(dZ),
+                                  *(_p(out[k]) for k in ("dX", "dWqkv", "dbqkv", "dWo", "dbo")))
+    if rc != 0:
+        raise ValueError("oracle_attn_backward failed (rc=%d)" % rc)
+    return out
+
+
+def attn_forward_backward(X, Wqkv, bqkv, Wo, bo, dZ, nb: int, heads: int, t: int, lib=None) -> dict:
+    fw = attn_forward(X, Wqkv, bqkv, Wo, bo, nb, heads, t, lib=lib)
+    fw.update(attn_backward(X, Wqkv, Wo, fw["QKV"], fw["P"], fw["O"], dZ, nb, heads, t, lib=lib))
+    return fw
 
 
 def num_threads(lib=None) -> int:

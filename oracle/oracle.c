@@ -449,6 +449,210 @@ int oracle_layernorm_backward(int64_t T, int64_t h, const double *dY, const doub
     return 0;
 }
 
+/* ---- tensor-parallel self-attention ---------------------------------------------
+ * The report's section 4.1 splits self-attention the same way as the MLP: the
+ * heads are divided among the t shards, the QKV projection is split by columns
+ * (each shard computes the Q, K and V of its own heads from the replicated
+ * input) and the output projection by rows, whose t partial products are summed
+ * (the all-reduce).  The attention of each head is the textbook causal scaled
+ * dot-product attention (Vaswani et al., 2017):
+ *   S = Q K^T / sqrt(d) (row r attends to positions c <= r),  P = softmax_row(S),
+ *   O = P V.
+ * Layout.  X[T,h] with T = nb*S tokens (nb sequences of S); heads of width
+ * d = h/heads; hpt = heads/t heads per shard.  QKV = X Wqkv + bqkv is [T,3h]
+ * with shard-major columns: shard i owns [i*3h/t, (i+1)*3h/t) = [Q_i | K_i | V_i],
+ * each h/t wide, head j of the shard at offset j*d inside each.  Global head
+ * g = i*hpt + j writes O columns [g*d, (g+1)*d), so shard i's heads are O's
+ * columns [i*h/t, (i+1)*h/t), which are the rows of Wo[h,h] the shard owns.
+ * P is [nb, heads, S, S]. */
+static int64_t qkv_col(int64_t h, int32_t t, int64_t d, int64_t hpt, int64_t g, int which) {
+    const int64_t i = g / hpt, j = g % hpt;
+    return i * (3 * h / t) + (int64_t)which * (h / t) + j * d;
+}
+
+static int bad_attn(int64_t nb, int64_t S, int64_t h, int64_t heads, int32_t t) {
+    return nb < 0 || S <= 0 || h <= 0 || heads <= 0 || t < 1 || h % heads != 0 || heads % t != 0;
+}
+
+int oracle_attn_forward(int64_t nb, int64_t S, int64_t h, int64_t heads, int32_t t,
+                        const double *X, const double *Wqkv, const double *bqkv,
+                        const double *Wo, const double *bo,
+                        double *QKV, double *P, double *O, double *Z) {
+    if (bad_attn(nb, S, h, heads, t)) return -1;
+    const int64_t T = nb * S, d = h / heads, hpt = heads / t, H3 = 3 * h, hs = h / t;
+    /* column-parallel QKV projection of all shards */
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T; ++r) {
+        double *q = QKV + r * H3;
+        for (int64_t c = 0; c < H3; ++c) q[c] = bqkv[c];
+        for (int64_t k = 0; k < h; ++k) {
+            const double x = X[r * h + k];
+            const double *w = Wqkv + k * H3;
+            for (int64_t c = 0; c < H3; ++c) q[c] += x * w[c];
+        }
+    }
+    /* causal attention of every head of every sequence */
+    const double scale = 1.0 / sqrt((double)d);
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t b = 0; b < nb; ++b)
+        for (int64_t g = 0; g < heads; ++g) {
+            const int64_t qc = qkv_col(h, t, d, hpt, g, 0), kc = qkv_col(h, t, d, hpt, g, 1),
+                          vc = qkv_col(h, t, d, hpt, g, 2);
+            double *Pg = P + (b * heads + g) * S * S;
+            for (int64_t r = 0; r < S; ++r) {
+                const double *qr = QKV + (b * S + r) * H3 + qc;
+                const int64_t last = r; /* causal: row r sees positions 0..r */
+                double mx = -INFINITY;
+                for (int64_t c = 0; c <= last; ++c) {
+                    const double *kr = QKV + (b * S + c) * H3 + kc;
+                    double sc = 0.0;
+                    for (int64_t e = 0; e < d; ++e) sc += qr[e] * kr[e];
+                    Pg[r * S + c] = sc * scale;
+                    if (Pg[r * S + c] > mx) mx = Pg[r * S + c];
+                }
+                double den = 0.0;
+                for (int64_t c = 0; c <= last; ++c) {
+                    Pg[r * S + c] = exp(Pg[r * S + c] - mx);
+                    den += Pg[r * S + c];
+                }
+                for (int64_t c = 0; c <= last; ++c) Pg[r * S + c] /= den;
+                for (int64_t c = last + 1; c < S; ++c) Pg[r * S + c] = 0.0;
+                double *orow = O + (b * S + r) * h + g * d;
+                for (int64_t e = 0; e < d; ++e) orow[e] = 0.0;
+                for (int64_t c = 0; c <= last; ++c) {
+                    const double pc = Pg[r * S + c];
+                    const double *vr = QKV + (b * S + c) * H3 + vc;
+                    for (int64_t e = 0; e < d; ++e) orow[e] += pc * vr[e];
+                }
+            }
+        }
+    /* row-parallel output projection, shard partials summed in order, + bo */
+#pragma omp parallel
+    {
+        double *part = (double *)malloc(sizeof(double) * (size_t)h);
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < T; ++r) {
+            if (!part) continue;
+            for (int64_t c = 0; c < h; ++c) Z[r * h + c] = 0.0;
+            for (int32_t i = 0; i < t; ++i) {
+                for (int64_t c = 0; c < h; ++c) part[c] = 0.0;
+                for (int64_t k = i * hs; k < (i + 1) * hs; ++k) {
+                    const double o = O[r * h + k];
+                    const double *w = Wo + k * h;
+                    for (int64_t c = 0; c < h; ++c) part[c] += o * w[c];
+                }
+                for (int64_t c = 0; c < h; ++c) Z[r * h + c] += part[c];
+            }
+            for (int64_t c = 0; c < h; ++c) Z[r * h + c] += bo[c];
+        }
+        free(part);
+    }
+    return 0;
+}
+
+/* Backward for L = sum(dZ * Z): the chain rule through the output projection,
+ * the attention of each head and the QKV projection:
+ *   dbo = 1^T dZ, dO = dZ Wo^T, dWo = O^T dZ;
+ *   per head: dV = P^T dO, dP = dO V^T, dS = P * (dP - rowsum(dP * P)),
+ *             dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d);
+ *   dbqkv = 1^T dQKV, dWqkv = X^T dQKV, dX = sum_i dQKV[:, shard i] Wqkv[:, shard i]^T. */
+int oracle_attn_backward(int64_t nb, int64_t S, int64_t h, int64_t heads, int32_t t,
+                         const double *X, const double *Wqkv, const double *Wo,
+                         const double *QKV, const double *P, const double *O, const double *dZ,
+                         double *dX, double *dWqkv, double *dbqkv, double *dWo, double *dbo) {
+    if (bad_attn(nb, S, h, heads, t)) return -1;
+    const int64_t T = nb * S, d = h / heads, hpt = heads / t, H3 = 3 * h, hs3 = H3 / t;
+    double *dO = (double *)malloc(sizeof(double) * (size_t)(T * h + 1));
+    double *dQKV = (double *)calloc((size_t)(T * H3 + 1), sizeof(double));
+    if (!dO || !dQKV) {
+        free(dO);
+        free(dQKV);
+        return -2;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < h; ++c) {
+        double sb = 0.0;
+        for (int64_t r = 0; r < T; ++r) sb += dZ[r * h + c];
+        dbo[c] = sb;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T; ++r)
+        for (int64_t k = 0; k < h; ++k) {
+            double s = 0.0;
+            for (int64_t c = 0; c < h; ++c) s += dZ[r * h + c] * Wo[k * h + c];
+            dO[r * h + k] = s;
+        }
+#pragma omp parallel for schedule(static)
+    for (int64_t k = 0; k < h; ++k)
+        for (int64_t c = 0; c < h; ++c) {
+            double s = 0.0;
+            for (int64_t r = 0; r < T; ++r) s += O[r * h + k] * dZ[r * h + c];
+            dWo[k * h + c] = s;
+        }
+    const double scale = 1.0 / sqrt((double)d);
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t b = 0; b < nb; ++b)
+        for (int64_t g = 0; g < heads; ++g) {
+            const int64_t qc = qkv_col(h, t, d, hpt, g, 0), kc = qkv_col(h, t, d, hpt, g, 1),
+                          vc = qkv_col(h, t, d, hpt, g, 2);
+            const double *Pg = P + (b * heads + g) * S * S;
+            double *dP = (double *)malloc(sizeof(double) * (size_t)S);
+            if (!dP) continue;
+            for (int64_t r = 0; r < S; ++r) {
+                const double *dor = dO + (b * S + r) * h + g * d;
+                double D = 0.0;
+                for (int64_t c = 0; c <= r; ++c) {
+                    const double *vr = QKV + (b * S + c) * H3 + vc;
+                    double s = 0.0;
+                    for (int64_t e = 0; e < d; ++e) s += dor[e] * vr[e];
+                    dP[c] = s;
+                    D += s * Pg[r * S + c];
+                }
+                for (int64_t c = 0; c <= r; ++c) {
+                    const double ds = Pg[r * S + c] * (dP[c] - D) * scale;
+                    const double *qr = QKV + (b * S + r) * H3 + qc;
+                    const double *kr = QKV + (b * S + c) * H3 + kc;
+                    double *dq = dQKV + (b * S + r) * H3 + qc;
+                    double *dk = dQKV + (b * S + c) * H3 + kc;
+                    double *dv = dQKV + (b * S + c) * H3 + vc;
+                    for (int64_t e = 0; e < d; ++e) {
+                        dq[e] += ds * kr[e];
+                        dk[e] += ds * qr[e];
+                        dv[e] += Pg[r * S + c] * dor[e];
+                    }
+                }
+            }
+            free(dP);
+        }
+#pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < H3; ++c) {
+        double sb = 0.0;
+        for (int64_t r = 0; r < T; ++r) sb += dQKV[r * H3 + c];
+        dbqkv[c] = sb;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t k = 0; k < h; ++k)
+        for (int64_t c = 0; c < H3; ++c) {
+            double s = 0.0;
+            for (int64_t r = 0; r < T; ++r) s += X[r * h + k] * dQKV[r * H3 + c];
+            dWqkv[k * H3 + c] = s;
+        }
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T; ++r)
+        for (int64_t k = 0; k < h; ++k) {
+            double sum = 0.0;
+            for (int32_t i = 0; i < t; ++i) {
+                double p = 0.0;
+                for (int64_t c = i * hs3; c < (i + 1) * hs3; ++c) p += dQKV[r * H3 + c] * Wqkv[k * H3 + c];
+                sum += p;
+            }
+            dX[r * h + k] = sum;
+        }
+    free(dO);
+    free(dQKV);
+    return 0;
+}
+
 /* Number of OpenMP threads a parallel region of this library will use. */
 int oracle_num_threads(void) {
 #ifdef _OPENMP

@@ -26,6 +26,12 @@ What pins what:
                  shift of a row; dX orthogonal to 1 and xhat; central finite
                  differences for dX, dgamma, dbeta, and for the whole
                  sequence-parallel block (LayerNorm, then the sharded MLP).
+  * attention -- numpy einsum/softmax on the canonical [Q|K|V] layout; the same
+                 outputs for t = 1, 2, 4 after the shard-major column permutation
+                 (the head split of section 4.1); rows of P sum to 1 and put no
+                 weight on later tokens; a token changes only its own and later
+                 outputs of its own sequence; central finite differences for dX,
+                 dWqkv, dbqkv, dWo, dbo.
 """
 from __future__ import annotations
 
@@ -343,10 +349,129 @@ def check_sp_composition_fd(lib, eps_fd=1e-6, tol=1e-6):
     return f
 
 
+def _attn_perm(h, heads, t):
+    """Column permutation from the canonical [Q | K | V] layout (heads in order)
+    to the shard-major layout [Q_0 | K_0 | V_0 | Q_1 | ...] of t shards."""
+    d, hpt, hs = h // heads, heads // t, h // t
+    perm = []
+    for i in range(t):
+        for which in range(3):
+            for j in range(hpt):
+                g = i * hpt + j
+                perm.extend(range(which * h + g * d, which * h + (g + 1) * d))
+    return np.array(perm)
+
+
+def _attn_case(nb, S, h, seed):
+    rng = np.random.default_rng(seed)
+    T = nb * S
+    return (rng.standard_normal((T, h)), rng.standard_normal((h, 3 * h)) * 0.5,
+            rng.standard_normal(3 * h) * 0.3, rng.standard_normal((h, h)) * 0.5,
+            rng.standard_normal(h) * 0.3, rng.standard_normal((T, h)))
+
+
+def _numpy_attention(X, Wc, bc, Wo, bo, nb, heads):
+    """Causal multi-head attention from numpy primitives, canonical [Q|K|V] layout."""
+    T, h = X.shape
+    S, d = T // nb, h // heads
+    qkv = X @ Wc + bc
+    q = qkv[:, :h].reshape(nb, S, heads, d).transpose(0, 2, 1, 3)
+    k = qkv[:, h:2 * h].reshape(nb, S, heads, d).transpose(0, 2, 1, 3)
+    v = qkv[:, 2 * h:].reshape(nb, S, heads, d).transpose(0, 2, 1, 3)
+    sc = np.einsum("bgrd,bgcd->bgrc", q, k) / np.sqrt(d)
+    sc = np.where(np.tril(np.ones((S, S), dtype=bool)), sc, -np.inf)
+    sc = sc - sc.max(axis=-1, keepdims=True)
+    p = np.exp(sc)
+    p /= p.sum(axis=-1, keepdims=True)
+    o = np.einsum("bgrc,bgcd->bgrd", p, v).transpose(0, 2, 1, 3).reshape(T, h)
+    return p, o, o @ Wo + bo
+
+
+def check_attn_numpy(lib):
+    f = []
+    nb, S, h, heads = 2, 5, 8, 2
+    X, Wc, bc, Wo, bo, _ = _attn_case(nb, S, h, 600)
+    p_ref, o_ref, z_ref = _numpy_attention(X, Wc, bc, Wo, bo, nb, heads)
+    for t in (1, 2):
+        perm = _attn_perm(h, heads, t)
+        out = oracle.attn_forward(X, Wc[:, perm], bc[perm], Wo, bo, nb, heads, t, lib=lib)
+        for name, got, ref in (("P", out["P"], p_ref), ("O", out["O"], o_ref), ("Z", out["Z"], z_ref)):
+            if _rel(got, ref) > 1e-12:
+                f.append("attention %s (t=%d) differs from numpy: %.3e" % (name, t, _rel(got, ref)))
+    return f
+
+
+def check_attn_sharding(lib):
+    """Z is the same for t = 1, 2, 4 once Wqkv's columns are laid out shard-major,
+    i.e. the head split of the report's section 4.1 does not change the result."""
+    f = []
+    nb, S, h, heads = 2, 4, 16, 4
+    X, Wc, bc, Wo, bo, dZ = _attn_case(nb, S, h, 601)
+    ref = None
+    for t in (1, 2, 4):
+        perm = _attn_perm(h, heads, t)
+        fw = oracle.attn_forward(X, Wc[:, perm], bc[perm], Wo, bo, nb, heads, t, lib=lib)
+        bw = oracle.attn_backward(X, Wc[:, perm], Wo, fw["QKV"], fw["P"], fw["O"], dZ, nb, heads, t, lib=lib)
+        inv = np.argsort(perm)
+        got = {"Z": fw["Z"], "dX": bw["dX"], "dWo": bw["dWo"], "dWqkv": bw["dWqkv"][:, inv]}
+        if ref is None:
+            ref = got
+        for k in got:
+            if _rel(got[k], ref[k]) > 1e-12:
+                f.append("attention %s for t=%d differs from t=1" % (k, t))
+    return f
+
+
+def check_attn_causal(lib):
+    f = []
+    nb, S, h, heads, t = 2, 6, 8, 2, 2
+    X, Wc, bc, Wo, bo, _ = _attn_case(nb, S, h, 602)
+    out = oracle.attn_forward(X, Wc, bc, Wo, bo, nb, heads, t, lib=lib)
+    P = out["P"]
+    if np.max(np.abs(P.sum(axis=-1) - 1)) > 1e-14:
+        f.append("attention rows do not sum to 1")
+    if np.max(np.abs(np.triu(P, 1))) != 0.0:
+        f.append("attention puts weight on later positions")
+    X2 = X.copy()
+    X2[S + 3] += 1.0  # token 3 of sequence 1
+    Z2 = oracle.attn_forward(X2, Wc, bc, Wo, bo, nb, heads, t, lib=lib)["Z"]
+    dz = np.abs(Z2 - out["Z"]).max(axis=1)
+    if dz[:S + 3].max() != 0.0 or dz[S + 3:].min() == 0.0:
+        f.append("a token changes outputs of earlier tokens or of another sequence")
+    return f
+
+
+def check_attn_fd(lib, eps_fd=1e-6, tol=1e-6):
+    f = []
+    nb, S, h, heads, t = 2, 3, 4, 2, 2
+    X, Wc, bc, Wo, bo, dZ = _attn_case(nb, S, h, 603)
+
+    def loss():
+        return float(np.sum(dZ * oracle.attn_forward(X, Wc, bc, Wo, bo, nb, heads, t, lib=lib)["Z"]))
+
+    out = oracle.attn_forward_backward(X, Wc, bc, Wo, bo, dZ, nb, heads, t, lib=lib)
+    for name, p, grad in (("X", X, out["dX"]), ("Wqkv", Wc, out["dWqkv"]), ("bqkv", bc, out["dbqkv"]),
+                          ("Wo", Wo, out["dWo"]), ("bo", bo, out["dbo"])):
+        fd = np.empty_like(p)
+        flat = p.reshape(-1)
+        for i in range(flat.size):
+            old = flat[i]
+            flat[i] = old + eps_fd
+            lp = loss()
+            flat[i] = old - eps_fd
+            lm = loss()
+            flat[i] = old
+            fd.reshape(-1)[i] = (lp - lm) / (2 * eps_fd)
+        if _rel(grad, fd) > tol:
+            f.append("attention d%s vs finite differences: rel %.3e" % (name, _rel(grad, fd)))
+    return f
+
+
 ALL = [check_gelu_vs_erf, check_gelu_identities, check_gelu_prime_fd, check_forward_numpy,
        check_worked_example_t2, check_backward_fd, check_backward_partials,
        check_closed_forms, check_slice_vs_full, check_layernorm_numpy, check_layernorm_invariants,
-       check_layernorm_backward_fd, check_sp_composition_fd]
+       check_layernorm_backward_fd, check_sp_composition_fd, check_attn_numpy, check_attn_sharding,
+       check_attn_causal, check_attn_fd]
 
 
 def run_all(lib) -> list:

@@ -47,6 +47,18 @@ MUTANTS = {
                          "dX[r * h + j] = rstd * (dy[j] * gamma[j] - mg);"),
     # dgamma without xhat
     "ln_dgamma": ("sg += dY[r * h + j] * (X[r * h + j] - mu[r]) * rs[r];", "sg += dY[r * h + j];"),
+    # attention without the causal mask on the scores
+    "attn_no_mask": ("const int64_t last = r; /* causal", "const int64_t last = S - 1; /* causal"),
+    # scores without the 1/sqrt(d) scale
+    "attn_no_scale": ("Pg[r * S + c] = sc * scale;", "Pg[r * S + c] = sc;"),
+    # softmax backward without the row term D
+    "attn_ds_no_D": ("const double ds = Pg[r * S + c] * (dP[c] - D) * scale;",
+                     "const double ds = Pg[r * S + c] * dP[c] * scale;"),
+    # dK built from K instead of Q
+    "attn_dk_operand": ("dk[e] += ds * qr[e];", "dk[e] += ds * kr[e];"),
+    # output projection: a shard's partial added twice
+    "attn_fold": ("                for (int64_t c = 0; c < h; ++c) Z[r * h + c] += part[c];\n            }\n            for (int64_t c = 0; c < h; ++c) Z[r * h + c] += bo[c];",
+                  "                for (int64_t c = 0; c < h; ++c) Z[r * h + c] += (i == 0 ? 2.0 : 1.0) * part[c];\n            }\n            for (int64_t c = 0; c < h; ++c) Z[r * h + c] += bo[c];"),
 }
 
 
