@@ -11,6 +11,7 @@ replica of the workload (the path has no cross-GPU step here): weak scaling.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on a token sample
   python bench.py --sweep                # microbatch sweep, one line per b
+  python bench.py --attn                 # the tensor-parallel self-attention block
 """
 from __future__ import annotations
 
@@ -385,6 +386,91 @@ def run_ours(args, rank, world, local, w=None, quiet=False):
     return line
 
 
+# ------------------------------------------------------------------ attention leg
+def run_attn_bench(args, rank, world, local):
+    """Forward + backward of the tensor-parallel self-attention block (heads split
+    among t shards; the projections and per-head products on the tensor-core
+    GEMMs).  One step = tpmlp_attn_forward + tpmlp_attn_backward."""
+    from tensor_transformer_mlp_tma_gb300 import tpmlp
+    from tensor_transformer_mlp_tma_gb300.workloads import ATTN_WORKLOADS
+    w = ATTN_WORKLOADS[args.attn_workload]
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    host = inputs.make_attn(w.tokens, w.hidden, args.seed + rank,
+                            {"Wqkv": w.std_W, "Wo": w.std_W, "bqkv": w.std_b, "bo": w.std_b})
+    d = {k: v.to(dev) for k, v in host.items()}
+    T, h, S = w.tokens, w.hidden, w.seq
+    ctx = tpmlp.AttnContext(w.batch, S, h, w.heads, w.t, device=dev)
+    Z = torch.empty((T, h), dtype=torch.bfloat16, device=dev)
+    g = {"dX": torch.empty((T, h), dtype=torch.bfloat16, device=dev),
+         "dWqkv": torch.empty((h, 3 * h), dtype=torch.bfloat16, device=dev),
+         "dbqkv": torch.empty((3 * h,), dtype=torch.bfloat16, device=dev),
+         "dWo": torch.empty((h, h), dtype=torch.bfloat16, device=dev),
+         "dbo": torch.empty((h,), dtype=torch.bfloat16, device=dev)}
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        tpmlp.attn_forward(ctx, d["X"], d["Wqkv"], d["bqkv"], d["Wo"], d["bo"], Z=Z, stream=stream)
+        tpmlp.attn_backward(ctx, d["dZ"], stream=stream, **g)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    if tpmlp.check_device_status(ctx, stream) != tpmlp.OK:
+        raise RuntimeError("device status after warm-up")
+    tpmlp.profile_reset()
+    tpmlp.profile_enable(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    launches0 = tpmlp.launch_count()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clocks:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    launches = tpmlp.launch_count() - launches0
+    tpmlp.profile_enable(False)
+    kernels = tpmlp.profile_collect()
+    if tpmlp.check_device_status(ctx, stream) != tpmlp.OK:
+        raise RuntimeError("device status after timed region")
+    ms_max = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    value = w.flops_fwd_bwd * world / (ms_max * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    proj, head = 2.0 * T * h * h, 2.0 * T * S * h
+    gemm_flops = {"attn_qkv_proj": 3 * proj, "attn_out_proj_fold": proj, "attn_scores": head, "attn_pv": head,
+                  "attn_bwd_dO": proj, "attn_bwd_dWo": proj, "attn_bwd_dV": head, "attn_bwd_dS": head,
+                  "attn_bwd_dQ": head, "attn_bwd_dK": head, "attn_bwd_dWqkv": 3 * proj,
+                  "attn_bwd_dX_shard_fold": 3 * proj}
+    name, (n, tot) = max(kernels.items(), key=lambda kv: kv[1][1])
+    achieved = gemm_flops[name] / (tot / n * 1e-3) / 1e12 if name in gemm_flops else None
+    peak = peaks["bf16_tflops_sustained"]
+    roof = {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": peak, "unit": UNIT,
+            "frac": achieved / peak if achieved else None, "traffic": None,
+            "peak_source": "%s bf16_tflops_sustained (kernel timed inside a long step)" % peak_src}
+    total = sum(v[1] for v in kernels.values())
+    clk = clocks.summary()
+    return {"metric": "TP self-attention fwd+bwd TFLOP/s (bf16, 1×GB300)", "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "seq": S, "hidden": h, "heads": w.heads, "t": w.t,
+                       "causal": True, "pass": "forward+backward",
+                       "flops_per_step": w.flops_fwd_bwd,
+                       "flops_note": "projections 24*T*h^2 + per-head products 12*T*seq*h (full seq x seq, "
+                                     "masked half included, as run)",
+                       "l2": "per-step working set larger than L2"},
+            "frac_of_peak": value / world / peak, "roofline": roof, "gpu_launches": int(sum_over_ranks(launches, world)),
+            "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
+            "kernels": {k: {"launches": n, "ms_per_launch": t_ / n, "share": t_ / total,
+                            "tflops": (gemm_flops[k] / (t_ / n * 1e-3) / 1e12) if k in gemm_flops else None}
+                        for k, (n, t_) in kernels.items()}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -401,6 +487,9 @@ def main():
                     help="activation recomputation: keep only H between forward and backward")
     ap.add_argument("--sp", action="store_true",
                     help="sequence-parallel block: LayerNorm in front of the MLP")
+    ap.add_argument("--attn", action="store_true",
+                    help="the tensor-parallel self-attention block (its own line, not the headline)")
+    ap.add_argument("--attn-workload", default="attn-h8192", choices=["attn-h4096", "attn-h8192"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-tokens", type=int, default=32,
@@ -411,6 +500,11 @@ def main():
     rank, world, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.attn:
+        line = run_attn_bench(args, rank, world, local)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
         return
     if args.sweep:
         for b in (1, 2, 4, 8):

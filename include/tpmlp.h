@@ -211,6 +211,67 @@ tpmlp_status tpmlp_sp_backward(const tpmlp_shape *shape, const tpmlp_layernorm *
                                const tpmlp_saved *saved, void *dX_in, void *dgamma, void *dbeta, void *dA,
                                void *da, void *dB, void *db, void *workspace, void *stream);
 
+/* ---- tensor-parallel self-attention block (report section 4.1) ---------------
+ * The report splits self-attention like the MLP: the heads are divided among
+ * the t shards; the QKV projection is column-parallel (each shard projects the
+ * replicated input onto the Q, K and V of its own heads) and the output
+ * projection row-parallel (each shard multiplies its heads' columns of O by its
+ * rows of Wo; the t partial products are summed, the all-reduce).  Each head is
+ * causal scaled dot-product attention:
+ *   S = Q K^T / sqrt(d) (row r sees positions <= r),  P = softmax_row(S),  O = P V,
+ *   Z = bo + sum_i O_i Wo_i   (fixed shard order).
+ * Layout: X, Z, O [T,h] with T = batch*seq tokens (batch sequences of seq
+ * tokens); Wqkv [h,3h], bqkv [3h] with shard-major columns: shard i owns columns
+ * [i*3h/t, (i+1)*3h/t) = [Q_i | K_i | V_i], each h/t wide, head j of the shard at
+ * offset j*d (d = h/heads); global head g = i*heads/t + j owns O's columns
+ * [g*d, (g+1)*d); Wo [h,h], bo [h].  bf16 only (tensor cores). */
+typedef struct {
+    int64_t batch;  /* sequences (>= 0) */
+    int64_t seq;    /* tokens per sequence, a multiple of 8 */
+    int64_t hidden; /* h */
+    int32_t heads;  /* h % heads == 0, heads % t == 0, d = h/heads a multiple of 64 */
+    int32_t t;      /* shards, 1..16 */
+    int32_t dtype;  /* TPMLP_BF16 */
+    int32_t flags;  /* 0 */
+} tpmlp_attn_shape;
+
+/* What the forward pass keeps for the backward pass (caller-owned except the
+ * weights, which tpmlp_attn_forward records): QKV [T,3h], P [batch*heads, seq,
+ * seq] (bf16 probabilities of every head), O [T,h]. */
+typedef struct {
+    const void *X;
+    const void *Wqkv;
+    const void *Wo;
+    void *QKV;
+    void *P;
+    void *O;
+} tpmlp_attn_saved;
+
+/* Bytes of QKV + P + O; 0 for an invalid shape. */
+size_t tpmlp_attn_saved_bytes(const tpmlp_attn_shape *shape);
+/* Bytes of device workspace for forward and backward (status word, column-sum
+ * partials, per-head Q, K, V, O, dO, dQ, dK, dV blocks, the fp32 scores, dS and
+ * the row terms); 256-byte aligned, first 8 bytes zero before first use. */
+size_t tpmlp_attn_workspace_bytes(const tpmlp_attn_shape *shape);
+
+/* Forward: QKV = X Wqkv + bqkv (one column-parallel GEMM for all shards), per
+ * head P = softmax(causal Q K^T / sqrt(d)) and O = P V (batched over heads),
+ * Z = bo + fixed-order sum of the t row-parallel partials.
+ * Errors: INVALID_ARG for a bad shape or NULL pointer; UNSUPPORTED for a non-bf16
+ * dtype, misaligned pointers, d % 64 != 0, seq % 8 != 0, or h/t or 3h/t not a
+ * multiple of 64 when t > 1; CUDA when a launch fails. */
+tpmlp_status tpmlp_attn_forward(const tpmlp_attn_shape *shape, const void *X, const void *Wqkv,
+                                const void *bqkv, const void *Wo, const void *bo, void *Z,
+                                tpmlp_attn_saved *saved, void *workspace, void *stream);
+
+/* Backward for L = sum(dZ * Z): dbo = 1^T dZ, dO = dZ Wo^T, dWo = O^T dZ; per head
+ * dV = P^T dO, dS = P * (dO V^T - rowsum(dO * O)) / sqrt(d), dQ = dS K, dK = dS^T Q;
+ * dbqkv = 1^T dQKV, dWqkv = X^T dQKV, dX = fixed-order sum over shards of
+ * dQKV_i Wqkv_i^T (the backward all-reduce).  Errors as the forward. */
+tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *shape, const void *dZ, const tpmlp_attn_saved *saved,
+                                 void *dX, void *dWqkv, void *dbqkv, void *dWo, void *dbo, void *workspace,
+                                 void *stream);
+
 /* Synchronises the stream, reads the workspace status word, clears it and
  * returns it (TPMLP_OK when no device-side error was recorded). */
 tpmlp_status tpmlp_check_device_status(void *workspace, void *stream);

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -647,6 +648,358 @@ int tpmlp_profile_entry(int i, char *name, int name_len, int64_t *launches, doub
     if (launches) *launches = t.second.launches;
     if (total_ms) *total_ms = t.second.ms;
     return 0;
+}
+
+}  // extern "C"
+
+// ---- tensor-parallel self-attention block ------------------------------------------------
+namespace {
+
+bool attn_shape_valid(const tpmlp_attn_shape *s) {
+    if (!s) return false;
+    if (s->batch < 0 || s->seq <= 0 || s->hidden <= 0 || s->heads <= 0) return false;
+    if (s->t < 1 || s->t > 16 || s->heads % s->t != 0 || s->hidden % s->heads != 0) return false;
+    if (s->flags != 0) return false;
+    // int32 tile and grid arithmetic inside the kernels
+    if (s->hidden > (1LL << 28) || s->seq > (1LL << 20) || s->batch * s->seq > (1LL << 30)) return false;
+    if (static_cast<int64_t>(s->batch) * s->heads > (1LL << 24)) return false;
+    return true;
+}
+
+// Device workspace of the attention block, 1 KB-aligned regions:
+//   status | column-sum partials | D [batch*heads*seq] fp32 | Qh Kh Vh Oh dOh dQh dKh dVh
+//   [batch*heads][seq][d] bf16 | dO [T,h] bf16 | dQKV [T,3h] bf16 | scores [batch*heads][seq][seq]
+//   fp32 (the backward reuses it for dS in bf16).
+struct AttnLayout {
+    size_t partials, D, head[8], dO, dQKV, scores, total;
+};
+enum { QH = 0, KH, VH, OH, DOH, DQH, DKH, DVH };
+
+AttnLayout attn_layout(const tpmlp_attn_shape *s) {
+    const int64_t T = s->batch * s->seq, h = s->hidden;
+    AttnLayout L;
+    size_t off = STATUS_BYTES;
+    L.partials = off;
+    int64_t np = tpmlp::colsum_chunks(T, h) * h;
+    const int64_t np3 = tpmlp::colsum_chunks(T, 3 * h) * 3 * h;
+    np = np > np3 ? np : np3;
+    off += align_up(static_cast<size_t>(np) * 4, 1024);
+    L.D = off;
+    off += align_up(static_cast<size_t>(T) * s->heads * 4, 1024);
+    const size_t th = align_up(static_cast<size_t>(T) * h * 2, 1024);
+    for (int i = 0; i < 8; ++i) {
+        L.head[i] = off;
+        off += th;
+    }
+    L.dO = off;
+    off += th;
+    L.dQKV = off;
+    off += 3 * th;
+    L.scores = off;
+    off += align_up(static_cast<size_t>(s->batch) * s->heads * s->seq * s->seq * 4, 1024);
+    L.total = off;
+    return L;
+}
+
+// The MLP shape that routes the attention GEMMs and column sums to the bf16
+// tensor-core path.
+tpmlp_shape attn_route(const tpmlp_attn_shape *s) {
+    tpmlp_shape m;
+    std::memset(&m, 0, sizeof(m));
+    m.tokens = s->batch * s->seq;
+    m.hidden = s->hidden;
+    m.ffn = 3 * s->hidden;
+    m.t = s->t;
+    m.dtype = TPMLP_BF16;
+    m.algo = TPMLP_ALGO_DEFAULT;
+    return m;
+}
+
+tpmlp::HeadLayout head_layout(const tpmlp_attn_shape *s, bool qkv) {
+    tpmlp::HeadLayout L;
+    L.nb = s->batch;
+    L.S = s->seq;
+    L.h = s->hidden;
+    L.heads = s->heads;
+    L.d = s->hidden / s->heads;
+    L.t = s->t;
+    L.qkv = qkv;
+    L.nmat = qkv ? 3 : 1;
+    return L;
+}
+
+tpmlp_status attn_check(const tpmlp_attn_shape *s, const char *who, std::initializer_list<const void *> required,
+                        std::initializer_list<const void *> token_ptrs, const void *workspace) {
+    if (!attn_shape_valid(s)) {
+        tpmlp::set_last_error("%s: invalid shape", who);
+        return TPMLP_ERR_INVALID_ARG;
+    }
+    if (!workspace) {
+        tpmlp::set_last_error("%s: workspace is NULL", who);
+        return TPMLP_ERR_INVALID_ARG;
+    }
+    const bool empty = s->batch == 0;
+    for (const void *p : required)
+        if (!p) {
+            tpmlp::set_last_error("%s: NULL pointer", who);
+            return TPMLP_ERR_INVALID_ARG;
+        }
+    for (const void *p : token_ptrs)
+        if (!p && !empty) {
+            tpmlp::set_last_error("%s: NULL pointer", who);
+            return TPMLP_ERR_INVALID_ARG;
+        }
+    if (s->dtype != TPMLP_BF16) {
+        tpmlp::set_last_error("%s: the attention block runs in bf16 only", who);
+        return TPMLP_ERR_UNSUPPORTED;
+    }
+    const int64_t d = s->hidden / s->heads;
+    if (d % 64 != 0 || s->seq % 8 != 0) {
+        tpmlp::set_last_error("%s: head size %lld must be a multiple of 64 and seq %lld of 8", who,
+                              static_cast<long long>(d), static_cast<long long>(s->seq));
+        return TPMLP_ERR_UNSUPPORTED;
+    }
+    if (!aligned16(workspace)) return TPMLP_ERR_UNSUPPORTED;
+    for (const void *p : required)
+        if (!aligned16(p)) return TPMLP_ERR_UNSUPPORTED;
+    for (const void *p : token_ptrs)
+        if (p && !aligned16(p)) return TPMLP_ERR_UNSUPPORTED;
+    return TPMLP_OK;
+}
+
+// One batched GEMM of the per-head products.
+GemmArgs head_gemm(uint32_t *status, const void *a, bool a_mn, const void *b, bool b_mn, int64_t M, int64_t N,
+                   int64_t K, int64_t batch, void *out) {
+    GemmArgs g = base_args(status);
+    g.a = a, g.a_mn = a_mn;
+    g.b = b, g.b_mn = b_mn;
+    g.M = M, g.N = N, g.K = K, g.kshard = K;
+    g.batch = batch;
+    g.out0 = out;
+    pick_raster(g);
+    return g;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t tpmlp_attn_saved_bytes(const tpmlp_attn_shape *s) {
+    if (!attn_shape_valid(s)) return 0;
+    const size_t T = static_cast<size_t>(s->batch * s->seq), h = static_cast<size_t>(s->hidden);
+    return 2 * (T * 3 * h + T * h + static_cast<size_t>(s->batch) * s->heads * s->seq * s->seq);
+}
+
+size_t tpmlp_attn_workspace_bytes(const tpmlp_attn_shape *s) {
+    if (!attn_shape_valid(s)) return 0;
+    return attn_layout(s).total;
+}
+
+tpmlp_status tpmlp_attn_forward(const tpmlp_attn_shape *s, const void *X, const void *Wqkv, const void *bqkv,
+                                const void *Wo, const void *bo, void *Z, tpmlp_attn_saved *saved, void *workspace,
+                                void *stream) {
+    tpmlp::g_last_error[0] = '\0';
+    if (!saved) return invalid("tpmlp_attn_forward: saved is NULL");
+    tpmlp_status rc = attn_check(s, "tpmlp_attn_forward", {Wqkv, bqkv, Wo, bo},
+                                 {X, Z, saved->QKV, saved->P, saved->O}, workspace);
+    if (rc != TPMLP_OK) return rc;
+    saved->X = X;
+    saved->Wqkv = Wqkv;
+    saved->Wo = Wo;
+    if (s->batch == 0) return TPMLP_OK;
+    const int sms = num_sms_current();
+    if (sms == 0) return TPMLP_ERR_CUDA;
+    if (sms < 0) return TPMLP_ERR_DEVICE;
+    const tpmlp_shape ms = attn_route(s);
+    const AttnLayout L = attn_layout(s);
+    const int64_t T = s->batch * s->seq, h = s->hidden, S = s->seq, d = h / s->heads;
+    const int64_t nz = s->batch * s->heads;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint32_t *status = reinterpret_cast<uint32_t *>(ws);
+    void *Qh = ws + L.head[QH], *Kh = ws + L.head[KH], *Vh = ws + L.head[VH], *Oh = ws + L.head[OH];
+    float *scores = reinterpret_cast<float *>(ws + L.scores);
+
+    // Column-parallel projection of all shards: QKV = X Wqkv + bqkv.
+    GemmArgs g1 = base_args(status);
+    g1.a = X, g1.a_mn = false;     // X[T,h]: K-major
+    g1.b = Wqkv, g1.b_mn = true;   // Wqkv[h,3h]: MN-major
+    g1.M = T, g1.N = 3 * h, g1.K = h, g1.kshard = h;
+    g1.out0 = saved->QKV, g1.bias = bqkv;
+    pick_raster(g1);
+    cudaError_t e = gemm(&ms, "attn_qkv_proj", tpmlp::EPI_FOLD_BIAS, g1, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    {
+        Timed timed("attn_to_heads", st);
+        e = tpmlp::launch_to_heads(head_layout(s, true), saved->QKV, Qh, Kh, Vh, st);
+        if (e != cudaSuccess) return from_cuda(e);
+        g_launches.fetch_add(1);
+    }
+
+    // Scores of every head: scale * Q K^T, causal.
+    GemmArgs g2 = head_gemm(status, Qh, false, Kh, false, S, S, d, nz, scores);
+    g2.scale = 1.0f / std::sqrt(static_cast<float>(d));
+    g2.causal = true;
+    e = gemm(&ms, "attn_scores", tpmlp::EPI_ATTN_SCORE, g2, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    {
+        Timed timed("attn_softmax", st);
+        e = tpmlp::launch_softmax(scores, saved->P, nz * S, S, true, st);
+        if (e != cudaSuccess) return from_cuda(e);
+        g_launches.fetch_add(1);
+    }
+
+    // O_head = P V
+    GemmArgs g3 = head_gemm(status, saved->P, false, Vh, true, S, d, S, nz, Oh);
+    e = gemm(&ms, "attn_pv", tpmlp::EPI_STORE, g3, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    {
+        Timed timed("attn_to_tokens", st);
+        e = tpmlp::launch_to_tokens(head_layout(s, false), Oh, nullptr, nullptr, saved->O, st);
+        if (e != cudaSuccess) return from_cuda(e);
+        g_launches.fetch_add(1);
+    }
+
+    // Row-parallel output projection: shard partials O_i Wo_i folded in order, + bo.
+    GemmArgs g4 = base_args(status);
+    g4.a = saved->O, g4.a_mn = false;  // O[T,h]: K-major
+    g4.b = Wo, g4.b_mn = true;         // Wo[h,h]: MN-major
+    g4.M = T, g4.N = h, g4.K = h;
+    g4.nshards = s->t, g4.kshard = h / s->t;
+    g4.out0 = Z, g4.bias = bo;
+    pick_raster(g4);
+    e = gemm(&ms, "attn_out_proj_fold", tpmlp::EPI_FOLD_BIAS, g4, sms, st);
+    return from_cuda(e);
+}
+
+tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, const tpmlp_attn_saved *saved,
+                                 void *dX, void *dWqkv, void *dbqkv, void *dWo, void *dbo, void *workspace,
+                                 void *stream) {
+    tpmlp::g_last_error[0] = '\0';
+    if (!saved) return invalid("tpmlp_attn_backward: saved is NULL");
+    tpmlp_status rc = attn_check(s, "tpmlp_attn_backward", {saved->Wqkv, saved->Wo, dWqkv, dbqkv, dWo, dbo},
+                                 {dZ, saved->X, saved->QKV, saved->P, saved->O, dX}, workspace);
+    if (rc != TPMLP_OK) return rc;
+    const int64_t T = s->batch * s->seq, h = s->hidden, S = s->seq, d = h / s->heads;
+    const int64_t nz = s->batch * s->heads;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        // Empty batch: the weight and bias gradients are sums over no tokens.
+        cudaError_t e = cudaMemsetAsync(dWqkv, 0, static_cast<size_t>(h) * 3 * h * 2, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dbqkv, 0, static_cast<size_t>(3 * h) * 2, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dWo, 0, static_cast<size_t>(h) * h * 2, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dbo, 0, static_cast<size_t>(h) * 2, st);
+        return from_cuda(e);
+    }
+    const int sms = num_sms_current();
+    if (sms == 0) return TPMLP_ERR_CUDA;
+    if (sms < 0) return TPMLP_ERR_DEVICE;
+    const tpmlp_shape ms = attn_route(s);
+    const AttnLayout L = attn_layout(s);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint32_t *status = reinterpret_cast<uint32_t *>(ws);
+    float *partials = reinterpret_cast<float *>(ws + L.partials);
+    float *D = reinterpret_cast<float *>(ws + L.D);
+    void *Qh = ws + L.head[QH], *Kh = ws + L.head[KH], *Vh = ws + L.head[VH];
+    void *dOh = ws + L.head[DOH], *dQh = ws + L.head[DQH], *dKh = ws + L.head[DKH], *dVh = ws + L.head[DVH];
+    void *dO = ws + L.dO, *dQKV = ws + L.dQKV;
+    void *dS = ws + L.scores;  // bf16 [nz][S][S] over the dead fp32 scores
+    const float scale = 1.0f / std::sqrt(static_cast<float>(d));
+
+    // dbo = column sums of dZ
+    cudaError_t e = colsum(&ms, "attn_colsum_dbo", dZ, T, h, partials, dbo, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    // dO = dZ Wo^T (every shard's columns at once; no fold needed)
+    GemmArgs g1 = base_args(status);
+    g1.a = dZ, g1.a_mn = false;         // dZ[T,h]: K-major
+    g1.b = saved->Wo, g1.b_mn = false;  // Wo[h,h] as [N, K]: K-major
+    g1.M = T, g1.N = h, g1.K = h, g1.kshard = h;
+    g1.out0 = dO;
+    pick_raster(g1);
+    e = gemm(&ms, "attn_bwd_dO", tpmlp::EPI_FOLD, g1, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    // dWo = O^T dZ
+    GemmArgs g2 = base_args(status);
+    g2.a = saved->O, g2.a_mn = true;  // O[T,h] as [K=T, M=h]: MN-major
+    g2.b = dZ, g2.b_mn = true;        // dZ[T,h] as [K=T, N=h]: MN-major
+    g2.M = h, g2.N = h, g2.K = T, g2.kshard = T;
+    g2.out0 = dWo;
+    pick_raster(g2);
+    e = gemm(&ms, "attn_bwd_dWo", tpmlp::EPI_STORE, g2, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    {
+        Timed timed("attn_bwd_to_heads", st);
+        // Q, K, V of every head again from the saved projection, and dO per head.
+        e = tpmlp::launch_to_heads(head_layout(s, true), saved->QKV, Qh, Kh, Vh, st);
+        if (e == cudaSuccess) e = tpmlp::launch_to_heads(head_layout(s, false), dO, dOh, nullptr, nullptr, st);
+        if (e != cudaSuccess) return from_cuda(e);
+        g_launches.fetch_add(2);
+    }
+    {
+        Timed timed("attn_bwd_rowdot", st);
+        e = tpmlp::launch_rowdot(head_layout(s, false), dO, saved->O, D, st);
+        if (e != cudaSuccess) return from_cuda(e);
+        g_launches.fetch_add(1);
+    }
+
+    // dV_head = P^T dO_head
+    GemmArgs g3 = head_gemm(status, saved->P, true, dOh, true, S, d, S, nz, dVh);
+    e = gemm(&ms, "attn_bwd_dV", tpmlp::EPI_STORE, g3, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    // dS = P * (dO V^T - D) * scale
+    GemmArgs g4 = head_gemm(status, dOh, false, Vh, false, S, S, d, nz, dS);
+    g4.aux = saved->P;
+    g4.rowvec = D;
+    g4.scale = scale;
+    e = gemm(&ms, "attn_bwd_dS", tpmlp::EPI_ATTN_DS, g4, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    // dQ_head = dS K_head,  dK_head = dS^T Q_head
+    GemmArgs g5 = head_gemm(status, dS, false, Kh, true, S, d, S, nz, dQh);
+    e = gemm(&ms, "attn_bwd_dQ", tpmlp::EPI_STORE, g5, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    GemmArgs g6 = head_gemm(status, dS, true, Qh, true, S, d, S, nz, dKh);
+    e = gemm(&ms, "attn_bwd_dK", tpmlp::EPI_STORE, g6, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    {
+        Timed timed("attn_bwd_to_tokens", st);
+        e = tpmlp::launch_to_tokens(head_layout(s, true), dQh, dKh, dVh, dQKV, st);
+        if (e != cudaSuccess) return from_cuda(e);
+        g_launches.fetch_add(1);
+    }
+
+    // dbqkv = column sums of dQKV
+    e = colsum(&ms, "attn_colsum_dbqkv", dQKV, T, 3 * h, partials, dbqkv, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    // dWqkv = X^T dQKV
+    GemmArgs g7 = base_args(status);
+    g7.a = saved->X, g7.a_mn = true;  // X[T,h] as [K=T, M=h]: MN-major
+    g7.b = dQKV, g7.b_mn = true;      // dQKV[T,3h] as [K=T, N=3h]: MN-major
+    g7.M = h, g7.N = 3 * h, g7.K = T, g7.kshard = T;
+    g7.out0 = dWqkv;
+    pick_raster(g7);
+    e = gemm(&ms, "attn_bwd_dWqkv", tpmlp::EPI_STORE, g7, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    // dX = sum_i dQKV_i Wqkv_i^T, shard partials folded in order (the backward all-reduce)
+    GemmArgs g8 = base_args(status);
+    g8.a = dQKV, g8.a_mn = false;         // dQKV[T,3h]: K-major
+    g8.b = saved->Wqkv, g8.b_mn = false;  // Wqkv[h,3h] as [N=h, K=3h]: K-major
+    g8.M = T, g8.N = h, g8.K = 3 * h;
+    g8.nshards = s->t, g8.kshard = 3 * h / s->t;
+    g8.out0 = dX;
+    pick_raster(g8);
+    e = gemm(&ms, "attn_bwd_dX_shard_fold", tpmlp::EPI_FOLD, g8, sms, st);
+    return from_cuda(e);
 }
 
 }  // extern "C"

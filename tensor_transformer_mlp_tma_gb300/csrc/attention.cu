@@ -1,0 +1,156 @@
+// Support kernels of the tensor-parallel self-attention block ("Megatron-LM"
+// report, section 4.1: heads divided among the t shards).  The projections and
+// the per-head products run on the tensor-core GEMMs; these memory-bound kernels
+// move data between the token-major projection layout and per-head blocks, and
+// compute the row-wise parts of the attention:
+//   - heads <-> tokens: QKV [T, 3h] with shard-major columns [Q_i | K_i | V_i]
+//     (head j of shard i at column i*3h/t + which*h/t + j*d), or O [T, h] (head g
+//     at column g*d), to / from per-head blocks [nb*heads][S][d];
+//   - causal softmax of fp32 scores [nb*heads*S][S] into bf16 P;
+//   - D[z, s] = sum_e dO[token, head cols] * O[token, head cols], the row term of
+//     the softmax backward.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+
+namespace tpmlp {
+namespace attn {
+
+// Column of head g's Q (which = 0), K (1) or V (2) in the shard-major QKV layout,
+// or of head g in O when qkv is false.
+__device__ __forceinline__ int64_t head_col(bool qkv, int64_t h, int t, int64_t d, int64_t hpt, int64_t g,
+                                            int which) {
+    if (!qkv) return g * d;
+    const int64_t i = g / hpt, j = g % hpt;
+    return i * (3 * h / t) + which * (h / t) + j * d;
+}
+
+// One thread moves 8 bf16 (16 bytes).  to_heads: token-major -> head blocks.
+__global__ void __launch_bounds__(256)
+    permute_kernel(const HeadLayout L, const __nv_bfloat16 *__restrict__ tok, __nv_bfloat16 *__restrict__ tok_out,
+                   const __nv_bfloat16 *__restrict__ h0, const __nv_bfloat16 *__restrict__ h1,
+                   const __nv_bfloat16 *__restrict__ h2, __nv_bfloat16 *__restrict__ o0,
+                   __nv_bfloat16 *__restrict__ o1, __nv_bfloat16 *__restrict__ o2, bool to_heads) {
+    const int64_t vec_per_row = L.d / 8;
+    const int64_t per_tensor = L.nb * L.heads * L.S * vec_per_row;
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= per_tensor * L.nmat) return;
+    const int which = static_cast<int>(idx / per_tensor);
+    int64_t rem = idx - which * per_tensor;
+    const int64_t e8 = rem % vec_per_row;
+    rem /= vec_per_row;
+    const int64_t s = rem % L.S;
+    const int64_t z = rem / L.S;
+    const int64_t b = z / L.heads, g = z % L.heads;
+    const int64_t ld = L.qkv ? 3 * L.h : L.h;
+    const int64_t tok_off = (b * L.S + s) * ld + head_col(L.qkv, L.h, L.t, L.d, L.heads / L.t, g, which) + e8 * 8;
+    const int64_t head_off = (z * L.S + s) * L.d + e8 * 8;
+    if (to_heads) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(tok + tok_off));
+        __nv_bfloat16 *dst = which == 0 ? o0 : (which == 1 ? o1 : o2);
+        *reinterpret_cast<uint4 *>(dst + head_off) = v;
+    } else {
+        const __nv_bfloat16 *src = which == 0 ? h0 : (which == 1 ? h1 : h2);
+        *reinterpret_cast<uint4 *>(tok_out + tok_off) = __ldg(reinterpret_cast<const uint4 *>(src + head_off));
+    }
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// One warp per score row.  Row r of a head (r = row % S) sees columns 0..r; the
+// others are written as exact zeros.  Max-subtracted exponentials, fp32 sum.
+__global__ void __launch_bounds__(256)
+    softmax_kernel(const float *__restrict__ S_, __nv_bfloat16 *__restrict__ P, int64_t rows, int64_t S,
+                   bool causal) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int64_t last = causal ? row % S : S - 1;
+    const float *in = S_ + row * S;
+    __nv_bfloat16 *out = P + row * S;
+    float mx = -INFINITY;
+    for (int64_t c = lane; c <= last; c += 32) mx = fmaxf(mx, in[c]);
+    mx = warp_max(mx);
+    float sum = 0.0f;
+    for (int64_t c = lane; c <= last; c += 32) sum += expf(in[c] - mx);
+    sum = warp_sum(sum);
+    const float inv = 1.0f / sum;
+    for (int64_t c = lane; c < S; c += 32)
+        out[c] = __float2bfloat16_rn(c <= last ? expf(in[c] - mx) * inv : 0.0f);
+}
+
+// One warp per (token r, head g): D[z*S + s] = sum_e dO[r, g*d + e] * O[r, g*d + e]
+// over the token-major [T, h] arrays, written in per-head order (z = b*heads + g,
+// r = b*S + s).  d is a multiple of 8.
+__global__ void __launch_bounds__(256)
+    rowdot_kernel(const HeadLayout L, const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ b,
+                  float *__restrict__ D) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (row >= L.nb * L.S * L.heads) return;
+    const int64_t r = row / L.heads, g = row % L.heads;
+    const int64_t base = r * L.h + g * L.d;
+    float s = 0.0f;
+    for (int64_t e = static_cast<int64_t>(lane) * 8; e < L.d; e += 256) {
+        const uint4 va = __ldg(reinterpret_cast<const uint4 *>(a + base + e));
+        const uint4 vb = __ldg(reinterpret_cast<const uint4 *>(b + base + e));
+        const uint32_t ua[4] = {va.x, va.y, va.z, va.w}, ub[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&ua[i]);
+            const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162 *>(&ub[i]);
+            s += __low2float(x) * __low2float(y) + __high2float(x) * __high2float(y);
+        }
+    }
+    s = warp_sum(s);
+    if (lane == 0) D[((r / L.S) * L.heads + g) * L.S + r % L.S] = s;
+}
+
+}  // namespace attn
+
+cudaError_t launch_to_heads(const HeadLayout &L, const void *tok, void *h0, void *h1, void *h2, cudaStream_t st) {
+    const int64_t n = L.nmat * L.nb * L.heads * L.S * (L.d / 8);
+    if (n <= 0) return cudaSuccess;
+    attn::permute_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+        L, static_cast<const __nv_bfloat16 *>(tok), nullptr, nullptr, nullptr, nullptr,
+        static_cast<__nv_bfloat16 *>(h0), static_cast<__nv_bfloat16 *>(h1), static_cast<__nv_bfloat16 *>(h2), true);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_to_tokens(const HeadLayout &L, const void *h0, const void *h1, const void *h2, void *tok,
+                             cudaStream_t st) {
+    const int64_t n = L.nmat * L.nb * L.heads * L.S * (L.d / 8);
+    if (n <= 0) return cudaSuccess;
+    attn::permute_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+        L, nullptr, static_cast<__nv_bfloat16 *>(tok), static_cast<const __nv_bfloat16 *>(h0),
+        static_cast<const __nv_bfloat16 *>(h1), static_cast<const __nv_bfloat16 *>(h2), nullptr, nullptr, nullptr,
+        false);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_softmax(const float *S, void *P, int64_t rows, int64_t cols, bool causal, cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    attn::softmax_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+        S, static_cast<__nv_bfloat16 *>(P), rows, cols, causal);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rowdot(const HeadLayout &L, const void *a, const void *b, float *D, cudaStream_t st) {
+    const int64_t rows = L.nb * L.S * L.heads;
+    if (rows <= 0) return cudaSuccess;
+    attn::rowdot_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+        L, static_cast<const __nv_bfloat16 *>(a), static_cast<const __nv_bfloat16 *>(b), D);
+    return cudaGetLastError();
+}
+
+}  // namespace tpmlp

@@ -13,6 +13,8 @@ enum Epi : int {
     EPI_DGELU = 2,      // dY = acc * GeLU'(H)                              -- dZ B^T
     EPI_STORE = 3,      // out = acc                                       -- dB, dA
     EPI_FOLD = 4,       // dX = ((P_1 + P_2) + ...)                        -- dY A^T
+    EPI_ATTN_SCORE = 5, // S = scale * acc, -inf above the diagonal (causal), fp32 out -- Q K^T
+    EPI_ATTN_DS = 6,    // dS = P * (acc - D[row]) * scale                  -- dO V^T -> dS
 };
 
 // One GEMM  out[M,N] = sum_k opA(m,k) opB(k,n)  over row-major operands.
@@ -39,6 +41,12 @@ struct GemmArgs {
     bool raster_n;
     bool cta_pair;     // tensor-core path: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2)
     float *colsum_part;  // EPI_DGELU on tensor cores: fp32 column sums per 32-row block [ceil(M/32), N]
+    // Batched GEMMs: `batch` independent problems whose operands and outputs are
+    // contiguous [batch][rows][cols] arrays (attention heads).  1 = plain GEMM.
+    int64_t batch;
+    float scale;          // EPI_ATTN_SCORE, EPI_ATTN_DS
+    bool causal;          // EPI_ATTN_SCORE: mask columns past the row
+    const float *rowvec;  // EPI_ATTN_DS: D, one fp32 per output row, [batch][M]
 };
 
 // Tensor-core path: bf16 operands, fp32 accumulation in TMEM (tcgen05).
@@ -79,6 +87,22 @@ struct LnArgs {
 int64_t ln_partial_floats(int64_t rows, int64_t h);
 cudaError_t launch_ln_forward(bool is_bf16, const LnArgs &a, cudaStream_t st);
 cudaError_t launch_ln_backward(bool is_bf16, const LnArgs &a, cudaStream_t st, int *launches);
+
+// Attention support.  Per-head blocks are [nb*heads][S][d] (z = b*heads + g);
+// token-major data is QKV [T, 3h] with shard-major columns (qkv = true, nmat = 3:
+// Q, K, V) or O [T, h] (qkv = false, nmat = 1).
+struct HeadLayout {
+    int64_t nb, S, h, heads, d;
+    int t;
+    bool qkv;
+    int nmat;
+};
+cudaError_t launch_to_heads(const HeadLayout &L, const void *tok, void *h0, void *h1, void *h2, cudaStream_t st);
+cudaError_t launch_to_tokens(const HeadLayout &L, const void *h0, const void *h1, const void *h2, void *tok,
+                             cudaStream_t st);
+cudaError_t launch_softmax(const float *S, void *P, int64_t rows, int64_t cols, bool causal, cudaStream_t st);
+// D[z*S + s] = row dot of dO and O over head g's columns of token b*S + s (token-major inputs).
+cudaError_t launch_rowdot(const HeadLayout &L, const void *dO, const void *O, float *D, cudaStream_t st);
 
 // Records a description of the last failure of this host thread (read back by
 // tpmlp_last_error()).

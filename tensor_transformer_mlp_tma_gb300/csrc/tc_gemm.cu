@@ -84,12 +84,19 @@ struct Params {
     uint32_t *status;
     unsigned long long wait_ns;
     float *colsum_part;  // GeLU' epilogue: fp32 column sums of dY per 32-row block, or null
+    int batch;           // independent problems, tiles of problem z follow those of z - 1
+    float scale;
+    int causal;
+    const float *rowvec;
 };
 
 // Tile order: super-rows of `group` tiles along one dimension; inside a
 // super-row the grouped index runs fastest, so the CTAs resident at one time
 // share `group` panels of one operand and a few of the other.
-__device__ __forceinline__ void tile_coords(int tile, const Params &p, int &mb, int &nb) {
+__device__ __forceinline__ void tile_coords(int tile, const Params &p, int &mb, int &nb, int &zb) {
+    const int per_batch = p.m_tiles * p.n_tiles;
+    zb = tile / per_batch;
+    tile -= zb * per_batch;
     const int fast_tiles = p.raster_n ? p.n_tiles : p.m_tiles;
     const int slow_tiles = p.raster_n ? p.m_tiles : p.n_tiles;
     const int per_group = p.group * slow_tiles;
@@ -178,6 +185,19 @@ __device__ __forceinline__ void unstage_row(uint32_t box, int r, float (&v)[32])
     }
 }
 
+// Row r of a 32 x 32 fp32 box (4 KB, both staging boxes of a warp) staged for a
+// 128-byte-swizzled TMA store: 16-byte chunk j of the 128-byte row sits at
+// chunk j ^ (r & 7).
+__device__ __forceinline__ void stage_row_f32(uint32_t box, int r, const float (&v)[32]) {
+    const uint32_t row = box + static_cast<uint32_t>(r) * 128u;
+    const int x = r & 7;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        ptx::st_shared_v4(row + (static_cast<uint32_t>(j ^ x) << 4), __float_as_uint(v[4 * j]),
+                          __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                          __float_as_uint(v[4 * j + 3]));
+}
+
 __device__ __forceinline__ void pack32(const float (&v)[32], uint32_t (&w)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
@@ -252,13 +272,13 @@ struct AuxLoad {
 };
 
 __device__ __forceinline__ void aux_issue(const CUtensorMap *tm, AuxLoad &a, uint32_t box, int col, int row0,
-                                          int lane) {
+                                          int z, int lane) {
     __syncwarp();  // every lane has read the previous chunk out of the box
     if (lane == 0) {
         ptx::bulk_wait_read0();  // a store staged in this box (rebuilt Y) has been read
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive_expect_tx(a.bar, STG_BOX);
-        ptx::tma_load_2d(box, tm, a.bar, col, row0);  // out-of-range parts read as zero
+        ptx::tma_load_3d(box, tm, a.bar, col, row0, z);  // out-of-range parts read as zero
     }
     a.pending = true;
 }
@@ -266,10 +286,27 @@ __device__ __forceinline__ void aux_issue(const CUtensorMap *tm, AuxLoad &a, uin
 template <int EPI>
 __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap *tm0, const CUtensorMap *tm1,
                                              const CUtensorMap *tm2, float (&v)[32], int64_t row, int row0,
-                                             int col, int lane, uint32_t stg, AuxLoad *aux = nullptr,
+                                             int col, int z, int lane, uint32_t stg, AuxLoad *aux = nullptr,
                                              int next_col = -1, int next_row0 = 0,
                                              volatile int *abort_flag = nullptr) {
-    (void)row;
+    if constexpr (EPI == EPI_ATTN_SCORE) {
+        // S = scale * Q K^T with the causal mask, kept in fp32 for the softmax.
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            v[i] *= p.scale;
+            if (p.causal && col + i > row) v[i] = -INFINITY;
+        }
+        if (lane == 0) ptx::bulk_wait_read0();
+        __syncwarp();
+        stage_row_f32(stg, lane, v);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && row0 < p.M && col < p.N) {
+            ptx::tma_store_3d(tm0, stg, col, row0, z);
+            ptx::bulk_commit();
+        }
+        return;
+    }
     uint32_t w0[16], w1[16];
     bool two = false, store0 = true;
     const CUtensorMap *tm_second = tm1;  // map of the second staged box
@@ -298,7 +335,7 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
         // With activation recomputation the H box is reused to stage the rebuilt
         // Y, so the next H load waits until that store has left the box.
         const bool rebuild_y = p.out1 != nullptr;
-        if (!rebuild_y && next_col >= 0) aux_issue(tm1, *aux, stg + STG_BOX, next_col, next_row0, lane);
+        if (!rebuild_y && next_col >= 0) aux_issue(tm1, *aux, stg + STG_BOX, next_col, next_row0, z, lane);
         if (rebuild_y) {
             float y[32];
 #pragma unroll
@@ -320,6 +357,22 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
             if (row0 < p.M && col + lane < p.N)
                 p.colsum_part[static_cast<int64_t>(row0 >> 5) * p.N + col + lane] = cs;
         }
+    } else if constexpr (EPI == EPI_ATTN_DS) {
+        // dS = P * (dP - D) * scale: P read through the second staging box (TMA,
+        // one chunk ahead), D one fp32 per row.
+        float pv[32];
+        bool got = ptx::mbar_wait(aux->bar, aux->phase, p.wait_ns, abort_flag);
+        aux->phase ^= 1u;
+        aux->pending = false;
+        if (!__all_sync(0xffffffffu, got)) {
+            if (lane == 0) record_timeout(p, abort_flag, 6);
+        }
+        unstage_row(stg + STG_BOX, lane, pv);
+        if (next_col >= 0) aux_issue(tm1, *aux, stg + STG_BOX, next_col, next_row0, z, lane);
+        const float D = row < p.M ? p.rowvec[static_cast<int64_t>(z) * p.M + row] : 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = pv[i] * (v[i] - D) * p.scale;
+        pack32(v, w0);
     } else if constexpr (EPI == EPI_FOLD_BIAS) {
         float bias[32];
         load32(p.bias, col, col, p.N, true, bias);
@@ -338,12 +391,12 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
     __syncwarp();
     // A box that lies wholly outside the output (ragged last tile) is not stored.
     if (lane == 0 && row0 < p.M && col < p.N) {
-        if (store0) ptx::tma_store_2d(tm0, stg, col, row0);
-        if (two) ptx::tma_store_2d(tm_second, stg + STG_BOX, col, row0);
+        if (store0) ptx::tma_store_3d(tm0, stg, col, row0, z);
+        if (two) ptx::tma_store_3d(tm_second, stg + STG_BOX, col, row0, z);
         ptx::bulk_commit();
     }
     if constexpr (EPI == EPI_DGELU) {
-        if (p.out1 != nullptr && next_col >= 0) aux_issue(tm1, *aux, stg + STG_BOX, next_col, next_row0, lane);
+        if (p.out1 != nullptr && next_col >= 0) aux_issue(tm1, *aux, stg + STG_BOX, next_col, next_row0, z, lane);
     }
 }
 
@@ -420,7 +473,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem_base = tmem_base_sh;
 
-    const int num_tiles = p.m_tiles * p.n_tiles;
+    const int num_tiles = p.m_tiles * p.n_tiles * p.batch;
     const int kb_total = p.nshards * p.kb_per_shard;
 
     if (warp == 0) {
@@ -431,8 +484,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int64_t issued = 0;
             bool ok = true;
             for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
-                int mb, nb;
-                tile_coords(tile, p, mb, nb);
+                int mb, nb, zb;
+                tile_coords(tile, p, mb, nb, zb);
                 const int m0 = mb * C::TILE_M + BM * static_cast<int>(rank);
                 const int n0 = nb * BN + C::B_ROWS * static_cast<int>(rank);
                 for (int kb = 0; kb < kb_total; ++kb) {
@@ -448,9 +501,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int k0 = kb * BK;
                     auto load = [&](uint32_t dst, const CUtensorMap *map, int x, int y) {
                         if constexpr (PAIR)
-                            ptx::tma_load_2d_pair(dst, map, full, x, y);
+                            ptx::tma_load_3d_pair(dst, map, full, x, y, zb);
                         else
-                            ptx::tma_load_2d(dst, map, full, x, y);
+                            ptx::tma_load_3d(dst, map, full, x, y, zb);
                     };
                     // The leader announces the bytes of both CTAs' copies; the peer's
                     // copies only complete bytes on the leader's barrier (they can land
@@ -577,12 +630,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         };
         for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
-            int mb, nb;
-            tile_coords(tile, p, mb, nb);
+            int mb, nb, zb;
+            tile_coords(tile, p, mb, nb, zb);
             const int row0 = mb * C::TILE_M + BM * static_cast<int>(rank) + quarter * 32;
             const int64_t row = static_cast<int64_t>(row0) + lane;
             const int col0 = nb * BN + half * 128;
-            if constexpr (EPI == EPI_DGELU) aux_issue(&tmO1, aux, stg + STG_BOX, col0, row0, lane);
+            if constexpr (EPI == EPI_DGELU || EPI == EPI_ATTN_DS)
+                aux_issue(&tmO1, aux, stg + STG_BOX, col0, row0, zb, lane);
             for (int s = 0; s < p.nshards; ++s, ++unit) {
                 const uint32_t buf = unit & 1u, use = unit >> 1;
                 bool got = ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_tfull[buf]), use & 1u, p.wait_ns,
@@ -613,7 +667,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             float v[32];
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i];
-                            finish_chunk<EPI>(p, &tmO0, &tmO1, &tmO2, v, row, row0, col0 + c * 32, lane, stg);
+                            finish_chunk<EPI>(p, &tmO0, &tmO1, &tmO2, v, row, row0, col0 + c * 32, zb, lane, stg);
                         }
                     }
                 } else {
@@ -627,7 +681,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         float v[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                        finish_chunk<EPI>(p, &tmO0, &tmO1, &tmO2, v, row, row0, col0 + c * 32, lane, stg, &aux,
+                        finish_chunk<EPI>(p, &tmO0, &tmO1, &tmO2, v, row, row0, col0 + c * 32, zb, lane, stg, &aux,
                                           c < 3 ? col0 + (c + 1) * 32 : -1, row0, &abort_sh);
                     }
                 }
@@ -676,24 +730,30 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Row-major bf16 matrix [rows, cols] with a box of box_cols (inner) x box_rows.
+// A batch of `batch` contiguous row-major [rows, cols] matrices is a 3-D tensor
+// (cols, rows, batch); a plain matrix has batch 1.
 static bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, uint32_t box_cols,
-                     uint32_t box_rows, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+                     uint32_t box_rows, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B, int64_t batch = 1,
+                     bool fp32 = false) {
     auto fn = encode_fn();
     if (!fn) {
         set_last_error("cuTensorMapEncodeTiled is not available from the driver");
         return false;
     }
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+    const cuuint64_t esz = fp32 ? 4 : 2;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * esz,
+                             static_cast<cuuint64_t>(cols) * static_cast<cuuint64_t>(rows) * esz};
+    cuuint32_t box[3] = {box_cols, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
-        set_last_error("cuTensorMapEncodeTiled failed (CUresult %d) for a [%lld, %lld] bf16 matrix, box %u x %u",
-                       static_cast<int>(r), static_cast<long long>(rows), static_cast<long long>(cols), box_cols,
-                       box_rows);
+        set_last_error("cuTensorMapEncodeTiled failed (CUresult %d) for %lld x [%lld, %lld] matrices, box %u x %u",
+                       static_cast<int>(r), static_cast<long long>(batch), static_cast<long long>(rows),
+                       static_cast<long long>(cols), box_cols, box_rows);
     return r == CUDA_SUCCESS;
 }
 
@@ -749,8 +809,11 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     CUtensorMap ma, mb;
     // A operand: K-major [M,K] with a 64 x 128 box, or MN-major [K,M] with 64 x 64 boxes.
     // B operand: this CTA's B_ROWS columns, K-major in one box or MN-major in 64-wide boxes.
-    const bool oka = A_MN ? make_map(&ma, g.a, g.K, g.M, 64, BK) : make_map(&ma, g.a, g.M, g.K, BK, BM);
-    const bool okb = B_MN ? make_map(&mb, g.b, g.K, g.N, 64, BK) : make_map(&mb, g.b, g.N, g.K, BK, C::B_ROWS);
+    const int64_t nb = g.batch < 1 ? 1 : g.batch;
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    const bool oka = A_MN ? make_map(&ma, g.a, g.K, g.M, 64, BK, sw, nb) : make_map(&ma, g.a, g.M, g.K, BK, BM, sw, nb);
+    const bool okb = B_MN ? make_map(&mb, g.b, g.K, g.N, 64, BK, sw, nb)
+                          : make_map(&mb, g.b, g.N, g.K, BK, C::B_ROWS, sw, nb);
     if (!oka || !okb) return cudaErrorInvalidValue;
     // Output maps: [M, N] row-major, 32 x 32 boxes, 64-byte swizzle (matches stage_row).
     // Bias + GeLU writes H (optional) and Y; GeLU' reads H through the second map;
@@ -758,11 +821,15 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     // The GeLU' epilogue can also write Y rebuilt from H (third map).
     CUtensorMap mo0, mo1, mo2;
     const void *o0 = g.out0 ? g.out0 : g.out1;
-    const void *o1 = (EPI == EPI_BIAS_GELU) ? g.out1 : (EPI == EPI_DGELU ? g.aux : o0);
+    // The attention scores are fp32 (32 x 32 box, 128-byte swizzle, see stage_row_f32);
+    // dS reads P through the second map.
+    const void *o1 = (EPI == EPI_BIAS_GELU) ? g.out1 : ((EPI == EPI_DGELU || EPI == EPI_ATTN_DS) ? g.aux : o0);
     const void *o2 = (EPI == EPI_DGELU && g.out1) ? g.out1 : o0;
-    if (!make_map(&mo0, o0, g.M, g.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&mo1, o1, g.M, g.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&mo2, o2, g.M, g.N, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    const bool f32out = EPI == EPI_ATTN_SCORE;
+    const CUtensorMapSwizzle so = f32out ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!make_map(&mo0, o0, g.M, g.N, 32, 32, so, nb, f32out) ||
+        !make_map(&mo1, o1, g.M, g.N, 32, 32, so, nb, f32out) ||
+        !make_map(&mo2, o2, g.M, g.N, 32, 32, so, nb, f32out))
         return cudaErrorInvalidValue;
 
     Params p;
@@ -784,7 +851,11 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     p.status = g.status;
     p.wait_ns = g.wait_ns;
     p.colsum_part = g.colsum_part;
-    const int tiles = p.m_tiles * p.n_tiles;
+    p.batch = static_cast<int>(nb);
+    p.scale = g.scale;
+    p.causal = g.causal ? 1 : 0;
+    p.rowvec = g.rowvec;
+    const int tiles = p.m_tiles * p.n_tiles * p.batch;
     int resident = max_clusters[dev];
     if (const char *o = std::getenv("TPMLP_MAX_UNITS")) resident = std::atoi(o) > 0 ? std::atoi(o) : resident;
     const int units = tiles < resident ? tiles : resident;
@@ -827,8 +898,15 @@ cudaError_t launch_tc_gemm(Epi epi, const GemmArgs &g, int num_sms, cudaStream_t
         case EPI_DGELU:  // dZ[T,h] (K-major) . B[F,h]^T (K-major)
             if (!g.a_mn && !g.b_mn) return launch_cg<EPI_DGELU, false, false>(g, num_sms, st);
             break;
-        case EPI_STORE:  // Y^T . dZ and X^T . dY: both operands MN-major
+        case EPI_STORE:  // Y^T . dZ and X^T . dY: both operands MN-major; P . V: K-major . MN-major
             if (g.a_mn && g.b_mn) return launch_cg<EPI_STORE, true, true>(g, num_sms, st);
+            if (!g.a_mn && g.b_mn) return launch_cg<EPI_STORE, false, true>(g, num_sms, st);
+            break;
+        case EPI_ATTN_SCORE:  // Q[S,d] (K-major) . K[S,d]^T (K-major), per head
+            if (!g.a_mn && !g.b_mn) return launch_cg<EPI_ATTN_SCORE, false, false>(g, num_sms, st);
+            break;
+        case EPI_ATTN_DS:  // dO[S,d] (K-major) . V[S,d]^T (K-major), per head
+            if (!g.a_mn && !g.b_mn) return launch_cg<EPI_ATTN_DS, false, false>(g, num_sms, st);
             break;
         case EPI_FOLD:  // dY[T,F] (K-major) . A[h,F]^T (K-major)
             if (!g.a_mn && !g.b_mn) return launch_cg<EPI_FOLD, false, false>(g, num_sms, st);

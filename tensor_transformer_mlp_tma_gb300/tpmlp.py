@@ -41,6 +41,17 @@ class LayerNorm(ctypes.Structure):
                 ("eps", ctypes.c_float)]
 
 
+class AttnShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seq", ctypes.c_int64), ("hidden", ctypes.c_int64),
+                ("heads", ctypes.c_int32), ("t", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("flags", ctypes.c_int32)]
+
+
+class AttnSaved(ctypes.Structure):
+    _fields_ = [("X", ctypes.c_void_p), ("Wqkv", ctypes.c_void_p), ("Wo", ctypes.c_void_p),
+                ("QKV", ctypes.c_void_p), ("P", ctypes.c_void_p), ("O", ctypes.c_void_p)]
+
+
 class TpmlpError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -70,6 +81,10 @@ def _load():
         "tpmlp_sp_forward": (i32, [SP, ctypes.POINTER(LayerNorm), vp, vp, vp, vp, vp, ctypes.POINTER(Saved),
                                    vp, vp]),
         "tpmlp_sp_backward": (i32, [SP, ctypes.POINTER(LayerNorm), vp, ctypes.POINTER(Saved)] + [vp] * 9),
+        "tpmlp_attn_saved_bytes": (sz, [ctypes.POINTER(AttnShape)]),
+        "tpmlp_attn_workspace_bytes": (sz, [ctypes.POINTER(AttnShape)]),
+        "tpmlp_attn_forward": (i32, [ctypes.POINTER(AttnShape)] + [vp] * 6 + [ctypes.POINTER(AttnSaved), vp, vp]),
+        "tpmlp_attn_backward": (i32, [ctypes.POINTER(AttnShape), vp, ctypes.POINTER(AttnSaved)] + [vp] * 7),
         "tpmlp_check_device_status": (i32, [vp, vp]),
         "tpmlp_set_wait_limit_ns": (None, [u64]),
         "tpmlp_debug_timeout_probe": (i32, [vp, u64, vp]),
@@ -302,8 +317,76 @@ def ln_backward(ctx: Context, dXn, stream=None):
     return {"dX_in": dX_in, "dgamma": dg, "dbeta": dbt}
 
 
+class AttnContext:
+    """Buffers of one tensor-parallel self-attention layer between forward and
+    backward: the saved QKV [T,3h], P [batch*heads, seq, seq], O [T,h] and the
+    workspace (bf16 only)."""
+
+    def __init__(self, batch, seq, hidden, heads, t, device=None):
+        self.shape = AttnShape(int(batch), int(seq), int(hidden), int(heads), int(t), BF16, 0)
+        n = int(lib.tpmlp_attn_workspace_bytes(ctypes.byref(self.shape)))
+        if n == 0:
+            raise ValueError("invalid attention shape (batch=%d seq=%d hidden=%d heads=%d t=%d)"
+                             % (batch, seq, hidden, heads, t))
+        dev = device or "cuda"
+        T, h = batch * seq, hidden
+        self.dtype = torch.bfloat16
+        self.QKV = torch.empty((T, 3 * h), dtype=self.dtype, device=dev)
+        self.P = torch.empty((batch * heads, seq, seq), dtype=self.dtype, device=dev)
+        self.O = torch.empty((T, h), dtype=self.dtype, device=dev)
+        self.workspace = torch.zeros(n, dtype=torch.uint8, device=dev)
+        self.saved = AttnSaved(None, None, None, _ptr(self.QKV), _ptr(self.P), _ptr(self.O))
+        self._keep = []
+
+    @property
+    def tokens(self) -> int:
+        return self.shape.batch * self.shape.seq
+
+
+def attn_saved_bytes(batch, seq, hidden, heads, t) -> int:
+    s = AttnShape(int(batch), int(seq), int(hidden), int(heads), int(t), BF16, 0)
+    return int(lib.tpmlp_attn_saved_bytes(ctypes.byref(s)))
+
+
+def attn_forward(ctx: AttnContext, X, Wqkv, bqkv, Wo, bo, Z=None, stream=None):
+    """Z = bo + sum_i O_i Wo_i with per-head causal attention over X Wqkv + bqkv."""
+    s = ctx.shape
+    T, h = ctx.tokens, s.hidden
+    for x, n, shp in ((X, "X", (T, h)), (Wqkv, "Wqkv", (h, 3 * h)), (bqkv, "bqkv", (3 * h,)),
+                      (Wo, "Wo", (h, h)), (bo, "bo", (h,))):
+        _need(x, n, ctx.dtype, shp)
+    if Z is None:
+        Z = torch.empty((T, h), dtype=ctx.dtype, device=X.device)
+    _need(Z, "Z", ctx.dtype, (T, h))
+    ctx._keep = [X, Wqkv, Wo]
+    st = lib.tpmlp_attn_forward(ctypes.byref(s), _ptr(X), _ptr(Wqkv), _ptr(bqkv), _ptr(Wo), _ptr(bo), _ptr(Z),
+                                ctypes.byref(ctx.saved), _ptr(ctx.workspace), _stream(stream))
+    _check(st, "tpmlp_attn_forward")
+    return Z
+
+
+def attn_backward(ctx: AttnContext, dZ, stream=None, **outs):
+    """dX, dWqkv, dbqkv, dWo, dbo for L = sum(dZ * Z), from what attn_forward saved."""
+    s = ctx.shape
+    T, h = ctx.tokens, s.hidden
+    _need(dZ, "dZ", ctx.dtype, (T, h))
+    out = {}
+    for name, shp in (("dX", (T, h)), ("dWqkv", (h, 3 * h)), ("dbqkv", (3 * h,)), ("dWo", (h, h)),
+                      ("dbo", (h,))):
+        val = outs.get(name)
+        if val is None:
+            val = torch.empty(shp, dtype=ctx.dtype, device=dZ.device)
+        _need(val, name, ctx.dtype, shp)
+        out[name] = val
+    st = lib.tpmlp_attn_backward(ctypes.byref(s), _ptr(dZ), ctypes.byref(ctx.saved),
+                                 *(_ptr(out[k]) for k in ("dX", "dWqkv", "dbqkv", "dWo", "dbo")),
+                                 _ptr(ctx.workspace), _stream(stream))
+    _check(st, "tpmlp_attn_backward")
+    return out
+
+
 def check_device_status(ctx_or_ws, stream=None) -> int:
-    ws = ctx_or_ws.workspace if isinstance(ctx_or_ws, Context) else ctx_or_ws
+    ws = ctx_or_ws.workspace if isinstance(ctx_or_ws, (Context, AttnContext)) else ctx_or_ws
     return int(lib.tpmlp_check_device_status(_ptr(ws), _stream(stream)))
 
 

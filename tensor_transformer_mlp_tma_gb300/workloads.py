@@ -64,3 +64,47 @@ WORKLOADS = {
 
 # The workload the headline throughput is measured on.
 HEADLINE = "h8192"
+
+
+@dataclasses.dataclass(frozen=True)
+class AttnWorkload:
+    """Causal self-attention over `batch` sequences of `seq` tokens, hidden size
+    h, `heads` heads of d = h/heads, split into t shards by heads (the
+    "Megatron-LM" industry report, section 4.1)."""
+    name: str
+    batch: int
+    seq: int
+    hidden: int
+    heads: int
+    t: int
+    std_X: float = 1.0
+    std_W: float = 0.02
+    std_b: float = 0.0
+    std_dZ: float = 1.0
+    note: str = ""
+
+    @property
+    def tokens(self) -> int:
+        return self.batch * self.seq
+
+    @property
+    def flops_fwd(self) -> float:
+        """QKV and output projections (2*T*h*3h + 2*T*h*h) plus the two per-head
+        products Q K^T and P V over the full seq x seq scores (4*T*seq*h), as run."""
+        T, h = self.tokens, self.hidden
+        return 8.0 * T * h * h + 4.0 * T * self.seq * h
+
+    @property
+    def flops_fwd_bwd(self) -> float:
+        """Backward: dO, dWo, dWqkv, dX (twice the projections) and dV, dP, dQ, dK
+        (twice the per-head products): three times the forward in total."""
+        return 3.0 * self.flops_fwd
+
+
+ATTN_WORKLOADS = {
+    w.name: w
+    for w in [
+        AttnWorkload("attn-h4096", 4, 2048, 4096, 32, 8, note="b=4, s=2048, d=128"),
+        AttnWorkload("attn-h8192", 2, 2048, 8192, 64, 8, note="b=2, s=2048, d=128"),
+    ]
+}

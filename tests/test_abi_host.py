@@ -147,3 +147,60 @@ def test_profile_table_starts_empty(tp):
     tp.profile_reset()
     assert tp.lib.tpmlp_profile_count() == 0
     assert tp.lib.tpmlp_profile_entry(0, None, 0, None, None) == -1
+
+
+def _attn_fwd(tp, shape, ptrs=None, saved=None, ws=FAKE):
+    p = ptrs or [FAKE] * 6
+    sv = saved if saved is not None else tp.AttnSaved(None, None, None, FAKE, FAKE, FAKE)
+    return tp.lib.tpmlp_attn_forward(ctypes.byref(shape) if shape is not None else None, *p,
+                                     ctypes.byref(sv) if sv is not False else None, ws, None)
+
+
+def _attn_bwd(tp, shape, ptrs=None, saved=None, ws=FAKE):
+    p = ptrs or [FAKE] * 6
+    sv = saved if saved is not None else tp.AttnSaved(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)
+    return tp.lib.tpmlp_attn_backward(ctypes.byref(shape), p[0], ctypes.byref(sv), *p[1:], ws, None)
+
+
+def test_attention_size_queries(tp):
+    s = tp.AttnShape(2, 2048, 8192, 64, 8, tp.BF16, 0)
+    T, h, S, nz = 4096, 8192, 2048, 128
+    assert tp.lib.tpmlp_attn_saved_bytes(ctypes.byref(s)) == 2 * (T * 3 * h + T * h + nz * S * S)
+    ws = tp.lib.tpmlp_attn_workspace_bytes(ctypes.byref(s))
+    # per-head Q, K, V, O, dO, dQ, dK, dV, token-major dO and dQKV, fp32 scores
+    assert ws >= 12 * T * h * 2 + nz * S * S * 4
+    assert ws % 1024 == 0
+    assert tp.attn_saved_bytes(2, 2048, 8192, 64, 8) == tp.lib.tpmlp_attn_saved_bytes(ctypes.byref(s))
+    for bad in (tp.AttnShape(1, 64, 256, 3, 1, tp.BF16, 0),    # h % heads != 0
+                tp.AttnShape(1, 64, 256, 2, 4, tp.BF16, 0),    # heads % t != 0
+                tp.AttnShape(1, 64, 256, 2, 0, tp.BF16, 0),    # t < 1
+                tp.AttnShape(1, 0, 256, 2, 1, tp.BF16, 0),     # seq = 0
+                tp.AttnShape(-1, 64, 256, 2, 1, tp.BF16, 0),   # batch < 0
+                tp.AttnShape(1, 64, 256, 2, 1, tp.BF16, 1)):   # flags
+        assert tp.lib.tpmlp_attn_saved_bytes(ctypes.byref(bad)) == 0
+        assert tp.lib.tpmlp_attn_workspace_bytes(ctypes.byref(bad)) == 0
+    assert tp.lib.tpmlp_attn_workspace_bytes(ctypes.byref(tp.AttnShape(0, 64, 256, 2, 2, tp.BF16, 0))) > 0
+
+
+def test_attention_invalid_and_unsupported_arguments(tp):
+    good = tp.AttnShape(2, 128, 256, 2, 2, tp.BF16, 0)
+    assert _attn_fwd(tp, None) == tp.ERR_INVALID_ARG
+    assert _attn_fwd(tp, good, saved=False) == tp.ERR_INVALID_ARG
+    assert _attn_fwd(tp, good, ws=None) == tp.ERR_INVALID_ARG
+    for i in range(6):
+        p = [FAKE] * 6
+        p[i] = None
+        assert _attn_fwd(tp, good, ptrs=p) == tp.ERR_INVALID_ARG
+        assert _attn_bwd(tp, good, ptrs=p) == tp.ERR_INVALID_ARG
+    for field in ("X", "Wqkv", "Wo", "QKV", "P", "O"):
+        sv = tp.AttnSaved(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)
+        setattr(sv, field, None)
+        assert _attn_bwd(tp, good, saved=sv) == tp.ERR_INVALID_ARG
+    # fp32, head size 32, seq not a multiple of 8, misaligned pointer: unsupported
+    assert _attn_fwd(tp, tp.AttnShape(2, 128, 256, 2, 2, tp.F32, 0)) == tp.ERR_UNSUPPORTED
+    assert _attn_fwd(tp, tp.AttnShape(2, 128, 256, 8, 2, tp.BF16, 0)) == tp.ERR_UNSUPPORTED
+    assert _attn_fwd(tp, tp.AttnShape(2, 100, 256, 2, 2, tp.BF16, 0)) == tp.ERR_UNSUPPORTED
+    p = [FAKE] * 6
+    p[1] = FAKE + 2
+    assert _attn_fwd(tp, good, ptrs=p) == tp.ERR_UNSUPPORTED
+    assert _attn_bwd(tp, good, ws=FAKE + 8) == tp.ERR_UNSUPPORTED

@@ -1,0 +1,201 @@
+"""Tensor-parallel self-attention block on the GPU against the fp64 oracle.
+
+Heads are split among the t shards: the QKV projection is column-parallel, the
+output projection row-parallel with the fixed-order shard fold ("Megatron-LM"
+industry report, section 4.1).  Every case runs the tensor-core path through the
+C ABI and compares, element by element, the saved activations (QKV, P, O), the
+output Z and every gradient with the oracle on the same seeded bf16 inputs.
+Shapes span several 256-wide tiles of the per-head products, ragged sequence
+tails, head sizes 64 and 128, t = 1..4, and the empty batch.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_cases import rel, to_np
+
+pytestmark = pytest.mark.gpu
+
+# max|out - ref| / max|ref|.  QKV comes out of one fp32-accumulated GEMM and is
+# stored in bf16: 1e-2 as for the MLP's outputs.  Everything downstream of the
+# logits carries two bf16 roundings in a row: Q and K are stored in bf16 (unit
+# roundoff u = 2^-9), which moves a logit s by up to about 2u|s| (|s| reaches 10
+# and more when the logit std is about 3, as at h = 8192 with weights of std
+# 0.02), and P is rounded to bf16 again before P V.  Observed errors there are
+# about 1.1e-2 at that logit scale: P, O and Z are held to 2e-2, the gradients
+# (through dO, dS and dQKV, also stored in bf16) to 3e-2.
+TOL = {"QKV": 1e-2, "P": 2e-2, "O": 2e-2, "Z": 2e-2,
+       "dX": 3e-2, "dWqkv": 3e-2, "dbqkv": 3e-2, "dWo": 3e-2, "dbo": 3e-2}
+
+# Weights large enough that the softmax is far from uniform: at h = 512 the
+# logits have a standard deviation of about 1.3.
+STD = {"X": 1.0, "Wqkv": 0.05, "bqkv": 0.1, "Wo": 0.04, "bo": 0.1, "dZ": 1.0}
+
+# Peaky logits (std about 3.3, as in the h = 8192 workload).
+STD_PEAKY = dict(STD, Wqkv=0.08)
+
+
+@pytest.fixture(scope="module")
+def tp():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from tensor_transformer_mlp_tma_gb300 import tpmlp
+    return tpmlp
+
+
+def run_attn(tp, nb, S, h, heads, t, seed, std=STD, perm=None):
+    """perm, if given, reorders the columns of Wqkv and bqkv (a layout change)."""
+    from tensor_transformer_mlp_tma_gb300 import inputs
+    inp = inputs.make_attn(nb * S, h, seed, std)
+    if perm is not None:
+        pt = torch.as_tensor(perm)
+        inp = dict(inp, Wqkv=inp["Wqkv"][:, pt].contiguous(), bqkv=inp["bqkv"][pt].contiguous())
+    d = {k: v.cuda() for k, v in inp.items()}
+    ctx = tp.AttnContext(nb, S, h, heads, t)
+    Z = tp.attn_forward(ctx, d["X"], d["Wqkv"], d["bqkv"], d["Wo"], d["bo"])
+    g = tp.attn_backward(ctx, d["dZ"])
+    torch.cuda.synchronize()
+    assert tp.check_device_status(ctx) == tp.OK
+    out = {"QKV": ctx.QKV, "P": ctx.P.view(nb, heads, S, S), "O": ctx.O, "Z": Z}
+    out.update(g)
+    return inp, out, ctx
+
+
+def shard_major(h, heads, t):
+    """Column permutation from the [Q | K | V] layout (heads in order) to the
+    shard-major layout [Q_1 | K_1 | V_1 | Q_2 | ...] the library takes."""
+    d, hpt = h // heads, heads // t
+    perm = []
+    for i in range(t):
+        for which in range(3):
+            for j in range(hpt):
+                g = i * hpt + j
+                perm.extend(range(which * h + g * d, which * h + (g + 1) * d))
+    return np.array(perm)
+
+
+def oracle_ref(inp, nb, heads, t):
+    import oracle
+    f = {k: v.double().numpy() for k, v in inp.items()}
+    return oracle.attn_forward_backward(f["X"], f["Wqkv"], f["bqkv"], f["Wo"], f["bo"], f["dZ"], nb, heads, t)
+
+
+CASES = [
+    # nb, S, h, heads, t
+    (2, 256, 512, 4, 2),     # d = 128, one 256 x 256 score tile per head
+    (1, 520, 512, 8, 4),     # d = 64, three score tiles with a ragged tail of 8
+    (3, 136, 384, 3, 3),     # ragged single tile, t = 3
+    (2, 384, 256, 2, 1),     # t = 1
+]
+
+
+@pytest.mark.parametrize("nb,S,h,heads,t", CASES)
+def test_attention_matches_oracle(tp, nb, S, h, heads, t):
+    inp, out, _ = run_attn(tp, nb, S, h, heads, t, seed=11 + S)
+    ref = oracle_ref(inp, nb, heads, t)
+    errs = {k: rel(to_np(out[k]), ref[k]) for k in TOL}
+    bad = {k: v for k, v in errs.items() if not (v <= TOL[k])}
+    assert not bad, "outside tolerance: %s (all: %s)" % (bad, errs)
+
+
+def test_attention_peaky_logits_match_oracle(tp):
+    nb, S, h, heads, t = 1, 520, 512, 8, 4
+    inp, out, _ = run_attn(tp, nb, S, h, heads, t, seed=7, std=STD_PEAKY)
+    ref = oracle_ref(inp, nb, heads, t)
+    errs = {k: rel(to_np(out[k]), ref[k]) for k in TOL}
+    bad = {k: v for k, v in errs.items() if not (v <= TOL[k])}
+    assert not bad, "outside tolerance: %s (all: %s)" % (bad, errs)
+
+
+def test_causal_probabilities_are_exact_zero_above_diagonal(tp):
+    nb, S, h, heads, t = 1, 264, 256, 2, 2
+    _, out, _ = run_attn(tp, nb, S, h, heads, t, seed=5)
+    P = out["P"].float()
+    upper = torch.triu(torch.ones(S, S, dtype=torch.bool, device=P.device), diagonal=1)
+    assert torch.all(P[..., upper] == 0)
+    # each row is a distribution (bf16 rounding of up to S terms)
+    rs = P.sum(-1)
+    assert torch.all((rs - 1).abs() < 2e-2)
+
+
+def test_attention_is_bit_identical_across_runs(tp):
+    nb, S, h, heads, t = 2, 256, 512, 4, 4
+    _, a, _ = run_attn(tp, nb, S, h, heads, t, seed=3)
+    a = {k: v.clone() for k, v in a.items()}
+    _, b, _ = run_attn(tp, nb, S, h, heads, t, seed=3)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_sharding_does_not_change_the_math(tp):
+    """One model, its Wqkv columns laid out for t = 1 and for t = 4: the results
+    agree within the bf16 tolerance (the head split and the shard fold only
+    regroup fp32 sums; dWqkv comes back in each run's own column layout)."""
+    nb, S, h, heads = 1, 256, 512, 8
+    runs = {}
+    for t in (1, 4):
+        perm = shard_major(h, heads, t)
+        _, out, _ = run_attn(tp, nb, S, h, heads, t, seed=21, perm=perm)
+        out = dict(out, dWqkv=out["dWqkv"][:, torch.as_tensor(np.argsort(perm), device="cuda")])
+        runs[t] = out
+    for k in ("Z", "dX", "dWqkv", "dWo", "dbo"):
+        assert rel(to_np(runs[4][k]), to_np(runs[1][k])) < 1e-2, k
+
+
+def test_empty_batch(tp):
+    ctx = tp.AttnContext(0, 64, 256, 2, 2)
+    z = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    W = torch.randn(256, 768, device="cuda").bfloat16()
+    Wo = torch.randn(256, 256, device="cuda").bfloat16()
+    bq = torch.zeros(768, device="cuda").bfloat16()
+    bo = torch.zeros(256, device="cuda").bfloat16()
+    Z = tp.attn_forward(ctx, z, W, bq, Wo, bo)
+    assert Z.shape == (0, 256)
+    g = tp.attn_backward(ctx, z)
+    torch.cuda.synchronize()
+    for k in ("dWqkv", "dbqkv", "dWo", "dbo"):
+        assert torch.count_nonzero(g[k]) == 0, k
+
+
+def test_rejects_unsupported_shapes(tp):
+    # head size 32 (not a multiple of 64) and seq not a multiple of 8
+    for args in ((1, 64, 256, 8, 2), (1, 60, 256, 2, 2)):
+        ctx = tp.AttnContext(*args)
+        nb, S, h = args[0], args[1], args[2]
+        X = torch.zeros((nb * S, h), dtype=torch.bfloat16, device="cuda")
+        W = torch.zeros((h, 3 * h), dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(tp.TpmlpError) as e:
+            tp.attn_forward(ctx, X, W, torch.zeros(3 * h, dtype=torch.bfloat16, device="cuda"),
+                            torch.zeros((h, h), dtype=torch.bfloat16, device="cuda"),
+                            torch.zeros(h, dtype=torch.bfloat16, device="cuda"))
+        assert e.value.status == tp.ERR_UNSUPPORTED
+
+
+def test_full_size_prefix_matches_oracle(tp):
+    """At the benchmark's size (h = 8192, 64 heads of 128, t = 8, two sequences of
+    2048) the causal mask makes the first rows of each sequence depend only on
+    the rows before them: the oracle runs on a 64-token prefix of each sequence
+    and must match those rows of QKV, O and Z and the prefix block of P."""
+    from tensor_transformer_mlp_tma_gb300 import inputs
+    from tensor_transformer_mlp_tma_gb300.workloads import ATTN_WORKLOADS
+    import oracle
+    w = ATTN_WORKLOADS["attn-h8192"]
+    inp = inputs.make_attn(w.tokens, w.hidden, 0, {"Wqkv": w.std_W, "Wo": w.std_W, "bqkv": w.std_b,
+                                                  "bo": w.std_b})
+    d = {k: v.cuda() for k, v in inp.items() if k != "dZ"}
+    ctx = tp.AttnContext(w.batch, w.seq, w.hidden, w.heads, w.t)
+    Z = tp.attn_forward(ctx, d["X"], d["Wqkv"], d["bqkv"], d["Wo"], d["bo"])
+    torch.cuda.synchronize()
+    assert tp.check_device_status(ctx) == tp.OK
+    pre = 64
+    P = ctx.P.view(w.batch, w.heads, w.seq, w.seq)
+    f = {k: v.double().numpy() for k, v in inp.items()}
+    for b in range(w.batch):
+        rows = slice(b * w.seq, b * w.seq + pre)
+        ref = oracle.attn_forward(f["X"][rows], f["Wqkv"], f["bqkv"], f["Wo"], f["bo"], 1, w.heads, w.t)
+        got = {"QKV": ctx.QKV[rows], "O": ctx.O[rows], "Z": Z[rows], "P": P[b, :, :pre, :pre]}
+        for k, v in got.items():
+            e = rel(to_np(v), ref[k].reshape(to_np(v).shape))
+            assert e <= TOL[k], (b, k, e)
+        # probabilities past the prefix are zero on the prefix rows
+        assert torch.count_nonzero(P[b, :, :pre, pre:]) == 0
