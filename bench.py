@@ -42,12 +42,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, with the hash of the kernel source they were taken at.  A kernel whose
 # source has changed since reports traffic null.
 NCU_TRAFFIC = {  # profiles/dram_traffic_h8192_gemms.md (h8192 workload)
-    "fc1_bias_gelu": (2.02e9 + 0.51988e9, "1f33cdadddf3"),
-    "fc2_shard_fold": (2.58e9 + 0.10298e9, "1f33cdadddf3"),
-    "bwd_dY_dgelu": (2.60e9 + 0.27456e9, "1f33cdadddf3"),
-    "bwd_dB": (1.14e9 + 0.51904e9, "1f33cdadddf3"),
-    "bwd_dA": (1.19e9 + 0.51934e9, "1f33cdadddf3"),
-    "bwd_dX_shard_fold": (2.55e9 + 0.09327e9, "1f33cdadddf3"),
+    "fc1_bias_gelu": (1.886146e9 + 0.518090e9, "df838eaca9db"),
+    "fc2_shard_fold": (2.249016e9 + 0.088255e9, "df838eaca9db"),
+    "bwd_dY_dgelu": (2.494592e9 + 0.274302e9, "df838eaca9db"),
+    "bwd_dB": (1.008575e9 + 0.517443e9, "df838eaca9db"),
+    "bwd_dA": (1.014905e9 + 0.517276e9, "df838eaca9db"),
+    "bwd_dX_shard_fold": (2.198687e9 + 0.075029e9, "df838eaca9db"),
 }
 
 
@@ -441,7 +441,8 @@ def run_attn_bench(args, rank, world, local):
     ms_max = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
     value = w.flops_fwd_bwd * world / (ms_max * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
-    proj, head = 2.0 * T * h * h, 2.0 * T * S * h
+    # per-head products over the causal lower triangle (the work the path needs)
+    proj, head = 2.0 * T * h * h, 1.0 * T * (S + 1) * h
     gemm_flops = {"attn_qkv_proj": 3 * proj, "attn_out_proj_fold": proj, "attn_scores": head, "attn_pv": head,
                   "attn_bwd_dO": proj, "attn_bwd_dWo": proj, "attn_bwd_dV": head, "attn_bwd_dS": head,
                   "attn_bwd_dQ": head, "attn_bwd_dK": head, "attn_bwd_dWqkv": 3 * proj,
@@ -461,8 +462,8 @@ def run_attn_bench(args, rank, world, local):
             "config": {"workload": w.name, "batch": w.batch, "seq": S, "hidden": h, "heads": w.heads, "t": w.t,
                        "causal": True, "pass": "forward+backward",
                        "flops_per_step": w.flops_fwd_bwd,
-                       "flops_note": "projections 24*T*h^2 + per-head products 12*T*seq*h (full seq x seq, "
-                                     "masked half included, as run)",
+                       "flops_note": "projections 24*T*h^2 + per-head products 6*T*h*(seq+1) (the causal "
+                                     "lower triangle only; tiles above the diagonal are skipped)",
                        "l2": "per-step working set larger than L2"},
             "frac_of_peak": value / world / peak, "roofline": roof, "gpu_launches": int(sum_over_ranks(launches, world)),
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},

@@ -841,6 +841,7 @@ tpmlp_status tpmlp_attn_forward(const tpmlp_attn_shape *s, const void *X, const 
     GemmArgs g2 = head_gemm(status, Qh, false, Kh, false, S, S, d, nz, scores);
     g2.scale = 1.0f / std::sqrt(static_cast<float>(d));
     g2.causal = true;
+    g2.skip_upper = true;  // never read: the softmax stops at the diagonal
     e = gemm(&ms, "attn_scores", tpmlp::EPI_ATTN_SCORE, g2, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
@@ -853,6 +854,7 @@ tpmlp_status tpmlp_attn_forward(const tpmlp_attn_shape *s, const void *X, const 
 
     // O_head = P V
     GemmArgs g3 = head_gemm(status, saved->P, false, Vh, true, S, d, S, nz, Oh);
+    g3.causal_k = 1;  // P is zero past each row's last key
     e = gemm(&ms, "attn_pv", tpmlp::EPI_STORE, g3, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
@@ -950,6 +952,7 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
 
     // dV_head = P^T dO_head
     GemmArgs g3 = head_gemm(status, saved->P, true, dOh, true, S, d, S, nz, dVh);
+    g3.causal_k = 2;  // key j only gets gradient from queries i >= j
     e = gemm(&ms, "attn_bwd_dV", tpmlp::EPI_STORE, g3, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
@@ -958,14 +961,17 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
     g4.aux = saved->P;
     g4.rowvec = D;
     g4.scale = scale;
+    g4.skip_upper = true;  // dS is zero above the diagonal; dQ and dK below never read those tiles
     e = gemm(&ms, "attn_bwd_dS", tpmlp::EPI_ATTN_DS, g4, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
     // dQ_head = dS K_head,  dK_head = dS^T Q_head
     GemmArgs g5 = head_gemm(status, dS, false, Kh, true, S, d, S, nz, dQh);
+    g5.causal_k = 1;
     e = gemm(&ms, "attn_bwd_dQ", tpmlp::EPI_STORE, g5, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
     GemmArgs g6 = head_gemm(status, dS, true, Qh, true, S, d, S, nz, dKh);
+    g6.causal_k = 2;
     e = gemm(&ms, "attn_bwd_dK", tpmlp::EPI_STORE, g6, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 

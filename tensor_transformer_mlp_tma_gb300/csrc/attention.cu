@@ -69,6 +69,61 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 // One warp per score row.  Row r of a head (r = row % S) sees columns 0..r; the
 // others are written as exact zeros.  Max-subtracted exponentials, fp32 sum.
+// The row is read once, 16 bytes per lane at a time, into V float4 registers per
+// lane (S <= 128 V); only the columns up to the diagonal are read.
+template <int V>
+__global__ void __launch_bounds__(256)
+    softmax_reg_kernel(const float *__restrict__ S_, __nv_bfloat16 *__restrict__ P, int64_t rows, int64_t S,
+                       bool causal) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int64_t last = causal ? row % S : S - 1;
+    const float4 *in = reinterpret_cast<const float4 *>(S_ + row * S);
+    float4 x[V];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int64_t c = 4 * (lane + 32 * v);
+        if (c <= last) {
+            x[v] = __ldcs(in + lane + 32 * v);  // streamed: read once
+            if (c + 1 > last) x[v].y = -INFINITY;
+            if (c + 2 > last) x[v].z = -INFINITY;
+            if (c + 3 > last) x[v].w = -INFINITY;
+        } else {
+            x[v] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+        mx = fmaxf(mx, fmaxf(fmaxf(x[v].x, x[v].y), fmaxf(x[v].z, x[v].w)));
+    }
+    mx = warp_max(mx);
+    float sum = 0.0f;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        x[v].x = expf(x[v].x - mx);  // exp(-inf) = 0 for the masked columns
+        x[v].y = expf(x[v].y - mx);
+        x[v].z = expf(x[v].z - mx);
+        x[v].w = expf(x[v].w - mx);
+        sum += (x[v].x + x[v].y) + (x[v].z + x[v].w);
+    }
+    sum = warp_sum(sum);
+    const float inv = 1.0f / sum;
+    uint2 *out = reinterpret_cast<uint2 *>(P + row * S);
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int64_t c = 4 * (lane + 32 * v);
+        if (c < S) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(x[v].x * inv, x[v].y * inv);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(x[v].z * inv, x[v].w * inv);
+            uint2 w;
+            w.x = *reinterpret_cast<uint32_t *>(&lo);
+            w.y = *reinterpret_cast<uint32_t *>(&hi);
+            out[lane + 32 * v] = w;
+        }
+    }
+}
+
+// Rows longer than the register version holds: the same arithmetic with three
+// passes over the row (max, sum, write).
 __global__ void __launch_bounds__(256)
     softmax_kernel(const float *__restrict__ S_, __nv_bfloat16 *__restrict__ P, int64_t rows, int64_t S,
                    bool causal) {
@@ -140,8 +195,19 @@ cudaError_t launch_to_tokens(const HeadLayout &L, const void *h0, const void *h1
 
 cudaError_t launch_softmax(const float *S, void *P, int64_t rows, int64_t cols, bool causal, cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
-    attn::softmax_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
-        S, static_cast<__nv_bfloat16 *>(P), rows, cols, causal);
+    const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(P);
+    // 16-byte row starts (cols a multiple of 4) for the vector loads
+    if (cols % 4 != 0 || cols > 128 * 32)
+        attn::softmax_kernel<<<grid, 256, 0, st>>>(S, out, rows, cols, causal);
+    else if (cols <= 128 * 4)
+        attn::softmax_reg_kernel<4><<<grid, 256, 0, st>>>(S, out, rows, cols, causal);
+    else if (cols <= 128 * 8)
+        attn::softmax_reg_kernel<8><<<grid, 256, 0, st>>>(S, out, rows, cols, causal);
+    else if (cols <= 128 * 16)
+        attn::softmax_reg_kernel<16><<<grid, 256, 0, st>>>(S, out, rows, cols, causal);
+    else
+        attn::softmax_reg_kernel<32><<<grid, 256, 0, st>>>(S, out, rows, cols, causal);
     return cudaGetLastError();
 }
 

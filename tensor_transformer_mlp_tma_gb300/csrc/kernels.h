@@ -47,6 +47,11 @@ struct GemmArgs {
     float scale;          // EPI_ATTN_SCORE, EPI_ATTN_DS
     bool causal;          // EPI_ATTN_SCORE: mask columns past the row
     const float *rowvec;  // EPI_ATTN_DS: D, one fp32 per output row, [batch][M]
+    // Causal per-head products (tensor-core path, square M = K, one shard): only
+    // the k range the zero pattern leaves, in whole tiles.  1: k below the end of
+    // the M-tile (P V, dS K); 2: k from the start of the M-tile on (P^T dO, dS^T Q).
+    int causal_k;
+    bool skip_upper;  // skip tiles wholly above the diagonal (scores, dS)
 };
 
 // Tensor-core path: bf16 operands, fp32 accumulation in TMEM (tcgen05).

@@ -88,7 +88,29 @@ struct Params {
     float scale;
     int causal;
     const float *rowvec;
+    int causal_k;    // K range of an M-tile: 0 all; 1 k < end of the tile's rows; 2 k >= start of its rows
+    int skip_upper;  // tiles wholly above the diagonal (every column past every row) are not computed
 };
+
+// Causal per-head products.  Square per-head problems (M = K = seq) whose A or B
+// operand is zero above the diagonal need only part of K: P V and dS K only keys
+// up to the tile's last query (causal_k = 1), P^T dO and dS^T Q only queries from
+// the tile's first key on (causal_k = 2).  The range ends are multiples of the
+// tile height, so of BK.  With nshards = 1 the range is [kb0, kb1) in k-blocks.
+template <int TILE_M>
+__device__ __forceinline__ void k_range(const Params &p, int mb, int &kb0, int &kb1) {
+    kb0 = 0;
+    kb1 = p.nshards * p.kb_per_shard;
+    if (p.causal_k == 1) kb1 = min(kb1, (mb + 1) * (TILE_M / BK));
+    else if (p.causal_k == 2) kb0 = mb * (TILE_M / BK);
+}
+
+// Scores and dS are not needed above the diagonal: a tile whose first column lies
+// past its last row is skipped by every role (none of its outputs is read).
+template <int TILE_M>
+__device__ __forceinline__ bool tile_active(const Params &p, int mb, int nb) {
+    return !p.skip_upper || nb * BN <= mb * TILE_M + TILE_M - 1;
+}
 
 // Tile order: super-rows of `group` tiles along one dimension; inside a
 // super-row the grouped index runs fastest, so the CTAs resident at one time
@@ -474,7 +496,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem_base = tmem_base_sh;
 
     const int num_tiles = p.m_tiles * p.n_tiles * p.batch;
-    const int kb_total = p.nshards * p.kb_per_shard;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -486,9 +507,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
                 int mb, nb, zb;
                 tile_coords(tile, p, mb, nb, zb);
+                if (!tile_active<C::TILE_M>(p, mb, nb)) continue;
                 const int m0 = mb * C::TILE_M + BM * static_cast<int>(rank);
                 const int n0 = nb * BN + C::B_ROWS * static_cast<int>(rank);
-                for (int kb = 0; kb < kb_total; ++kb) {
+                int kb0, kb1;
+                k_range<C::TILE_M>(p, mb, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_empty[stage]), phase ^ 1u, p.wait_ns,
                                                      &abort_sh)) {
                         ok = false;
@@ -551,6 +575,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t unit = 0;
             bool ok = true;
             for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
+                int mb, nb, zb;
+                tile_coords(tile, p, mb, nb, zb);
+                if (!tile_active<C::TILE_M>(p, mb, nb)) continue;
+                int kb0, kb1;
+                k_range<C::TILE_M>(p, mb, kb0, kb1);
+                // one shard: the tile's k-block range; several: kb_per_shard blocks each
+                if (p.nshards > 1) kb0 = 0, kb1 = p.kb_per_shard;
                 for (int s = 0; s < p.nshards && ok; ++s, ++unit) {
                     const uint32_t buf = unit & 1u, use = unit >> 1;
                     if (!ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_tempty[buf]), (use & 1u) ^ 1u, p.wait_ns,
@@ -560,7 +591,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BN;
-                    for (int kb = 0; kb < p.kb_per_shard; ++kb) {
+                    for (int kb = kb0; kb < kb1; ++kb) {
                         if (!ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_full[stage]), phase, p.wait_ns,
                                                          &abort_sh)) {
                             ok = false;
@@ -576,9 +607,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const uint64_t bd = B_MN ? ptx::sdesc_sw128(sb + k * 2048, MN_BLOCK_BYTES, 1024)
                                                      : ptx::sdesc_sw128(sb + k * 32, 16, 1024);
                             if constexpr (PAIR)
-                                ptx::umma_f16_ss_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                                ptx::umma_f16_ss_pair(d_tmem, ad, bd, IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
                             else
-                                ptx::umma_f16_ss(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                                ptx::umma_f16_ss(d_tmem, ad, bd, IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
                         }
                         if constexpr (PAIR)
                             ptx::umma_commit_pair_multicast(ptx::smem_u32(&bar_empty[stage]), 0x3);
@@ -632,6 +663,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
             int mb, nb, zb;
             tile_coords(tile, p, mb, nb, zb);
+            if (!tile_active<C::TILE_M>(p, mb, nb)) continue;
             const int row0 = mb * C::TILE_M + BM * static_cast<int>(rank) + quarter * 32;
             const int64_t row = static_cast<int64_t>(row0) + lane;
             const int col0 = nb * BN + half * 128;
@@ -855,6 +887,14 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     p.scale = g.scale;
     p.causal = g.causal ? 1 : 0;
     p.rowvec = g.rowvec;
+    p.causal_k = g.causal_k;
+    p.skip_upper = g.skip_upper ? 1 : 0;
+    // The causal ranges are defined for square per-head problems in one shard.
+    if ((g.causal_k != 0 || g.skip_upper) && (g.nshards != 1 || (g.causal_k != 0 && g.M != g.K))) {
+        set_last_error("causal K ranges need one shard and M = K (M=%lld K=%lld, %d shards)",
+                       static_cast<long long>(g.M), static_cast<long long>(g.K), g.nshards);
+        return cudaErrorInvalidValue;
+    }
     const int tiles = p.m_tiles * p.n_tiles * p.batch;
     int resident = max_clusters[dev];
     if (const char *o = std::getenv("TPMLP_MAX_UNITS")) resident = std::atoi(o) > 0 ? std::atoi(o) : resident;

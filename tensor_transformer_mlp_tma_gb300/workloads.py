@@ -90,9 +90,11 @@ class AttnWorkload:
     @property
     def flops_fwd(self) -> float:
         """QKV and output projections (2*T*h*3h + 2*T*h*h) plus the two per-head
-        products Q K^T and P V over the full seq x seq scores (4*T*seq*h), as run."""
+        products Q K^T and P V over the causal lower triangle only: per head
+        seq*(seq+1)/2 dot products of length d each, 2*T*h*(seq+1) for both.
+        The masked upper triangle is not counted (the kernels skip it)."""
         T, h = self.tokens, self.hidden
-        return 8.0 * T * h * h + 4.0 * T * self.seq * h
+        return 8.0 * T * h * h + 2.0 * T * h * (self.seq + 1)
 
     @property
     def flops_fwd_bwd(self) -> float:

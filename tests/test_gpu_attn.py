@@ -5,8 +5,9 @@ output projection row-parallel with the fixed-order shard fold ("Megatron-LM"
 industry report, section 4.1).  Every case runs the tensor-core path through the
 C ABI and compares, element by element, the saved activations (QKV, P, O), the
 output Z and every gradient with the oracle on the same seeded bf16 inputs.
-Shapes span several 256-wide tiles of the per-head products, ragged sequence
-tails, head sizes 64 and 128, t = 1..4, and the empty batch.
+Shapes span several 256-wide tiles of the per-head products (whose causal
+tile skipping and K ranges depend on the tile row), ragged sequence tails, every
+softmax row-length class, head sizes 64 and 128, t = 1..4, and the empty batch.
 """
 import numpy as np
 import pytest
@@ -86,6 +87,8 @@ CASES = [
     (1, 520, 512, 8, 4),     # d = 64, three score tiles with a ragged tail of 8
     (3, 136, 384, 3, 3),     # ragged single tile, t = 3
     (2, 384, 256, 2, 1),     # t = 1
+    (1, 2056, 256, 2, 2),    # rows past 2048 columns (widest register softmax)
+    (1, 4104, 128, 1, 1),    # rows past 4096 columns (multi-pass softmax)
 ]
 
 
@@ -199,3 +202,15 @@ def test_full_size_prefix_matches_oracle(tp):
             assert e <= TOL[k], (b, k, e)
         # probabilities past the prefix are zero on the prefix rows
         assert torch.count_nonzero(P[b, :, :pre, pre:]) == 0
+
+
+def test_attention_single_cta_tiles_match_oracle(tp, monkeypatch):
+    """128-row tiles on single CTAs: the causal tile skipping and K ranges follow
+    the tile height."""
+    monkeypatch.setenv("TPMLP_CTA_PAIR", "0")
+    nb, S, h, heads, t = 1, 520, 512, 8, 4
+    inp, out, _ = run_attn(tp, nb, S, h, heads, t, seed=9)
+    ref = oracle_ref(inp, nb, heads, t)
+    errs = {k: rel(to_np(out[k]), ref[k]) for k in TOL}
+    bad = {k: v for k, v in errs.items() if not (v <= TOL[k])}
+    assert not bad, "outside tolerance: %s (all: %s)" % (bad, errs)
