@@ -320,58 +320,104 @@ def run_ours(args, rank, world, local, w=None, quiet=False):
         roof = {"bound": "hbm", "kernel": name, "achieved": None, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": None, "traffic": None}
 
-    # ---- end to end: pinned host inputs in, results out, every step
+    # ---- end to end: pinned host inputs in, results out, every step.  The copies
+    # run on their own streams, overlapped with compute: step i+1's inputs are
+    # copied in while step i computes, and step i's results are copied out while
+    # step i+1 computes (device inputs and outputs double-buffered).  The timed
+    # region opens before the first step's input copy and closes after the last
+    # step's results have reached host memory.
     e2e = None
     if not args.no_e2e:
         hX = host["X"].pin_memory()
         hdZ = host["dZ"].pin_memory()
-        oZ = torch.empty((T, h), dtype=dt).pin_memory()
-        odX = torch.empty((T, h), dtype=dt).pin_memory()
-        oda = torch.empty((F,), dtype=dt).pin_memory()
-        odb = torch.empty((h,), dtype=dt).pin_memory()
-        dX_in = torch.empty_like(d["X"])
-        dZ_in = torch.empty_like(d["dZ"])
+        Xd = [torch.empty_like(d["X"]) for _ in range(2)]
+        dZd = [torch.empty_like(d["dZ"]) for _ in range(2)]
+        Zd = [torch.empty((T, h), dtype=dt, device=dev) for _ in range(2)]
+        gd = [{k: torch.empty_like(v) for k, v in g.items()} for _ in range(2)]
+        oZ = [torch.empty((T, h), dtype=dt).pin_memory() for _ in range(2)]
+        odX = [torch.empty((T, h), dtype=dt).pin_memory() for _ in range(2)]
+        oda = [torch.empty((F,), dtype=dt).pin_memory() for _ in range(2)]
+        odb = [torch.empty((h,), dtype=dt).pin_memory() for _ in range(2)]
+        s_in = torch.cuda.Stream(device=dev)
+        s_out = torch.cuda.Stream(device=dev)
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        fwd_done = [torch.cuda.Event() for _ in range(2)]
+        step_done = [torch.cuda.Event() for _ in range(2)]
+        out_done = [torch.cuda.Event() for _ in range(2)]
+        pend = {"done": [False, False], "out": [False, False]}
 
-        def e2e_step():
-            dX_in.copy_(hX, non_blocking=True)
-            if not args.fwd_only:
-                dZ_in.copy_(hdZ, non_blocking=True)
+        def copy_in(b):
+            if pend["done"][b]:  # the step that last read buffer b has finished
+                s_in.wait_event(step_done[b])
+            with torch.cuda.stream(s_in):
+                Xd[b].copy_(hX, non_blocking=True)
+                if not args.fwd_only:
+                    dZd[b].copy_(hdZ, non_blocking=True)
+            in_ready[b].record(s_in)
+
+        def e2e_step(i, last):
+            b = i % 2
+            stream.wait_event(in_ready[b])
+            if pend["out"][b]:  # results of step i-2 have left buffer b
+                stream.wait_event(out_done[b])
             if args.sp:
-                tpmlp.sp_forward(ctx, dX_in, gamma, beta, d["A"], d["a"], d["B"], d["b"], Z=Z, stream=stream)
+                tpmlp.sp_forward(ctx, Xd[b], gamma, beta, d["A"], d["a"], d["B"], d["b"], Z=Zd[b], stream=stream)
             else:
-                tpmlp.forward(ctx, dX_in, d["A"], d["a"], d["B"], d["b"], Z=Z, stream=stream)
-            oZ.copy_(Z, non_blocking=True)
+                tpmlp.forward(ctx, Xd[b], d["A"], d["a"], d["B"], d["b"], Z=Zd[b], stream=stream)
+            fwd_done[b].record(stream)
             if not args.fwd_only:
                 if args.sp:
-                    tpmlp.sp_backward(ctx, dZ_in, stream=stream, dX_in=g["dX"], dgamma=sp_dg, dbeta=sp_db,
-                                      dA=g["dA"], da=g["da"], dB=g["dB"], db=g["db"])
+                    tpmlp.sp_backward(ctx, dZd[b], stream=stream, dX_in=gd[b]["dX"], dgamma=sp_dg, dbeta=sp_db,
+                                      dA=gd[b]["dA"], da=gd[b]["da"], dB=gd[b]["dB"], db=gd[b]["db"])
                 else:
-                    tpmlp.backward(ctx, dZ_in, stream=stream, **g)
-                odX.copy_(g["dX"], non_blocking=True)
-                oda.copy_(g["da"], non_blocking=True)
-                odb.copy_(g["db"], non_blocking=True)
+                    tpmlp.backward(ctx, dZd[b], stream=stream, **gd[b])
+            step_done[b].record(stream)
+            pend["done"][b] = True
+            if not last:
+                copy_in(b ^ 1)
+            s_out.wait_event(fwd_done[b])
+            with torch.cuda.stream(s_out):
+                oZ[b].copy_(Zd[b], non_blocking=True)
+            if not args.fwd_only:
+                s_out.wait_event(step_done[b])
+                with torch.cuda.stream(s_out):
+                    odX[b].copy_(gd[b]["dX"], non_blocking=True)
+                    oda[b].copy_(gd[b]["da"], non_blocking=True)
+                    odb[b].copy_(gd[b]["db"], non_blocking=True)
+            out_done[b].record(s_out)
+            pend["out"][b] = True
 
-        with torch.cuda.stream(stream):
-            for _ in range(max(1, args.warmup)):
-                e2e_step()
+        def run_steps(n, start_event=None, end_event=None):
+            if start_event is not None:
+                start_event.record(stream)
+                s_in.wait_event(start_event)
+            copy_in(0)
+            for i in range(n):
+                e2e_step(i, i == n - 1)
+            for b in range(2):
+                if pend["out"][b]:
+                    stream.wait_event(out_done[b])
+            if end_event is not None:
+                end_event.record(stream)
             torch.cuda.synchronize(dev)
-            barrier(world)
-            f0 = torch.cuda.Event(enable_timing=True)
-            f1 = torch.cuda.Event(enable_timing=True)
-            f0.record(stream)
-            for _ in range(args.steps):
-                e2e_step()
-            f1.record(stream)
-            torch.cuda.synchronize(dev)
+            pend["done"] = [False, False]
+            pend["out"] = [False, False]
+
+        run_steps(max(1, args.warmup))
+        barrier(world)
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        run_steps(args.steps, f0, f1)
         barrier(world)
         ems = max_over_ranks(f0.elapsed_time(f1) / args.steps, world)
         esz = hX.element_size()
         h2d = hX.numel() + (0 if args.fwd_only else hdZ.numel())
-        d2h = oZ.numel() + (0 if args.fwd_only else odX.numel() + oda.numel() + odb.numel())
+        d2h = oZ[0].numel() + (0 if args.fwd_only else odX[0].numel() + oda[0].numel() + odb[0].numel())
         e2e = {"value": flops * world / (ems * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ems,
                "h2d_bytes_per_step": h2d * esz, "d2h_bytes_per_step": d2h * esz,
                "what": "X and dZ copied in from pinned host memory, Z, dX, da, db copied out, every "
-                       "step; weights and weight gradients stay resident"}
+                       "step, on copy streams overlapped with the neighbouring steps' compute; weights "
+                       "and weight gradients stay resident"}
 
     clk = clocks.summary()
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
