@@ -42,12 +42,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, with the hash of the kernel source they were taken at.  A kernel whose
 # source has changed since reports traffic null.
 NCU_TRAFFIC = {  # profiles/dram_traffic_h8192_gemms.md (h8192 workload)
-    "fc1_bias_gelu": (1.886146e9 + 0.518090e9, "df838eaca9db"),
-    "fc2_shard_fold": (2.249016e9 + 0.088255e9, "df838eaca9db"),
-    "bwd_dY_dgelu": (2.494592e9 + 0.274302e9, "df838eaca9db"),
-    "bwd_dB": (1.008575e9 + 0.517443e9, "df838eaca9db"),
-    "bwd_dA": (1.014905e9 + 0.517276e9, "df838eaca9db"),
-    "bwd_dX_shard_fold": (2.198687e9 + 0.075029e9, "df838eaca9db"),
+    "fc1_bias_gelu": (1.995372e9 + 0.519934e9, "9e753c7ea958"),
+    "fc2_shard_fold": (2.199154e9 + 0.080803e9, "9e753c7ea958"),
+    "bwd_dY_dgelu": (2.678131e9 + 0.274630e9, "9e753c7ea958"),
+    "bwd_dB": (1.078401e9 + 0.517316e9, "9e753c7ea958"),
+    "bwd_dA": (1.063686e9 + 0.517553e9, "9e753c7ea958"),
+    "bwd_dX_shard_fold": (2.637676e9 + 0.095505e9, "9e753c7ea958"),
 }
 
 

@@ -591,34 +591,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BN;
-                    for (int kb = kb0; kb < kb1; ++kb) {
+                    // Stages are taken two at a time where an operand is K-major: wait
+                    // for both, then issue their eight MMAs back to back.  Measured on
+                    // GB300 this issues 2-7% faster per clock than one stage at a time;
+                    // with both operands MN-major (load-bound) single stages are faster.
+                    for (int kb = kb0; kb < kb1;) {
+                        const int nst = (!(A_MN && B_MN) && kb + 1 < kb1) ? 2 : 1;
+                        int st2 = stage + 1;
+                        uint32_t ph2 = phase;
+                        if (st2 == STAGES) st2 = 0, ph2 ^= 1u;
                         if (!ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_full[stage]), phase, p.wait_ns,
                                                          &abort_sh)) {
                             ok = false;
                             break;
                         }
+                        if (nst == 2 &&
+                            !ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_full[st2]), ph2, p.wait_ns, &abort_sh)) {
+                            ok = false;
+                            break;
+                        }
                         ptx::tc_fence_after();
-                        const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
-                        const uint32_t sb = sa + C::A_STAGE;
+                        for (int q = 0; q < nst; ++q) {
+                            const int kk = kb + q;
+                            const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
+                            const uint32_t sb = sa + C::A_STAGE;
 #pragma unroll
-                        for (int k = 0; k < BK / 16; ++k) {
-                            const uint64_t ad = A_MN ? ptx::sdesc_sw128(sa + k * 2048, MN_BLOCK_BYTES, 1024)
-                                                     : ptx::sdesc_sw128(sa + k * 32, 16, 1024);
-                            const uint64_t bd = B_MN ? ptx::sdesc_sw128(sb + k * 2048, MN_BLOCK_BYTES, 1024)
-                                                     : ptx::sdesc_sw128(sb + k * 32, 16, 1024);
+                            for (int k = 0; k < BK / 16; ++k) {
+                                const uint64_t ad = A_MN ? ptx::sdesc_sw128(sa + k * 2048, MN_BLOCK_BYTES, 1024)
+                                                         : ptx::sdesc_sw128(sa + k * 32, 16, 1024);
+                                const uint64_t bd = B_MN ? ptx::sdesc_sw128(sb + k * 2048, MN_BLOCK_BYTES, 1024)
+                                                         : ptx::sdesc_sw128(sb + k * 32, 16, 1024);
+                                const uint32_t acc = (kk != kb0 || k != 0) ? 1u : 0u;
+                                if constexpr (PAIR)
+                                    ptx::umma_f16_ss_pair(d_tmem, ad, bd, IDESC, acc);
+                                else
+                                    ptx::umma_f16_ss(d_tmem, ad, bd, IDESC, acc);
+                            }
                             if constexpr (PAIR)
-                                ptx::umma_f16_ss_pair(d_tmem, ad, bd, IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
+                                ptx::umma_commit_pair_multicast(ptx::smem_u32(&bar_empty[stage]), 0x3);
                             else
-                                ptx::umma_f16_ss(d_tmem, ad, bd, IDESC, (kb != kb0 || k != 0) ? 1u : 0u);
+                                ptx::umma_commit(ptx::smem_u32(&bar_empty[stage]));
+                            if (++stage == STAGES) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
                         }
-                        if constexpr (PAIR)
-                            ptx::umma_commit_pair_multicast(ptx::smem_u32(&bar_empty[stage]), 0x3);
-                        else
-                            ptx::umma_commit(ptx::smem_u32(&bar_empty[stage]));
-                        if (++stage == STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                        kb += nst;
                     }
                     if (!ok) break;
                     if constexpr (PAIR)
