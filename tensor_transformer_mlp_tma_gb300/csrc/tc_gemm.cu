@@ -90,6 +90,7 @@ struct Params {
     const float *rowvec;
     int causal_k;    // K range of an M-tile: 0 all; 1 k < end of the tile's rows; 2 k >= start of its rows
     int skip_upper;  // tiles wholly above the diagonal (every column past every row) are not computed
+    int a_mn4, b_mn4;  // MN-major operand mapped as 4-D (all of a stage's 64-wide blocks in one copy)
 };
 
 // Causal per-head products.  Square per-head problems (M = K = seq) whose A or B
@@ -529,18 +530,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         else
                             ptx::tma_load_3d(dst, map, full, x, y, zb);
                     };
+                    // one copy of every 64-wide MN block of the stage: (0, k, block, problem)
+                    auto load4 = [&](uint32_t dst, const CUtensorMap *map, int k, int blk) {
+                        if constexpr (PAIR)
+                            ptx::tma_load_4d_pair(dst, map, full, 0, k, blk, zb);
+                        else
+                            ptx::tma_load_4d(dst, map, full, 0, k, blk, zb);
+                    };
                     // The leader announces the bytes of both CTAs' copies; the peer's
                     // copies only complete bytes on the leader's barrier (they can land
                     // before the announcement: the phase still needs the arrival).
                     if (leader) ptx::mbar_arrive_expect_tx(full_local, CG * C::STAGE_BYTES);
                     if constexpr (!A_MN) {
                         load(sa, &tmA, k0, m0);
+                    } else if (p.a_mn4) {
+                        load4(sa, &tmA, k0, m0 / 64);
                     } else {
 #pragma unroll
                         for (int j = 0; j < BM / 64; ++j) load(sa + j * MN_BLOCK_BYTES, &tmA, m0 + 64 * j, k0);
                     }
                     if constexpr (!B_MN) {
                         load(sb, &tmB, k0, n0);
+                    } else if (p.b_mn4) {
+                        load4(sb, &tmB, k0, n0 / 64);
                     } else {
 #pragma unroll
                         for (int j = 0; j < C::B_ROWS / 64; ++j)
@@ -807,6 +819,28 @@ static bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols
     return r == CUDA_SUCCESS;
 }
 
+// An MN-major operand [K, MN] (MN contiguous, MN a multiple of 64) as the 4-D
+// tensor (64, K, MN/64, batch): one copy brings `nblk` consecutive 64-wide MN
+// blocks of `box_k` rows, laid out block after block in shared memory exactly
+// as the per-block copies do.  The third dimension steps 128 bytes, inside the
+// row pitch of the second; returns false if the driver does not take the map
+// (the caller then keeps the per-block 3-D map).
+static bool make_map_mn4(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, uint32_t box_k,
+                         uint32_t nblk, int64_t batch) {
+    auto fn = encode_fn();
+    if (!fn || cols % 64 != 0) return false;
+    cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64),
+                          static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(cols) * 2, 128,
+                             static_cast<cuuint64_t>(cols) * static_cast<cuuint64_t>(rows) * 2};
+    cuuint32_t box[4] = {64, box_k, nblk, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int EPI, bool A_MN, bool B_MN, int CG>
 static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     using C = Cfg<CG>;
@@ -861,9 +895,17 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     // B operand: this CTA's B_ROWS columns, K-major in one box or MN-major in 64-wide boxes.
     const int64_t nb = g.batch < 1 ? 1 : g.batch;
     const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
-    const bool oka = A_MN ? make_map(&ma, g.a, g.K, g.M, 64, BK, sw, nb) : make_map(&ma, g.a, g.M, g.K, BK, BM, sw, nb);
-    const bool okb = B_MN ? make_map(&mb, g.b, g.K, g.N, 64, BK, sw, nb)
-                          : make_map(&mb, g.b, g.N, g.K, BK, C::B_ROWS, sw, nb);
+    // MN-major operands whose MN extent is a multiple of 64 take the 4-D map
+    // (one copy per stage instead of one per 64-wide block); TPMLP_MN4=0 keeps
+    // the per-block maps (a tuning knob, read per call).
+    const char *mn4_env = std::getenv("TPMLP_MN4");
+    const bool mn4 = !(mn4_env && mn4_env[0] == '0');
+    const bool a4 = A_MN && mn4 && g.M % 64 == 0 && make_map_mn4(&ma, g.a, g.K, g.M, BK, BM / 64, nb);
+    const bool b4 = B_MN && mn4 && g.N % 64 == 0 && make_map_mn4(&mb, g.b, g.K, g.N, BK, C::B_ROWS / 64, nb);
+    const bool oka = a4 || (A_MN ? make_map(&ma, g.a, g.K, g.M, 64, BK, sw, nb)
+                                 : make_map(&ma, g.a, g.M, g.K, BK, BM, sw, nb));
+    const bool okb = b4 || (B_MN ? make_map(&mb, g.b, g.K, g.N, 64, BK, sw, nb)
+                                 : make_map(&mb, g.b, g.N, g.K, BK, C::B_ROWS, sw, nb));
     if (!oka || !okb) return cudaErrorInvalidValue;
     // Output maps: [M, N] row-major, 32 x 32 boxes, 64-byte swizzle (matches stage_row).
     // Bias + GeLU writes H (optional) and Y; GeLU' reads H through the second map;
@@ -906,6 +948,8 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     p.causal = g.causal ? 1 : 0;
     p.rowvec = g.rowvec;
     p.causal_k = g.causal_k;
+    p.a_mn4 = a4 ? 1 : 0;
+    p.b_mn4 = b4 ? 1 : 0;
     p.skip_upper = g.skip_upper ? 1 : 0;
     // The causal ranges are defined for square per-head problems in one shard.
     if ((g.causal_k != 0 || g.skip_upper) && (g.nshards != 1 || (g.causal_k != 0 && g.M != g.K))) {
