@@ -42,12 +42,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, with the hash of the kernel source they were taken at.  A kernel whose
 # source has changed since reports traffic null.
 NCU_TRAFFIC = {  # profiles/dram_traffic_h8192_gemms.md (h8192 workload)
-    "fc1_bias_gelu": (1.995372e9 + 0.519934e9, "9e753c7ea958"),
-    "fc2_shard_fold": (2.199154e9 + 0.080803e9, "9e753c7ea958"),
-    "bwd_dY_dgelu": (2.678131e9 + 0.274630e9, "9e753c7ea958"),
-    "bwd_dB": (1.078401e9 + 0.517316e9, "9e753c7ea958"),
-    "bwd_dA": (1.063686e9 + 0.517553e9, "9e753c7ea958"),
-    "bwd_dX_shard_fold": (2.637676e9 + 0.095505e9, "9e753c7ea958"),
+    "fc1_bias_gelu": (1.958879e9 + 0.519755e9, "56a669b34d54"),
+    "fc2_shard_fold": (2.289380e9 + 0.092381e9, "56a669b34d54"),
+    "bwd_dY_dgelu": (2.630839e9 + 0.274798e9, "56a669b34d54"),
+    "bwd_dB": (1.008790e9 + 0.516112e9, "56a669b34d54"),
+    "bwd_dA": (0.989859e9 + 0.515640e9, "56a669b34d54"),
+    "bwd_dX_shard_fold": (2.468365e9 + 0.091914e9, "56a669b34d54"),
 }
 
 

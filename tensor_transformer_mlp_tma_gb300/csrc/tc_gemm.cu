@@ -603,12 +603,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BN;
-                    // Stages are taken two at a time where an operand is K-major: wait
-                    // for both, then issue their eight MMAs back to back.  Measured on
-                    // GB300 this issues 2-7% faster per clock than one stage at a time;
-                    // with both operands MN-major (load-bound) single stages are faster.
+                    // Stages are taken two at a time: wait for both, then issue their
+                    // eight MMAs back to back.  Measured on GB300 this issues 2-7% faster
+                    // per clock than one stage at a time (MN/MN GEMMs gain once their
+                    // operands come in one 4-D copy per stage).
                     for (int kb = kb0; kb < kb1;) {
-                        const int nst = (!(A_MN && B_MN) && kb + 1 < kb1) ? 2 : 1;
+                        const int nst = (kb + 1 < kb1) ? 2 : 1;
                         int st2 = stage + 1;
                         uint32_t ph2 = phase;
                         if (st2 == STAGES) st2 = 0, ph2 ^= 1u;
