@@ -17,42 +17,50 @@
 namespace tpmlp {
 namespace attn {
 
-// Column of head g's Q (which = 0), K (1) or V (2) in the shard-major QKV layout,
-// or of head g in O when qkv is false.
-__device__ __forceinline__ int64_t head_col(bool qkv, int64_t h, int t, int64_t d, int64_t hpt, int64_t g,
-                                            int which) {
-    if (!qkv) return g * d;
-    const int64_t i = g / hpt, j = g % hpt;
-    return i * (3 * h / t) + which * (h / t) + j * d;
-}
-
-// One thread moves 8 bf16 (16 bytes).  to_heads: token-major -> head blocks.
+// One block per token row r = b*S + s.  The row's nmat*h elements (QKV: its 3h
+// shard-major columns [Q_i | K_i | V_i]; O or dO: its h columns, head g at g*d)
+// move in 16-byte vectors, consecutive threads on consecutive vectors: reads of
+// the token row and writes of each head's d-wide row are both contiguous.
+// Column c of the row belongs to matrix `which`, head g = i*hpt + j, element e:
+//   QKV: i = c / (3h/t), which = (c mod 3h/t) / (h/t), j = (c mod h/t) / d;
+//   O:   g = c / d.
+// The per-head address is ((b*heads + g)*S + s)*d + e.
 __global__ void __launch_bounds__(256)
     permute_kernel(const HeadLayout L, const __nv_bfloat16 *__restrict__ tok, __nv_bfloat16 *__restrict__ tok_out,
                    const __nv_bfloat16 *__restrict__ h0, const __nv_bfloat16 *__restrict__ h1,
                    const __nv_bfloat16 *__restrict__ h2, __nv_bfloat16 *__restrict__ o0,
                    __nv_bfloat16 *__restrict__ o1, __nv_bfloat16 *__restrict__ o2, bool to_heads) {
-    const int64_t vec_per_row = L.d / 8;
-    const int64_t per_tensor = L.nb * L.heads * L.S * vec_per_row;
-    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (idx >= per_tensor * L.nmat) return;
-    const int which = static_cast<int>(idx / per_tensor);
-    int64_t rem = idx - which * per_tensor;
-    const int64_t e8 = rem % vec_per_row;
-    rem /= vec_per_row;
-    const int64_t s = rem % L.S;
-    const int64_t z = rem / L.S;
-    const int64_t b = z / L.heads, g = z % L.heads;
-    const int64_t ld = L.qkv ? 3 * L.h : L.h;
-    const int64_t tok_off = (b * L.S + s) * ld + head_col(L.qkv, L.h, L.t, L.d, L.heads / L.t, g, which) + e8 * 8;
-    const int64_t head_off = (z * L.S + s) * L.d + e8 * 8;
-    if (to_heads) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(tok + tok_off));
-        __nv_bfloat16 *dst = which == 0 ? o0 : (which == 1 ? o1 : o2);
-        *reinterpret_cast<uint4 *>(dst + head_off) = v;
-    } else {
-        const __nv_bfloat16 *src = which == 0 ? h0 : (which == 1 ? h1 : h2);
-        *reinterpret_cast<uint4 *>(tok_out + tok_off) = __ldg(reinterpret_cast<const uint4 *>(src + head_off));
+    const int64_t r = blockIdx.x;
+    const int64_t b = r / L.S, s = r - b * L.S;
+    const int h = static_cast<int>(L.h), d = static_cast<int>(L.d), heads = static_cast<int>(L.heads);
+    const int hs = h / L.t, hpt = heads / L.t;
+    const int ld = L.qkv ? 3 * h : h;
+    const int nvec = L.nmat * h / 8;
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+        const int c = v * 8;
+        int which = 0, g, e;
+        if (L.qkv) {
+            const int i = c / (3 * hs);
+            int rem = c - i * 3 * hs;
+            which = rem / hs;
+            rem -= which * hs;
+            const int j = rem / d;
+            e = rem - j * d;
+            g = i * hpt + j;
+        } else {
+            g = c / d;
+            e = c - g * d;
+        }
+        const int64_t head_off = ((b * heads + g) * L.S + s) * d + e;
+        const int64_t tok_off = r * ld + c;
+        if (to_heads) {
+            const uint4 val = __ldg(reinterpret_cast<const uint4 *>(tok + tok_off));
+            __nv_bfloat16 *dst = which == 0 ? o0 : (which == 1 ? o1 : o2);
+            *reinterpret_cast<uint4 *>(dst + head_off) = val;
+        } else {
+            const __nv_bfloat16 *src = which == 0 ? h0 : (which == 1 ? h1 : h2);
+            *reinterpret_cast<uint4 *>(tok_out + tok_off) = __ldg(reinterpret_cast<const uint4 *>(src + head_off));
+        }
     }
 }
 
@@ -174,9 +182,9 @@ __global__ void __launch_bounds__(256)
 }  // namespace attn
 
 cudaError_t launch_to_heads(const HeadLayout &L, const void *tok, void *h0, void *h1, void *h2, cudaStream_t st) {
-    const int64_t n = L.nmat * L.nb * L.heads * L.S * (L.d / 8);
-    if (n <= 0) return cudaSuccess;
-    attn::permute_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+    const int64_t rows = L.nb * L.S;
+    if (rows <= 0) return cudaSuccess;
+    attn::permute_kernel<<<static_cast<unsigned>(rows), 256, 0, st>>>(
         L, static_cast<const __nv_bfloat16 *>(tok), nullptr, nullptr, nullptr, nullptr,
         static_cast<__nv_bfloat16 *>(h0), static_cast<__nv_bfloat16 *>(h1), static_cast<__nv_bfloat16 *>(h2), true);
     return cudaGetLastError();
@@ -184,9 +192,9 @@ cudaError_t launch_to_heads(const HeadLayout &L, const void *tok, void *h0, void
 
 cudaError_t launch_to_tokens(const HeadLayout &L, const void *h0, const void *h1, const void *h2, void *tok,
                              cudaStream_t st) {
-    const int64_t n = L.nmat * L.nb * L.heads * L.S * (L.d / 8);
-    if (n <= 0) return cudaSuccess;
-    attn::permute_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+    const int64_t rows = L.nb * L.S;
+    if (rows <= 0) return cudaSuccess;
+    attn::permute_kernel<<<static_cast<unsigned>(rows), 256, 0, st>>>(
         L, nullptr, static_cast<__nv_bfloat16 *>(tok), static_cast<const __nv_bfloat16 *>(h0),
         static_cast<const __nv_bfloat16 *>(h1), static_cast<const __nv_bfloat16 *>(h2), nullptr, nullptr, nullptr,
         false);
