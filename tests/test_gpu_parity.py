@@ -1,7 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
 
 Small shapes are compared element by element on every output; they span several
-128x256 tiles and leave ragged tails in every dimension.  The named workloads
+256x256 (CTA pair) and 128x256 (single CTA) tiles and leave ragged tails in
+every dimension.  The named workloads
 are run at full size in the same launch configuration as the benchmark and
 compared on seeded rows and ffn columns against the exact slice oracle.
 """
@@ -33,6 +34,21 @@ SMALL = [
 @pytest.mark.parametrize("T,h,F,t", SMALL)
 def test_tensor_core_path_matches_oracle(T, h, F, t):
     inp = inputs.make(T, h, F, "bf16", seed=T + h + F + t, std=STD)
+    out, _ = run_gpu(inp, t)
+    ref = oracle.forward_backward(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], inp["dZ"], t)
+    compare_full(out, ref, TOL_BF16)
+
+
+@pytest.mark.parametrize("env", [{"TPMLP_CTA_PAIR": "0"}, {"TPMLP_MN4": "0"}, {"TPMLP_RASTER": "n:3"},
+                                 {"TPMLP_RASTER": "m:1", "TPMLP_CTA_PAIR": "0"}])
+@pytest.mark.parametrize("T,h,F,t", [(300, 384, 1280, 2), (257, 512, 1024, 4)])
+def test_tuning_knobs_keep_parity(T, h, F, t, env, monkeypatch):
+    """The library's tuning knobs (single-CTA 128 x 256 tiles, per-block maps
+    for MN-major operands, forced tile orders) change the schedule, not the
+    result."""
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    inp = inputs.make(T, h, F, "bf16", seed=T + h + len(env), std=STD)
     out, _ = run_gpu(inp, t)
     ref = oracle.forward_backward(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], inp["dZ"], t)
     compare_full(out, ref, TOL_BF16)
