@@ -139,7 +139,8 @@ const char *tpmlp_last_error(void);
 size_t tpmlp_saved_bytes(const tpmlp_shape *shape);
 
 /* Bytes of device workspace forward and backward need: the status word, the
- * column-sum partials and the dY intermediate.  A 256-byte aligned buffer of at
+ * column-sum partials, the dY intermediate (plus Y or dXn under the flags) and an
+ * 8 KiB block the backward fills with bf16 ones.  A 256-byte aligned buffer of at
  * least this size, whose first 8 bytes are zero before first use, is required.
  * 0 when the shape is invalid. */
 size_t tpmlp_workspace_bytes(const tpmlp_shape *shape);
@@ -170,6 +171,10 @@ tpmlp_status tpmlp_forward(const tpmlp_shape *shape, const void *X, const void *
  *   dB = Y^T dZ,  dA = X^T dY,  dX = sum_{i=1..t} dY_i A_i^T  (fixed-order sum).
  * dZ[T,h] and the saved activations are inputs; dX[T,h], dA[h,F], da[F],
  * dB[F,h], db[h] are outputs.  dY is left in the workspace (TPMLP_WS_DY).
+ * On the tensor-core path da comes from the dY GEMM's epilogue (fixed-order
+ * per-32-row block sums) and db from the dB GEMM itself: one extra M-tile whose
+ * A operand is a block of ones yields 1^T dZ in fp32 (bf16 at the end).  The
+ * FFMA path computes both as two-pass column sums.
  * With T = 0 the weight and bias gradients are set to zero.
  * Errors: as tpmlp_forward; saved->H, saved->Y, X, A, B must all be set. */
 tpmlp_status tpmlp_backward(const tpmlp_shape *shape, const void *dZ, const tpmlp_saved *saved,
@@ -249,9 +254,10 @@ typedef struct {
 
 /* Bytes of QKV + P + O; 0 for an invalid shape. */
 size_t tpmlp_attn_saved_bytes(const tpmlp_attn_shape *shape);
-/* Bytes of device workspace for forward and backward (status word, column-sum
- * partials, per-head Q, K, V, O, dO, dQ, dK, dV blocks, the fp32 scores, dS and
- * the row terms); 256-byte aligned, first 8 bytes zero before first use. */
+/* Bytes of device workspace for forward and backward (status word, the row terms,
+ * per-head Q, K, V, O, dO, dQ, dK, dV blocks, token-major dO and dQKV, the fp32
+ * scores reused for dS, and an 8 KiB block of ones); 256-byte aligned, first 8
+ * bytes zero before first use. */
 size_t tpmlp_attn_workspace_bytes(const tpmlp_attn_shape *shape);
 
 /* Forward: QKV = X Wqkv + bqkv (one column-parallel GEMM for all shards), per
@@ -267,7 +273,8 @@ tpmlp_status tpmlp_attn_forward(const tpmlp_attn_shape *shape, const void *X, co
 /* Backward for L = sum(dZ * Z): dbo = 1^T dZ, dO = dZ Wo^T, dWo = O^T dZ; per head
  * dV = P^T dO, dS = P * (dO V^T - rowsum(dO * O)) / sqrt(d), dQ = dS K, dK = dS^T Q;
  * dbqkv = 1^T dQKV, dWqkv = X^T dQKV, dX = fixed-order sum over shards of
- * dQKV_i Wqkv_i^T (the backward all-reduce).  Errors as the forward. */
+ * dQKV_i Wqkv_i^T (the backward all-reduce).  dbo and dbqkv come from extra
+ * ones tiles of the dWo and dWqkv GEMMs.  Errors as the forward. */
 tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *shape, const void *dZ, const tpmlp_attn_saved *saved,
                                  void *dX, void *dWqkv, void *dbqkv, void *dWo, void *dbo, void *workspace,
                                  void *stream);

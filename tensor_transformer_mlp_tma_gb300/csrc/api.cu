@@ -165,6 +165,11 @@ size_t dxn_bytes(const tpmlp_shape *s) {
                         : 0;
 }
 
+// 64 x 64 bf16 ones: the A operand of the bias-gradient tile of dB = Y^T dZ.
+constexpr size_t ONES_BYTES = 64 * 64 * 2;
+
+size_t ones_offset(const tpmlp_shape *s) { return dxn_offset(s) + dxn_bytes(s); }
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned_elt(const void *p, size_t e) { return (reinterpret_cast<uintptr_t>(p) % e) == 0; }
 
@@ -300,7 +305,7 @@ size_t tpmlp_saved_bytes(const tpmlp_shape *s) {
 
 size_t tpmlp_workspace_bytes(const tpmlp_shape *s) {
     if (!shape_valid(s)) return 0;
-    return dxn_offset(s) + dxn_bytes(s);
+    return ones_offset(s) + ONES_BYTES;
 }
 
 size_t tpmlp_workspace_offset(const tpmlp_shape *s, int region) {
@@ -416,8 +421,17 @@ tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_sa
     // Under recomputation the GeLU' epilogue rebuilds Y = GeLU(H) into the workspace.
     void *Y = rec ? static_cast<void *>(ws + y_offset(s)) : saved->Y;
 
-    // db = column sums of dZ
-    cudaError_t e = colsum(s, "colsum_db", dZ, T, h, partials, db, st);
+    // db = column sums of dZ: on tensor cores from the dB GEMM's ones tile (below),
+    // on the FFMA path a two-pass column sum.
+    void *ones = ws + ones_offset(s);
+    cudaError_t e = cudaSuccess;
+    if (use_tc(s)) {
+        Timed timed("fill_ones", st);
+        e = tpmlp::launch_fill_ones_bf16(ones, 64 * 64, st);
+        if (e == cudaSuccess) g_launches.fetch_add(1);
+    } else {
+        e = colsum(s, "colsum_db", dZ, T, h, partials, db, st);
+    }
     if (e != cudaSuccess) return from_cuda(e);
 
     // dY = (dZ B^T) * GeLU'(H)
@@ -450,6 +464,7 @@ tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_sa
     g4.b = dZ, g4.b_mn = true;        // dZ[T,h] as [K=T, N=h]: MN-major
     g4.M = F, g4.N = h, g4.K = T, g4.kshard = T;
     g4.out0 = dB;
+    if (use_tc(s)) g4.ones = ones, g4.bias_grad = db;  // db = 1^T dZ from an extra ones tile
     pick_raster(g4);
     e = gemm(s, "bwd_dB", tpmlp::EPI_STORE, g4, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
@@ -667,11 +682,11 @@ bool attn_shape_valid(const tpmlp_attn_shape *s) {
 }
 
 // Device workspace of the attention block, 1 KB-aligned regions:
-//   status | column-sum partials | D [batch*heads*seq] fp32 | Qh Kh Vh Oh dOh dQh dKh dVh
-//   [batch*heads][seq][d] bf16 | dO [T,h] bf16 | dQKV [T,3h] bf16 | scores [batch*heads][seq][seq]
-//   fp32 (the backward reuses it for dS in bf16).
+//   status | D [batch*heads*seq] fp32 | Qh Kh Vh Oh dOh dQh dKh dVh [batch*heads][seq][d] bf16 |
+//   dO [T,h] bf16 | dQKV [T,3h] bf16 | scores [batch*heads][seq][seq] fp32 (the backward reuses
+//   it for dS in bf16) | a 64 x 64 bf16 block of ones (bias-gradient tiles).
 struct AttnLayout {
-    size_t partials, D, head[8], dO, dQKV, scores, total;
+    size_t D, head[8], dO, dQKV, scores, ones, total;
 };
 enum { QH = 0, KH, VH, OH, DOH, DQH, DKH, DVH };
 
@@ -679,11 +694,6 @@ AttnLayout attn_layout(const tpmlp_attn_shape *s) {
     const int64_t T = s->batch * s->seq, h = s->hidden;
     AttnLayout L;
     size_t off = STATUS_BYTES;
-    L.partials = off;
-    int64_t np = tpmlp::colsum_chunks(T, h) * h;
-    const int64_t np3 = tpmlp::colsum_chunks(T, 3 * h) * 3 * h;
-    np = np > np3 ? np : np3;
-    off += align_up(static_cast<size_t>(np) * 4, 1024);
     L.D = off;
     off += align_up(static_cast<size_t>(T) * s->heads * 4, 1024);
     const size_t th = align_up(static_cast<size_t>(T) * h * 2, 1024);
@@ -697,6 +707,8 @@ AttnLayout attn_layout(const tpmlp_attn_shape *s) {
     off += 3 * th;
     L.scores = off;
     off += align_up(static_cast<size_t>(s->batch) * s->heads * s->seq * s->seq * 4, 1024);
+    L.ones = off;
+    off += ONES_BYTES;
     L.total = off;
     return L;
 }
@@ -903,7 +915,6 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
     const AttnLayout L = attn_layout(s);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     uint32_t *status = reinterpret_cast<uint32_t *>(ws);
-    float *partials = reinterpret_cast<float *>(ws + L.partials);
     float *D = reinterpret_cast<float *>(ws + L.D);
     void *Qh = ws + L.head[QH], *Kh = ws + L.head[KH], *Vh = ws + L.head[VH];
     void *dOh = ws + L.head[DOH], *dQh = ws + L.head[DQH], *dKh = ws + L.head[DKH], *dVh = ws + L.head[DVH];
@@ -911,9 +922,16 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
     void *dS = ws + L.scores;  // bf16 [nz][S][S] over the dead fp32 scores
     const float scale = 1.0f / std::sqrt(static_cast<float>(d));
 
-    // dbo = column sums of dZ
-    cudaError_t e = colsum(&ms, "attn_colsum_dbo", dZ, T, h, partials, dbo, st);
-    if (e != cudaSuccess) return from_cuda(e);
+    // dbo = 1^T dZ and dbqkv = 1^T dQKV come from the ones tiles of the dWo and
+    // dWqkv GEMMs.
+    void *ones = ws + L.ones;
+    cudaError_t e;
+    {
+        Timed timed("attn_fill_ones", st);
+        e = tpmlp::launch_fill_ones_bf16(ones, 64 * 64, st);
+        if (e != cudaSuccess) return from_cuda(e);
+        g_launches.fetch_add(1);
+    }
 
     // dO = dZ Wo^T (every shard's columns at once; no fold needed)
     GemmArgs g1 = base_args(status);
@@ -931,6 +949,7 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
     g2.b = dZ, g2.b_mn = true;        // dZ[T,h] as [K=T, N=h]: MN-major
     g2.M = h, g2.N = h, g2.K = T, g2.kshard = T;
     g2.out0 = dWo;
+    g2.ones = ones, g2.bias_grad = dbo;
     pick_raster(g2);
     e = gemm(&ms, "attn_bwd_dWo", tpmlp::EPI_STORE, g2, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
@@ -982,16 +1001,13 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
         g_launches.fetch_add(1);
     }
 
-    // dbqkv = column sums of dQKV
-    e = colsum(&ms, "attn_colsum_dbqkv", dQKV, T, 3 * h, partials, dbqkv, st);
-    if (e != cudaSuccess) return from_cuda(e);
-
     // dWqkv = X^T dQKV
     GemmArgs g7 = base_args(status);
     g7.a = saved->X, g7.a_mn = true;  // X[T,h] as [K=T, M=h]: MN-major
     g7.b = dQKV, g7.b_mn = true;      // dQKV[T,3h] as [K=T, N=3h]: MN-major
     g7.M = h, g7.N = 3 * h, g7.K = T, g7.kshard = T;
     g7.out0 = dWqkv;
+    g7.ones = ones, g7.bias_grad = dbqkv;
     pick_raster(g7);
     e = gemm(&ms, "attn_bwd_dWqkv", tpmlp::EPI_STORE, g7, sms, st);
     if (e != cudaSuccess) return from_cuda(e);

@@ -52,7 +52,15 @@ struct GemmArgs {
     // the M-tile (P V, dS K); 2: k from the start of the M-tile on (P^T dO, dS^T Q).
     int causal_k;
     bool skip_upper;  // skip tiles wholly above the diagonal (scores, dS)
+    // EPI_STORE with an MN-major A on tensor cores: also write bias_grad[n] =
+    // sum_k B(k, n) (bf16), computed by the MMA from an extra M-tile whose A is
+    // `ones`, a 64 x 64 bf16 block of ones (8 KiB, 16-byte aligned).
+    const void *ones;
+    void *bias_grad;
 };
+
+// Fills n bf16 elements with 1.0 (n a multiple of 8, p 16-byte aligned).
+cudaError_t launch_fill_ones_bf16(void *p, int64_t n, cudaStream_t st);
 
 // Tensor-core path: bf16 operands, fp32 accumulation in TMEM (tcgen05).
 cudaError_t launch_tc_gemm(Epi epi, const GemmArgs &g, int num_sms, cudaStream_t st);

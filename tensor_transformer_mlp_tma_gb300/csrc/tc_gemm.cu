@@ -91,6 +91,11 @@ struct Params {
     int causal_k;    // K range of an M-tile: 0 all; 1 k < end of the tile's rows; 2 k >= start of its rows
     int skip_upper;  // tiles wholly above the diagonal (every column past every row) are not computed
     int a_mn4, b_mn4;  // MN-major operand mapped as 4-D (all of a stage's 64-wide blocks in one copy)
+    // Bias gradient from the MMA (EPI_STORE with MN-major A): one extra M-tile
+    // whose A is a 64 x 64 block of ones (map tmO2), so its first accumulator
+    // row is 1^T B, the column sums of the B operand over K; written to bias_grad.
+    int bias_tile;
+    void *bias_grad;
 };
 
 // Causal per-head products.  Square per-head problems (M = K = seq) whose A or B
@@ -306,6 +311,14 @@ __device__ __forceinline__ void aux_issue(const CUtensorMap *tm, AuxLoad &a, uin
     a.pending = true;
 }
 
+// 32 consecutive column sums (fp32) to the bf16 bias gradient, past N skipped.
+__device__ __forceinline__ void store_bias_grad(const Params &p, int col, const float (&v)[32]) {
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.bias_grad);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (col + i < p.N) out[col + i] = __float2bfloat16_rn(v[i]);
+}
+
 template <int EPI>
 __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap *tm0, const CUtensorMap *tm1,
                                              const CUtensorMap *tm2, float (&v)[32], int64_t row, int row0,
@@ -513,6 +526,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int n0 = nb * BN + C::B_ROWS * static_cast<int>(rank);
                 int kb0, kb1;
                 k_range<C::TILE_M>(p, mb, kb0, kb1);
+                if constexpr (EPI == EPI_STORE && A_MN && B_MN) {
+                    if (p.bias_tile && mb == p.m_tiles - 1) {
+                        // The ones tile (its own loop, so the main loop below is unchanged):
+                        // A's columns 0..63 are ones (rank 0, block 0), the rest read as
+                        // zero; the same 64 x 64 block serves every k-block, since rows
+                        // past K meet zero-filled B rows.
+                        for (int kb = kb0; kb < kb1 && ok; ++kb) {
+                            if (!ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_empty[stage]), phase ^ 1u,
+                                                             p.wait_ns, &abort_sh)) {
+                                ok = false;
+                                break;
+                            }
+                            const uint32_t full_local = ptx::smem_u32(&bar_full[stage]);
+                            const uint32_t full = PAIR ? ptx::mapa_shared(full_local, 0) : full_local;
+                            const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
+                            const uint32_t sb = sa + C::A_STAGE;
+                            if (leader) ptx::mbar_arrive_expect_tx(full_local, CG * C::STAGE_BYTES);
+#pragma unroll
+                            for (int j = 0; j < BM / 64; ++j) {
+                                const int x = BM * static_cast<int>(rank) + 64 * j;
+                                if constexpr (PAIR)
+                                    ptx::tma_load_3d_pair(sa + j * MN_BLOCK_BYTES, &tmO2, full, x, 0, 0);
+                                else
+                                    ptx::tma_load_3d(sa + j * MN_BLOCK_BYTES, &tmO2, full, x, 0, 0);
+                            }
+                            // B exactly as in the main loop: one 4-D copy, or one per block
+                            if (p.b_mn4) {
+                                if constexpr (PAIR)
+                                    ptx::tma_load_4d_pair(sb, &tmB, full, 0, kb * BK, n0 / 64, zb);
+                                else
+                                    ptx::tma_load_4d(sb, &tmB, full, 0, kb * BK, n0 / 64, zb);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < C::B_ROWS / 64; ++j) {
+                                    if constexpr (PAIR)
+                                        ptx::tma_load_3d_pair(sb + j * MN_BLOCK_BYTES, &tmB, full, n0 + 64 * j,
+                                                              kb * BK, zb);
+                                    else
+                                        ptx::tma_load_3d(sb + j * MN_BLOCK_BYTES, &tmB, full, n0 + 64 * j, kb * BK,
+                                                         zb);
+                                }
+                            }
+                            ++issued;
+                            if (++stage == STAGES) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                        }
+                        continue;
+                    }
+                }
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_empty[stage]), phase ^ 1u, p.wait_ns,
                                                      &abort_sh)) {
@@ -733,6 +797,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                 } else {
+                    if (EPI == EPI_STORE && A_MN && B_MN && p.bias_tile && mb == p.m_tiles - 1) {
+                        // The ones tile: its row 0 holds the column sums of B; it has no
+                        // rows of the output (all of them lie past M).
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t r[32];
+                            ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+                            ptx::tmem_ld_wait(r);
+                            if (c == 3) release(buf);
+                            if (rank == 0 && quarter == 0 && lane == 0) {
+                                float v[32];
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                                store_bias_grad(p, col0 + c * 32, v);
+                            }
+                        }
+                        continue;
+                    }
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t r[32];
@@ -919,9 +1000,16 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     const void *o2 = (EPI == EPI_DGELU && g.out1) ? g.out1 : o0;
     const bool f32out = EPI == EPI_ATTN_SCORE;
     const CUtensorMapSwizzle so = f32out ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    // The bias-gradient tile takes its A from a 64 x 64 block of ones (third map).
+    const bool bias_tile = EPI == EPI_STORE && A_MN && B_MN && g.bias_grad != nullptr;
+    if (bias_tile && (g.ones == nullptr || nb != 1 || g.nshards != 1 || g.causal_k != 0 || g.skip_upper)) {
+        set_last_error("bias-gradient tile: needs the ones block, one problem, one shard, no causal ranges");
+        return cudaErrorInvalidValue;
+    }
     if (!make_map(&mo0, o0, g.M, g.N, 32, 32, so, nb, f32out) ||
         !make_map(&mo1, o1, g.M, g.N, 32, 32, so, nb, f32out) ||
-        !make_map(&mo2, o2, g.M, g.N, 32, 32, so, nb, f32out))
+        !(bias_tile ? make_map(&mo2, g.ones, 64, 64, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B, 1)
+                    : make_map(&mo2, o2, g.M, g.N, 32, 32, so, nb, f32out)))
         return cudaErrorInvalidValue;
 
     Params p;
@@ -950,6 +1038,9 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     p.causal_k = g.causal_k;
     p.a_mn4 = a4 ? 1 : 0;
     p.b_mn4 = b4 ? 1 : 0;
+    p.bias_tile = bias_tile ? 1 : 0;
+    p.bias_grad = g.bias_grad;
+    if (bias_tile) p.m_tiles += 1;  // the ones tile, after every row of the output
     p.skip_upper = g.skip_upper ? 1 : 0;
     // The causal ranges are defined for square per-head problems in one shard.
     if ((g.causal_k != 0 || g.skip_upper) && (g.nshards != 1 || (g.causal_k != 0 && g.M != g.K))) {

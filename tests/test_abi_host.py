@@ -70,7 +70,9 @@ def test_size_queries(tp):
     # recomputation keeps H only and moves Y into the workspace
     rec = tp.make_shape(4096, 8192, 32768, 8, tp.BF16, flags=tp.FLAG_RECOMPUTE)
     assert tp.saved_bytes(rec) == 4096 * 32768 * 2
-    assert tp.workspace_offset(rec, tp.WS_Y) == tp.workspace_bytes(s)
+    # Y follows dY; the workspace grows by exactly Y (the 8 KiB block of ones for
+    # the bias-gradient tiles stays at the end)
+    assert tp.workspace_offset(rec, tp.WS_Y) == tp.workspace_offset(s, tp.WS_DY) + 4096 * 32768 * 2
     assert tp.workspace_bytes(rec) == tp.workspace_bytes(s) + 4096 * 32768 * 2
     # an empty batch is valid
     assert tp.workspace_bytes(tp.make_shape(0, 256, 1024, 2, tp.BF16)) > 0
