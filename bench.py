@@ -42,12 +42,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, with the hash of the kernel source they were taken at.  A kernel whose
 # source has changed since reports traffic null.
 NCU_TRAFFIC = {  # profiles/dram_traffic_h8192_gemms.md (h8192 workload)
-    "fc1_bias_gelu": (1.958879e9 + 0.519755e9, "56a669b34d54"),
-    "fc2_shard_fold": (2.289380e9 + 0.092381e9, "56a669b34d54"),
-    "bwd_dY_dgelu": (2.630839e9 + 0.274798e9, "56a669b34d54"),
-    "bwd_dB": (1.008790e9 + 0.516112e9, "56a669b34d54"),
-    "bwd_dA": (0.989859e9 + 0.515640e9, "56a669b34d54"),
-    "bwd_dX_shard_fold": (2.468365e9 + 0.091914e9, "56a669b34d54"),
+    "fc1_bias_gelu": (1.931609e9 + 0.518971e9, "b88b8bf97986"),
+    "fc2_shard_fold": (2.399264e9 + 0.101729e9, "b88b8bf97986"),
+    "bwd_dY_dgelu": (2.796134e9 + 0.274888e9, "b88b8bf97986"),
+    "bwd_dB": (1.086311e9 + 0.518991e9, "b88b8bf97986"),
+    "bwd_dA": (1.045509e9 + 0.517855e9, "b88b8bf97986"),
+    "bwd_dX_shard_fold": (2.866486e9 + 0.099965e9, "b88b8bf97986"),
 }
 
 
