@@ -205,6 +205,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until this thread's committed bulk stores have finished reading shared memory.
+// Programmatic dependent launch: let the next kernel in the stream be scheduled
+// (its CTAs take SMs as this grid's CTAs exit), and wait for the previous
+// kernel's grid to complete with its memory visible.  Both are no-ops when the
+// launch did not opt in.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void bulk_wait_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }

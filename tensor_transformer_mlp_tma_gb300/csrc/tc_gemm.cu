@@ -508,6 +508,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = tmem_base_sh;
+    // Programmatic dependent launch: the set-up above touched only on-chip state
+    // and may overlap the previous kernel's tail; global memory is used only
+    // after that kernel's grid has completed.
+    ptx::griddep_wait();
 
     const int num_tiles = p.m_tiles * p.n_tiles * p.batch;
 
@@ -755,6 +759,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         };
         for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
+            // On starting this CTA's last tile, allow the next kernel in the stream
+            // to be scheduled: its CTAs take the SMs of CTAs that have finished.
+            // Only CTAs already running get here, so the next kernel can never
+            // hold SMs that a CTA of this grid still waits for.
+            if (tile + num_units >= num_tiles) ptx::griddep_launch_dependents();
             int mb, nb, zb;
             tile_coords(tile, p, mb, nb, zb);
             if (!tile_active<C::TILE_M>(p, mb, nb)) continue;
@@ -935,11 +944,16 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    cudaLaunchAttribute attr[1];
+    // attr[0]: the CTA-pair cluster; attr[1]: programmatic dependent launch (the
+    // kernel's set-up overlaps the previous kernel's tail; TPMLP_PDL=0 turns it
+    // off, a tuning knob read per call).
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CG;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_DYN;
@@ -1057,6 +1071,16 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
                      EPI, CG, static_cast<long long>(g.M), static_cast<long long>(g.N), static_cast<long long>(g.K),
                      tiles, max_clusters[dev], units * CG, p.group, p.raster_n ? 'n' : 'm');
     cfg.gridDim = dim3(static_cast<unsigned>(units * CG), 1, 1);
+    const char *pdl_env = std::getenv("TPMLP_PDL");
+    if (!(pdl_env && pdl_env[0] == '0')) {
+        if (CG > 1) {
+            cfg.attrs = attr;
+            cfg.numAttrs = 2;
+        } else {
+            cfg.attrs = attr + 1;
+            cfg.numAttrs = 1;
+        }
+    }
     e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo0, mo1, mo2, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
