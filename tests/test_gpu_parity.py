@@ -40,12 +40,12 @@ def test_tensor_core_path_matches_oracle(T, h, F, t):
 
 
 @pytest.mark.parametrize("env", [{"TPMLP_CTA_PAIR": "0"}, {"TPMLP_MN4": "0"}, {"TPMLP_RASTER": "n:3"},
-                                 {"TPMLP_RASTER": "m:1", "TPMLP_CTA_PAIR": "0"}])
+                                 {"TPMLP_RASTER": "m:1", "TPMLP_CTA_PAIR": "0"}, {"TPMLP_PDL": "0"}])
 @pytest.mark.parametrize("T,h,F,t", [(300, 384, 1280, 2), (257, 512, 1024, 4)])
 def test_tuning_knobs_keep_parity(T, h, F, t, env, monkeypatch):
     """The library's tuning knobs (single-CTA 128 x 256 tiles, per-block maps
-    for MN-major operands, forced tile orders) change the schedule, not the
-    result."""
+    for MN-major operands, forced tile orders, launches without programmatic
+    dependence) change the schedule, not the result."""
     for k, v in env.items():
         monkeypatch.setenv(k, v)
     inp = inputs.make(T, h, F, "bf16", seed=T + h + len(env), std=STD)
