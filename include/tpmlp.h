@@ -255,9 +255,9 @@ typedef struct {
 /* Bytes of QKV + P + O; 0 for an invalid shape. */
 size_t tpmlp_attn_saved_bytes(const tpmlp_attn_shape *shape);
 /* Bytes of device workspace for forward and backward (status word, the row terms,
- * per-head Q, K, V, O, dO, dQ, dK, dV blocks, token-major dO and dQKV, the fp32
- * scores reused for dS, and an 8 KiB block of ones); 256-byte aligned, first 8
- * bytes zero before first use. */
+ * token-major dO and dQKV, the fp32 scores reused for dS, and an 8 KiB block of
+ * ones; the per-head GEMMs address Q, K, V, O, dO, dQ, dK, dV in place inside the
+ * token-major arrays); 256-byte aligned, first 8 bytes zero before first use. */
 size_t tpmlp_attn_workspace_bytes(const tpmlp_attn_shape *shape);
 
 /* Forward: QKV = X Wqkv + bqkv (one column-parallel GEMM for all shards), per

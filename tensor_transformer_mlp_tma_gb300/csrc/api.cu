@@ -682,13 +682,14 @@ bool attn_shape_valid(const tpmlp_attn_shape *s) {
 }
 
 // Device workspace of the attention block, 1 KB-aligned regions:
-//   status | D [batch*heads*seq] fp32 | Qh Kh Vh Oh dOh dQh dKh dVh [batch*heads][seq][d] bf16 |
-//   dO [T,h] bf16 | dQKV [T,3h] bf16 | scores [batch*heads][seq][seq] fp32 (the backward reuses
-//   it for dS in bf16) | a 64 x 64 bf16 block of ones (bias-gradient tiles).
+//   status | D [batch*heads*seq] fp32 | dO [T,h] bf16 | dQKV [T,3h] bf16 |
+//   scores [batch*heads][seq][seq] fp32 (the backward reuses it for dS in bf16) |
+//   a 64 x 64 bf16 block of ones (bias-gradient tiles).
+// The per-head GEMMs address Q, K, V, O, dO, dQ, dK, dV in place inside the
+// token-major QKV, O, dO and dQKV arrays (4-D and 5-D tensor maps).
 struct AttnLayout {
-    size_t D, head[8], dO, dQKV, scores, ones, total;
+    size_t D, dO, dQKV, scores, ones, total;
 };
-enum { QH = 0, KH, VH, OH, DOH, DQH, DKH, DVH };
 
 AttnLayout attn_layout(const tpmlp_attn_shape *s) {
     const int64_t T = s->batch * s->seq, h = s->hidden;
@@ -697,10 +698,6 @@ AttnLayout attn_layout(const tpmlp_attn_shape *s) {
     L.D = off;
     off += align_up(static_cast<size_t>(T) * s->heads * 4, 1024);
     const size_t th = align_up(static_cast<size_t>(T) * h * 2, 1024);
-    for (int i = 0; i < 8; ++i) {
-        L.head[i] = off;
-        off += th;
-    }
     L.dO = off;
     off += th;
     L.dQKV = off;
@@ -738,6 +735,40 @@ tpmlp::HeadLayout head_layout(const tpmlp_attn_shape *s, bool qkv) {
     L.qkv = qkv;
     L.nmat = qkv ? 3 : 1;
     return L;
+}
+
+// Head g's Q (which = 0), K (1) or V (2) columns inside a token-major [T, 3h]
+// array with shard-major columns (QKV, dQKV), as a rank-5 view; its base is the
+// array plus which * h/t elements.
+tpmlp::HeadView qkv_view(const tpmlp_attn_shape *s) {
+    tpmlp::HeadView v;
+    v.rank = 5;
+    v.S = s->seq;
+    v.nb = s->batch;
+    v.heads = s->heads;
+    v.hpt = s->heads / s->t;
+    v.d = s->hidden / s->heads;
+    v.ld = 3 * s->hidden;
+    v.coli = 3 * s->hidden / s->t;
+    return v;
+}
+
+// Head g's columns [g*d, (g+1)*d) of a token-major [T, h] array (O, dO), rank 4.
+tpmlp::HeadView tok_view(const tpmlp_attn_shape *s) {
+    tpmlp::HeadView v;
+    v.rank = 4;
+    v.S = s->seq;
+    v.nb = s->batch;
+    v.heads = s->heads;
+    v.hpt = s->heads / s->t;
+    v.d = s->hidden / s->heads;
+    v.ld = s->hidden;
+    v.coli = 0;
+    return v;
+}
+
+const void *qkv_part(const void *base, const tpmlp_attn_shape *s, int which) {
+    return static_cast<const uint8_t *>(base) + static_cast<size_t>(which) * (s->hidden / s->t) * 2;
 }
 
 tpmlp_status attn_check(const tpmlp_attn_shape *s, const char *who, std::initializer_list<const void *> required,
@@ -829,8 +860,9 @@ tpmlp_status tpmlp_attn_forward(const tpmlp_attn_shape *s, const void *X, const 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     uint32_t *status = reinterpret_cast<uint32_t *>(ws);
-    void *Qh = ws + L.head[QH], *Kh = ws + L.head[KH], *Vh = ws + L.head[VH], *Oh = ws + L.head[OH];
     float *scores = reinterpret_cast<float *>(ws + L.scores);
+    const tpmlp::HeadView qv = qkv_view(s), tv = tok_view(s);
+    const void *Qp = qkv_part(saved->QKV, s, 0), *Kp = qkv_part(saved->QKV, s, 1), *Vp = qkv_part(saved->QKV, s, 2);
 
     // Column-parallel projection of all shards: QKV = X Wqkv + bqkv.
     GemmArgs g1 = base_args(status);
@@ -842,15 +874,9 @@ tpmlp_status tpmlp_attn_forward(const tpmlp_attn_shape *s, const void *X, const 
     cudaError_t e = gemm(&ms, "attn_qkv_proj", tpmlp::EPI_FOLD_BIAS, g1, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
-    {
-        Timed timed("attn_to_heads", st);
-        e = tpmlp::launch_to_heads(head_layout(s, true), saved->QKV, Qh, Kh, Vh, st);
-        if (e != cudaSuccess) return from_cuda(e);
-        g_launches.fetch_add(1);
-    }
-
-    // Scores of every head: scale * Q K^T, causal.
-    GemmArgs g2 = head_gemm(status, Qh, false, Kh, false, S, S, d, nz, scores);
+    // Scores of every head: scale * Q K^T, causal; Q and K read in place in QKV.
+    GemmArgs g2 = head_gemm(status, Qp, false, Kp, false, S, S, d, nz, scores);
+    g2.heads_layout = true, g2.a_view = qv, g2.b_view = qv;
     g2.scale = 1.0f / std::sqrt(static_cast<float>(d));
     g2.causal = true;
     g2.skip_upper = true;  // never read: the softmax stops at the diagonal
@@ -864,18 +890,12 @@ tpmlp_status tpmlp_attn_forward(const tpmlp_attn_shape *s, const void *X, const 
         g_launches.fetch_add(1);
     }
 
-    // O_head = P V
-    GemmArgs g3 = head_gemm(status, saved->P, false, Vh, true, S, d, S, nz, Oh);
+    // O_head = P V, V read in place in QKV, O_head written in place in O[T,h].
+    GemmArgs g3 = head_gemm(status, saved->P, false, Vp, true, S, d, S, nz, saved->O);
     g3.causal_k = 1;  // P is zero past each row's last key
+    g3.heads_layout = true, g3.b_view = qv, g3.o_view = tv;
     e = gemm(&ms, "attn_pv", tpmlp::EPI_STORE, g3, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
-
-    {
-        Timed timed("attn_to_tokens", st);
-        e = tpmlp::launch_to_tokens(head_layout(s, false), Oh, nullptr, nullptr, saved->O, st);
-        if (e != cudaSuccess) return from_cuda(e);
-        g_launches.fetch_add(1);
-    }
 
     // Row-parallel output projection: shard partials O_i Wo_i folded in order, + bo.
     GemmArgs g4 = base_args(status);
@@ -916,9 +936,13 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     uint32_t *status = reinterpret_cast<uint32_t *>(ws);
     float *D = reinterpret_cast<float *>(ws + L.D);
-    void *Qh = ws + L.head[QH], *Kh = ws + L.head[KH], *Vh = ws + L.head[VH];
-    void *dOh = ws + L.head[DOH], *dQh = ws + L.head[DQH], *dKh = ws + L.head[DKH], *dVh = ws + L.head[DVH];
     void *dO = ws + L.dO, *dQKV = ws + L.dQKV;
+    // Per-head Q, K, V (in the saved QKV), dO (in dO[T,h]) and dQ, dK, dV (in
+    // dQKV) are addressed in place through rank-5 and rank-4 views.
+    const tpmlp::HeadView qv = qkv_view(s), tv = tok_view(s);
+    const void *Qp = qkv_part(saved->QKV, s, 0), *Kp = qkv_part(saved->QKV, s, 1), *Vp = qkv_part(saved->QKV, s, 2);
+    void *dQp = const_cast<void *>(qkv_part(dQKV, s, 0)), *dKp = const_cast<void *>(qkv_part(dQKV, s, 1)),
+         *dVp = const_cast<void *>(qkv_part(dQKV, s, 2));
     void *dS = ws + L.scores;  // bf16 [nz][S][S] over the dead fp32 scores
     const float scale = 1.0f / std::sqrt(static_cast<float>(d));
 
@@ -955,14 +979,6 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
     if (e != cudaSuccess) return from_cuda(e);
 
     {
-        Timed timed("attn_bwd_to_heads", st);
-        // Q, K, V of every head again from the saved projection, and dO per head.
-        e = tpmlp::launch_to_heads(head_layout(s, true), saved->QKV, Qh, Kh, Vh, st);
-        if (e == cudaSuccess) e = tpmlp::launch_to_heads(head_layout(s, false), dO, dOh, nullptr, nullptr, st);
-        if (e != cudaSuccess) return from_cuda(e);
-        g_launches.fetch_add(2);
-    }
-    {
         Timed timed("attn_bwd_rowdot", st);
         e = tpmlp::launch_rowdot(head_layout(s, false), dO, saved->O, D, st);
         if (e != cudaSuccess) return from_cuda(e);
@@ -970,13 +986,15 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
     }
 
     // dV_head = P^T dO_head
-    GemmArgs g3 = head_gemm(status, saved->P, true, dOh, true, S, d, S, nz, dVh);
+    GemmArgs g3 = head_gemm(status, saved->P, true, dO, true, S, d, S, nz, dVp);
     g3.causal_k = 2;  // key j only gets gradient from queries i >= j
+    g3.heads_layout = true, g3.b_view = tv, g3.o_view = qv;
     e = gemm(&ms, "attn_bwd_dV", tpmlp::EPI_STORE, g3, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
     // dS = P * (dO V^T - D) * scale
-    GemmArgs g4 = head_gemm(status, dOh, false, Vh, false, S, S, d, nz, dS);
+    GemmArgs g4 = head_gemm(status, dO, false, Vp, false, S, S, d, nz, dS);
+    g4.heads_layout = true, g4.a_view = tv, g4.b_view = qv;
     g4.aux = saved->P;
     g4.rowvec = D;
     g4.scale = scale;
@@ -985,21 +1003,16 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
     if (e != cudaSuccess) return from_cuda(e);
 
     // dQ_head = dS K_head,  dK_head = dS^T Q_head
-    GemmArgs g5 = head_gemm(status, dS, false, Kh, true, S, d, S, nz, dQh);
+    GemmArgs g5 = head_gemm(status, dS, false, Kp, true, S, d, S, nz, dQp);
     g5.causal_k = 1;
+    g5.heads_layout = true, g5.b_view = qv, g5.o_view = qv;
     e = gemm(&ms, "attn_bwd_dQ", tpmlp::EPI_STORE, g5, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
-    GemmArgs g6 = head_gemm(status, dS, true, Qh, true, S, d, S, nz, dKh);
+    GemmArgs g6 = head_gemm(status, dS, true, Qp, true, S, d, S, nz, dKp);
     g6.causal_k = 2;
+    g6.heads_layout = true, g6.b_view = qv, g6.o_view = qv;
     e = gemm(&ms, "attn_bwd_dK", tpmlp::EPI_STORE, g6, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
-
-    {
-        Timed timed("attn_bwd_to_tokens", st);
-        e = tpmlp::launch_to_tokens(head_layout(s, true), dQh, dKh, dVh, dQKV, st);
-        if (e != cudaSuccess) return from_cuda(e);
-        g_launches.fetch_add(1);
-    }
 
     // dWqkv = X^T dQKV
     GemmArgs g7 = base_args(status);

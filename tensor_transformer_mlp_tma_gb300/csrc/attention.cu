@@ -1,11 +1,8 @@
 // Support kernels of the tensor-parallel self-attention block ("Megatron-LM"
 // report, section 4.1: heads divided among the t shards).  The projections and
-// the per-head products run on the tensor-core GEMMs; these memory-bound kernels
-// move data between the token-major projection layout and per-head blocks, and
-// compute the row-wise parts of the attention:
-//   - heads <-> tokens: QKV [T, 3h] with shard-major columns [Q_i | K_i | V_i]
-//     (head j of shard i at column i*3h/t + which*h/t + j*d), or O [T, h] (head g
-//     at column g*d), to / from per-head blocks [nb*heads][S][d];
+// the per-head products run on the tensor-core GEMMs, which read and write each
+// head's Q, K, V, O, dO, dQ, dK, dV in place in the token-major arrays; these
+// memory-bound kernels compute the row-wise parts of the attention:
 //   - causal softmax of fp32 scores [nb*heads*S][S] into bf16 P;
 //   - D[z, s] = sum_e dO[token, head cols] * O[token, head cols], the row term of
 //     the softmax backward.
@@ -16,53 +13,6 @@
 
 namespace tpmlp {
 namespace attn {
-
-// One block per token row r = b*S + s.  The row's nmat*h elements (QKV: its 3h
-// shard-major columns [Q_i | K_i | V_i]; O or dO: its h columns, head g at g*d)
-// move in 16-byte vectors, consecutive threads on consecutive vectors: reads of
-// the token row and writes of each head's d-wide row are both contiguous.
-// Column c of the row belongs to matrix `which`, head g = i*hpt + j, element e:
-//   QKV: i = c / (3h/t), which = (c mod 3h/t) / (h/t), j = (c mod h/t) / d;
-//   O:   g = c / d.
-// The per-head address is ((b*heads + g)*S + s)*d + e.
-__global__ void __launch_bounds__(256)
-    permute_kernel(const HeadLayout L, const __nv_bfloat16 *__restrict__ tok, __nv_bfloat16 *__restrict__ tok_out,
-                   const __nv_bfloat16 *__restrict__ h0, const __nv_bfloat16 *__restrict__ h1,
-                   const __nv_bfloat16 *__restrict__ h2, __nv_bfloat16 *__restrict__ o0,
-                   __nv_bfloat16 *__restrict__ o1, __nv_bfloat16 *__restrict__ o2, bool to_heads) {
-    const int64_t r = blockIdx.x;
-    const int64_t b = r / L.S, s = r - b * L.S;
-    const int h = static_cast<int>(L.h), d = static_cast<int>(L.d), heads = static_cast<int>(L.heads);
-    const int hs = h / L.t, hpt = heads / L.t;
-    const int ld = L.qkv ? 3 * h : h;
-    const int nvec = L.nmat * h / 8;
-    for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-        const int c = v * 8;
-        int which = 0, g, e;
-        if (L.qkv) {
-            const int i = c / (3 * hs);
-            int rem = c - i * 3 * hs;
-            which = rem / hs;
-            rem -= which * hs;
-            const int j = rem / d;
-            e = rem - j * d;
-            g = i * hpt + j;
-        } else {
-            g = c / d;
-            e = c - g * d;
-        }
-        const int64_t head_off = ((b * heads + g) * L.S + s) * d + e;
-        const int64_t tok_off = r * ld + c;
-        if (to_heads) {
-            const uint4 val = __ldg(reinterpret_cast<const uint4 *>(tok + tok_off));
-            __nv_bfloat16 *dst = which == 0 ? o0 : (which == 1 ? o1 : o2);
-            *reinterpret_cast<uint4 *>(dst + head_off) = val;
-        } else {
-            const __nv_bfloat16 *src = which == 0 ? h0 : (which == 1 ? h1 : h2);
-            *reinterpret_cast<uint4 *>(tok_out + tok_off) = __ldg(reinterpret_cast<const uint4 *>(src + head_off));
-        }
-    }
-}
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -180,26 +130,6 @@ __global__ void __launch_bounds__(256)
 }
 
 }  // namespace attn
-
-cudaError_t launch_to_heads(const HeadLayout &L, const void *tok, void *h0, void *h1, void *h2, cudaStream_t st) {
-    const int64_t rows = L.nb * L.S;
-    if (rows <= 0) return cudaSuccess;
-    attn::permute_kernel<<<static_cast<unsigned>(rows), 256, 0, st>>>(
-        L, static_cast<const __nv_bfloat16 *>(tok), nullptr, nullptr, nullptr, nullptr,
-        static_cast<__nv_bfloat16 *>(h0), static_cast<__nv_bfloat16 *>(h1), static_cast<__nv_bfloat16 *>(h2), true);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_to_tokens(const HeadLayout &L, const void *h0, const void *h1, const void *h2, void *tok,
-                             cudaStream_t st) {
-    const int64_t rows = L.nb * L.S;
-    if (rows <= 0) return cudaSuccess;
-    attn::permute_kernel<<<static_cast<unsigned>(rows), 256, 0, st>>>(
-        L, nullptr, static_cast<__nv_bfloat16 *>(tok), static_cast<const __nv_bfloat16 *>(h0),
-        static_cast<const __nv_bfloat16 *>(h1), static_cast<const __nv_bfloat16 *>(h2), nullptr, nullptr, nullptr,
-        false);
-    return cudaGetLastError();
-}
 
 cudaError_t launch_softmax(const float *S, void *P, int64_t rows, int64_t cols, bool causal, cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;

@@ -17,6 +17,17 @@ enum Epi : int {
     EPI_ATTN_DS = 6,    // dS = P * (acc - D[row]) * scale                  -- dO V^T -> dS
 };
 
+// A per-head operand or output read or written in place inside a token-major
+// array (rank 4 or 5), instead of a contiguous [batch][rows][cols] block (rank 3).
+// Element (e, s) of problem z = b * heads + g, head g = i * hpt + j:
+//   rank 4 (O, dO [T, h]):           base[(b*S + s) * ld + g * d + e]
+//   rank 5 (Q, K, V inside QKV or dQKV [T, 3h], base at the Q/K/V column offset):
+//                                     base[(b*S + s) * ld + i * coli + j * d + e]
+struct HeadView {
+    int rank;  // 3 (plain block), 4 or 5
+    int64_t S, nb, heads, hpt, d, ld, coli;
+};
+
 // One GEMM  out[M,N] = sum_k opA(m,k) opB(k,n)  over row-major operands.
 //   A operand: K-major ([M,K] row-major, a_mn = false) or MN-major ([K,M], a_mn = true)
 //   B operand: K-major ([N,K] row-major, b_mn = false) or MN-major ([K,N], b_mn = true)
@@ -57,6 +68,11 @@ struct GemmArgs {
     // `ones`, a 64 x 64 bf16 block of ones (8 KiB, 16-byte aligned).
     const void *ones;
     void *bias_grad;
+    // Per-head GEMMs addressing their operands and output in place (tensor-core
+    // path; EPI_ATTN_SCORE, EPI_ATTN_DS, EPI_STORE): a rank of 0 or 3 is the
+    // plain [batch][rows][cols] block.
+    bool heads_layout;
+    HeadView a_view, b_view, o_view;
 };
 
 // Fills n bf16 elements with 1.0 (n a multiple of 8, p 16-byte aligned).
@@ -101,18 +117,15 @@ int64_t ln_partial_floats(int64_t rows, int64_t h);
 cudaError_t launch_ln_forward(bool is_bf16, const LnArgs &a, cudaStream_t st);
 cudaError_t launch_ln_backward(bool is_bf16, const LnArgs &a, cudaStream_t st, int *launches);
 
-// Attention support.  Per-head blocks are [nb*heads][S][d] (z = b*heads + g);
-// token-major data is QKV [T, 3h] with shard-major columns (qkv = true, nmat = 3:
-// Q, K, V) or O [T, h] (qkv = false, nmat = 1).
+// Attention support.  Problem z = b*heads + g; token-major data is QKV [T, 3h]
+// with shard-major columns (qkv = true, nmat = 3: Q, K, V) or O [T, h] (qkv =
+// false, nmat = 1).
 struct HeadLayout {
     int64_t nb, S, h, heads, d;
     int t;
     bool qkv;
     int nmat;
 };
-cudaError_t launch_to_heads(const HeadLayout &L, const void *tok, void *h0, void *h1, void *h2, cudaStream_t st);
-cudaError_t launch_to_tokens(const HeadLayout &L, const void *h0, const void *h1, const void *h2, void *tok,
-                             cudaStream_t st);
 cudaError_t launch_softmax(const float *S, void *P, int64_t rows, int64_t cols, bool causal, cudaStream_t st);
 // D[z*S + s] = row dot of dO and O over head g's columns of token b*S + s (token-major inputs).
 cudaError_t launch_rowdot(const HeadLayout &L, const void *dO, const void *O, float *D, cudaStream_t st);

@@ -96,7 +96,57 @@ struct Params {
     // row is 1^T B, the column sums of the B operand over K; written to bias_grad.
     int bias_tile;
     void *bias_grad;
+    // Per-head problems read and written in place in token-major arrays (kernels
+    // instantiated with HEADS): the rank of each operand's and the output's map.
+    // Rank 3: (x, y, z); rank 4: (x, y, g, b); rank 5: (x, y, j, i, b), where
+    // problem z = b * heads + g and head g = i * hpt + j (hpt heads per shard).
+    int a_rank, b_rank, o_rank;
+    int heads, hpt;
 };
+
+// Coordinates after (x, y) of problem z in a map of the given rank.
+__device__ __forceinline__ void head_coords(int rank, int z, int heads, int hpt, int &c2, int &c3, int &c4) {
+    if (rank <= 3) {
+        c2 = z, c3 = 0, c4 = 0;
+        return;
+    }
+    const int g = z % heads, b = z / heads;
+    if (rank == 4)
+        c2 = g, c3 = b, c4 = 0;
+    else
+        c2 = g % hpt, c3 = g / hpt, c4 = b;
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void tma_load_rank(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y,
+                                              int rank, int c2, int c3, int c4) {
+    if (rank <= 3) {
+        if constexpr (PAIR)
+            ptx::tma_load_3d_pair(dst, map, bar, x, y, c2);
+        else
+            ptx::tma_load_3d(dst, map, bar, x, y, c2);
+    } else if (rank == 4) {
+        if constexpr (PAIR)
+            ptx::tma_load_4d_pair(dst, map, bar, x, y, c2, c3);
+        else
+            ptx::tma_load_4d(dst, map, bar, x, y, c2, c3);
+    } else {
+        if constexpr (PAIR)
+            ptx::tma_load_5d_pair(dst, map, bar, x, y, c2, c3, c4);
+        else
+            ptx::tma_load_5d(dst, map, bar, x, y, c2, c3, c4);
+    }
+}
+
+__device__ __forceinline__ void tma_store_rank(const CUtensorMap *map, uint32_t src, int x, int y, int rank, int c2,
+                                               int c3, int c4) {
+    if (rank <= 3)
+        ptx::tma_store_3d(map, src, x, y, c2);
+    else if (rank == 4)
+        ptx::tma_store_4d(map, src, x, y, c2, c3);
+    else
+        ptx::tma_store_5d(map, src, x, y, c2, c3, c4);
+}
 
 // Causal per-head products.  Square per-head problems (M = K = seq) whose A or B
 // operand is zero above the diagonal need only part of K: P V and dS K only keys
@@ -319,7 +369,7 @@ __device__ __forceinline__ void store_bias_grad(const Params &p, int col, const 
         if (col + i < p.N) out[col + i] = __float2bfloat16_rn(v[i]);
 }
 
-template <int EPI>
+template <int EPI, bool HEADS = false>
 __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap *tm0, const CUtensorMap *tm1,
                                              const CUtensorMap *tm2, float (&v)[32], int64_t row, int row0,
                                              int col, int z, int lane, uint32_t stg, AuxLoad *aux = nullptr,
@@ -427,7 +477,15 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
     __syncwarp();
     // A box that lies wholly outside the output (ragged last tile) is not stored.
     if (lane == 0 && row0 < p.M && col < p.N) {
-        if (store0) ptx::tma_store_3d(tm0, stg, col, row0, z);
+        if (store0) {
+            if constexpr (HEADS) {
+                int c2, c3, c4;
+                head_coords(p.o_rank, z, p.heads, p.hpt, c2, c3, c4);
+                tma_store_rank(tm0, stg, col, row0, p.o_rank, c2, c3, c4);
+            } else {
+                ptx::tma_store_3d(tm0, stg, col, row0, z);
+            }
+        }
         if (two) ptx::tma_store_3d(tm_second, stg + STG_BOX, col, row0, z);
         ptx::bulk_commit();
     }
@@ -436,7 +494,7 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
     }
 }
 
-template <int EPI, bool A_MN, bool B_MN, int CG>
+template <int EPI, bool A_MN, bool B_MN, int CG, bool HEADS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
@@ -530,7 +588,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int n0 = nb * BN + C::B_ROWS * static_cast<int>(rank);
                 int kb0, kb1;
                 k_range<C::TILE_M>(p, mb, kb0, kb1);
-                if constexpr (EPI == EPI_STORE && A_MN && B_MN) {
+                if constexpr (EPI == EPI_STORE && A_MN && B_MN && !HEADS) {
                     if (p.bias_tile && mb == p.m_tiles - 1) {
                         // The ones tile (its own loop, so the main loop below is unchanged):
                         // A's columns 0..63 are ones (rank 0, block 0), the rest read as
@@ -609,6 +667,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // copies only complete bytes on the leader's barrier (they can land
                     // before the announcement: the phase still needs the arrival).
                     if (leader) ptx::mbar_arrive_expect_tx(full_local, CG * C::STAGE_BYTES);
+                    if constexpr (HEADS) {
+                        // per-head operands addressed in place (rank-3/4/5 maps)
+                        int a2, a3, a4, b2, b3, b4;
+                        head_coords(p.a_rank, zb, p.heads, p.hpt, a2, a3, a4);
+                        head_coords(p.b_rank, zb, p.heads, p.hpt, b2, b3, b4);
+                        if constexpr (!A_MN) {
+                            tma_load_rank<PAIR>(sa, &tmA, full, k0, m0, p.a_rank, a2, a3, a4);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < BM / 64; ++j)
+                                tma_load_rank<PAIR>(sa + j * MN_BLOCK_BYTES, &tmA, full, m0 + 64 * j, k0, p.a_rank, a2,
+                                                    a3, a4);
+                        }
+                        if constexpr (!B_MN) {
+                            tma_load_rank<PAIR>(sb, &tmB, full, k0, n0, p.b_rank, b2, b3, b4);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < C::B_ROWS / 64; ++j)
+                                tma_load_rank<PAIR>(sb + j * MN_BLOCK_BYTES, &tmB, full, n0 + 64 * j, k0, p.b_rank,
+                                                    b2, b3, b4);
+                        }
+                    } else {
                     if constexpr (!A_MN) {
                         load(sa, &tmA, k0, m0);
                     } else if (p.a_mn4) {
@@ -625,6 +705,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < C::B_ROWS / 64; ++j)
                             load(sb + j * MN_BLOCK_BYTES, &tmB, n0 + 64 * j, k0);
+                    }
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -802,7 +883,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             float v[32];
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i];
-                            finish_chunk<EPI>(p, &tmO0, &tmO1, &tmO2, v, row, row0, col0 + c * 32, zb, lane, stg);
+                            finish_chunk<EPI, HEADS>(p, &tmO0, &tmO1, &tmO2, v, row, row0, col0 + c * 32, zb, lane, stg);
                         }
                     }
                 } else {
@@ -833,7 +914,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         float v[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                        finish_chunk<EPI>(p, &tmO0, &tmO1, &tmO2, v, row, row0, col0 + c * 32, zb, lane, stg, &aux,
+                        finish_chunk<EPI, HEADS>(p, &tmO0, &tmO1, &tmO2, v, row, row0, col0 + c * 32, zb, lane, stg, &aux,
                                           c < 3 ? col0 + (c + 1) * 32 : -1, row0, &abort_sh);
                     }
                 }
@@ -931,10 +1012,50 @@ static bool make_map_mn4(CUtensorMap *m, const void *ptr, int64_t rows, int64_t 
     return r == CUDA_SUCCESS;
 }
 
-template <int EPI, bool A_MN, bool B_MN, int CG>
+// A rank-4 or rank-5 view (see HeadView) with a box of box0 elements along d and
+// box1 along S (1 in the head and batch dimensions).
+static bool make_map_view(CUtensorMap *m, const void *ptr, const HeadView &v, uint32_t box0, uint32_t box1,
+                          CUtensorMapSwizzle swz) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t e = 2;
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5] = {box0, box1, 1, 1, 1}, estr[5] = {1, 1, 1, 1, 1};
+    int rank = 0;
+    if (v.rank == 4) {
+        rank = 4;
+        const cuuint64_t d4[4] = {static_cast<cuuint64_t>(v.d), static_cast<cuuint64_t>(v.S),
+                                  static_cast<cuuint64_t>(v.heads), static_cast<cuuint64_t>(v.nb)};
+        const cuuint64_t s4[3] = {static_cast<cuuint64_t>(v.ld) * e, static_cast<cuuint64_t>(v.d) * e,
+                                  static_cast<cuuint64_t>(v.S) * static_cast<cuuint64_t>(v.ld) * e};
+        for (int i = 0; i < 4; ++i) dims[i] = d4[i];
+        for (int i = 0; i < 3; ++i) strides[i] = s4[i];
+    } else if (v.rank == 5) {
+        rank = 5;
+        const cuuint64_t d5[5] = {static_cast<cuuint64_t>(v.d), static_cast<cuuint64_t>(v.S),
+                                  static_cast<cuuint64_t>(v.hpt), static_cast<cuuint64_t>(v.heads / v.hpt),
+                                  static_cast<cuuint64_t>(v.nb)};
+        const cuuint64_t s5[4] = {static_cast<cuuint64_t>(v.ld) * e, static_cast<cuuint64_t>(v.d) * e,
+                                  static_cast<cuuint64_t>(v.coli) * e,
+                                  static_cast<cuuint64_t>(v.S) * static_cast<cuuint64_t>(v.ld) * e};
+        for (int i = 0; i < 5; ++i) dims[i] = d5[i];
+        for (int i = 0; i < 4; ++i) strides[i] = s5[i];
+    } else {
+        return false;
+    }
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        set_last_error("cuTensorMapEncodeTiled failed (CUresult %d) for a rank-%d head view", static_cast<int>(r),
+                       rank);
+    return r == CUDA_SUCCESS;
+}
+
+template <int EPI, bool A_MN, bool B_MN, int CG, bool HEADS = false>
 static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     using C = Cfg<CG>;
-    auto kern = gemm_kernel<EPI, A_MN, B_MN, CG>;
+    auto kern = gemm_kernel<EPI, A_MN, B_MN, CG, HEADS>;
     // Per-device, once: the shared-memory opt-in, and for CTA pairs the number of
     // 2-CTA clusters that can be resident at once (the persistent grid size).
     static std::mutex mu;
@@ -995,12 +1116,25 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     // the per-block maps (a tuning knob, read per call).
     const char *mn4_env = std::getenv("TPMLP_MN4");
     const bool mn4 = !(mn4_env && mn4_env[0] == '0');
-    const bool a4 = A_MN && mn4 && g.M % 64 == 0 && make_map_mn4(&ma, g.a, g.K, g.M, BK, BM / 64, nb);
-    const bool b4 = B_MN && mn4 && g.N % 64 == 0 && make_map_mn4(&mb, g.b, g.K, g.N, BK, C::B_ROWS / 64, nb);
-    const bool oka = a4 || (A_MN ? make_map(&ma, g.a, g.K, g.M, 64, BK, sw, nb)
-                                 : make_map(&ma, g.a, g.M, g.K, BK, BM, sw, nb));
-    const bool okb = b4 || (B_MN ? make_map(&mb, g.b, g.K, g.N, 64, BK, sw, nb)
-                                 : make_map(&mb, g.b, g.N, g.K, BK, C::B_ROWS, sw, nb));
+    // Per-head views (HEADS): K-major boxes of 64 (d) x rows, MN-major boxes of
+    // 64 (d) x BK; the 4-D per-stage copy is not used for them.
+    const int a_rank = HEADS && g.a_view.rank > 3 ? g.a_view.rank : 3;
+    const int b_rank = HEADS && g.b_view.rank > 3 ? g.b_view.rank : 3;
+    const int o_rank = HEADS && g.o_view.rank > 3 ? g.o_view.rank : 3;
+    // (HEADS kernels always copy MN-major operands block by block.)
+    const bool a4 = !HEADS && A_MN && mn4 && g.M % 64 == 0 && make_map_mn4(&ma, g.a, g.K, g.M, BK, BM / 64, nb);
+    const bool b4 = !HEADS && B_MN && mn4 && g.N % 64 == 0 &&
+                    make_map_mn4(&mb, g.b, g.K, g.N, BK, C::B_ROWS / 64, nb);
+    bool oka, okb;
+    if (a_rank > 3)
+        oka = make_map_view(&ma, g.a, g.a_view, 64, A_MN ? BK : BM, sw);
+    else
+        oka = a4 || (A_MN ? make_map(&ma, g.a, g.K, g.M, 64, BK, sw, nb) : make_map(&ma, g.a, g.M, g.K, BK, BM, sw, nb));
+    if (b_rank > 3)
+        okb = make_map_view(&mb, g.b, g.b_view, 64, B_MN ? BK : C::B_ROWS, sw);
+    else
+        okb = b4 || (B_MN ? make_map(&mb, g.b, g.K, g.N, 64, BK, sw, nb)
+                          : make_map(&mb, g.b, g.N, g.K, BK, C::B_ROWS, sw, nb));
     if (!oka || !okb) return cudaErrorInvalidValue;
     // Output maps: [M, N] row-major, 32 x 32 boxes, 64-byte swizzle (matches stage_row).
     // Bias + GeLU writes H (optional) and Y; GeLU' reads H through the second map;
@@ -1020,7 +1154,7 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
         set_last_error("bias-gradient tile: needs the ones block, one problem, one shard, no causal ranges");
         return cudaErrorInvalidValue;
     }
-    if (!make_map(&mo0, o0, g.M, g.N, 32, 32, so, nb, f32out) ||
+    if (!(o_rank > 3 ? make_map_view(&mo0, o0, g.o_view, 32, 32, so) : make_map(&mo0, o0, g.M, g.N, 32, 32, so, nb, f32out)) ||
         !make_map(&mo1, o1, g.M, g.N, 32, 32, so, nb, f32out) ||
         !(bias_tile ? make_map(&mo2, g.ones, 64, 64, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B, 1)
                     : make_map(&mo2, o2, g.M, g.N, 32, 32, so, nb, f32out)))
@@ -1052,6 +1186,14 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     p.causal_k = g.causal_k;
     p.a_mn4 = a4 ? 1 : 0;
     p.b_mn4 = b4 ? 1 : 0;
+    p.a_rank = a_rank;
+    p.b_rank = b_rank;
+    p.o_rank = o_rank;
+    {
+        const HeadView &hv = g.a_view.rank > 3 ? g.a_view : (g.b_view.rank > 3 ? g.b_view : g.o_view);
+        p.heads = hv.heads > 0 ? static_cast<int>(hv.heads) : 1;
+        p.hpt = hv.hpt > 0 ? static_cast<int>(hv.hpt) : 1;
+    }
     p.bias_tile = bias_tile ? 1 : 0;
     p.bias_grad = g.bias_grad;
     if (bias_tile) p.m_tiles += 1;  // the ones tile, after every row of the output
@@ -1097,6 +1239,11 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
 
 template <int EPI, bool A_MN, bool B_MN>
 static cudaError_t launch_cg(const GemmArgs &g, int num_sms, cudaStream_t st) {
+    if constexpr (EPI == EPI_ATTN_SCORE || EPI == EPI_ATTN_DS || EPI == EPI_STORE) {
+        if (g.heads_layout)
+            return g.cta_pair ? launch_t<EPI, A_MN, B_MN, 2, true>(g, num_sms, st)
+                              : launch_t<EPI, A_MN, B_MN, 1, true>(g, num_sms, st);
+    }
     return g.cta_pair ? launch_t<EPI, A_MN, B_MN, 2>(g, num_sms, st) : launch_t<EPI, A_MN, B_MN, 1>(g, num_sms, st);
 }
 
