@@ -109,6 +109,13 @@ int num_sms_current() {
 }
 
 // ---- shapes and workspace --------------------------------------------------------------
+// The GEMM kernels count output tiles (128 x 256 at the smallest, times the
+// problem count) in 32-bit integers.
+bool tiles_fit(int64_t M, int64_t N, int64_t batch = 1) {
+    const int64_t t = ((M + 127) / 128) * ((N + 255) / 256);
+    return t <= (int64_t{1} << 31) / 2 && batch <= (int64_t{1} << 31) / 2 / (t > 0 ? t : 1);
+}
+
 bool shape_valid(const tpmlp_shape *s) {
     if (!s) return false;
     if (s->tokens < 0 || s->hidden <= 0 || s->ffn <= 0) return false;
@@ -118,6 +125,9 @@ bool shape_valid(const tpmlp_shape *s) {
     if ((s->flags & ~(TPMLP_FLAG_RECOMPUTE | TPMLP_FLAG_LAYERNORM)) != 0) return false;
     // int32 tile and grid arithmetic inside the kernels
     if (s->tokens > (1LL << 30) || s->hidden > (1LL << 30) || s->ffn > (1LL << 30)) return false;
+    const int64_t T = s->tokens, h = s->hidden, F = s->ffn;
+    // the six GEMMs: T x F (fc1, dY), T x h (fc2, dX), F x h (dB), h x F (dA)
+    if (!tiles_fit(T, F) || !tiles_fit(T, h) || !tiles_fit(F + 256, h) || !tiles_fit(h, F)) return false;
     return true;
 }
 
@@ -678,6 +688,11 @@ bool attn_shape_valid(const tpmlp_attn_shape *s) {
     // int32 tile and grid arithmetic inside the kernels
     if (s->hidden > (1LL << 28) || s->seq > (1LL << 20) || s->batch * s->seq > (1LL << 30)) return false;
     if (static_cast<int64_t>(s->batch) * s->heads > (1LL << 24)) return false;
+    // tile counts of the projections and the per-head products; the fp32 scores
+    // ([batch*heads][seq][seq]) must be addressable
+    const int64_t T = s->batch * s->seq, h = s->hidden, nz = s->batch * s->heads;
+    if (!tiles_fit(T, 3 * h) || !tiles_fit(h + 256, 3 * h) || !tiles_fit(s->seq, s->seq, nz)) return false;
+    if (static_cast<double>(nz) * s->seq * s->seq > static_cast<double>(1LL << 48)) return false;
     return true;
 }
 

@@ -67,6 +67,10 @@ def test_size_queries(tp):
                 tp.Shape(128, 256, 1024, 2, 1, 0, 4)):       # unknown flag
         assert tp.saved_bytes(bad) == 0
         assert tp.workspace_bytes(bad) == 0
+    # every dimension within its limit, but more output tiles than the kernels'
+    # 32-bit tile counter holds
+    huge = tp.make_shape(1 << 30, 256, 1 << 30, 1, tp.BF16)
+    assert tp.saved_bytes(huge) == 0 and tp.workspace_bytes(huge) == 0
     # recomputation keeps H only and moves Y into the workspace
     rec = tp.make_shape(4096, 8192, 32768, 8, tp.BF16, flags=tp.FLAG_RECOMPUTE)
     assert tp.saved_bytes(rec) == 4096 * 32768 * 2
@@ -179,7 +183,8 @@ def test_attention_size_queries(tp):
                 tp.AttnShape(1, 64, 256, 2, 0, tp.BF16, 0),    # t < 1
                 tp.AttnShape(1, 0, 256, 2, 1, tp.BF16, 0),     # seq = 0
                 tp.AttnShape(-1, 64, 256, 2, 1, tp.BF16, 0),   # batch < 0
-                tp.AttnShape(1, 64, 256, 2, 1, tp.BF16, 1)):   # flags
+                tp.AttnShape(1, 64, 256, 2, 1, tp.BF16, 1),    # flags
+                tp.AttnShape(1 << 10, 1 << 20, 1024, 8, 1, tp.BF16, 0)):  # scores past 2^48 elements
         assert tp.lib.tpmlp_attn_saved_bytes(ctypes.byref(bad)) == 0
         assert tp.lib.tpmlp_attn_workspace_bytes(ctypes.byref(bad)) == 0
     assert tp.lib.tpmlp_attn_workspace_bytes(ctypes.byref(tp.AttnShape(0, 64, 256, 2, 2, tp.BF16, 0))) > 0
