@@ -87,6 +87,7 @@ CASES = [
     (1, 520, 512, 8, 4),     # d = 64, three score tiles with a ragged tail of 8
     (3, 136, 384, 3, 3),     # ragged single tile, t = 3
     (2, 384, 256, 2, 1),     # t = 1
+    (2, 256, 1024, 16, 8),   # t = 8 shards of two heads (d = 64), as in the bench's shard count
     (1, 2056, 256, 2, 2),    # rows past 2048 columns (widest register softmax)
     (1, 4104, 128, 1, 1),    # rows past 4096 columns (multi-pass softmax)
 ]
