@@ -155,9 +155,11 @@ size_t tpmlp_workspace_offset(const tpmlp_shape *shape, int region);
  *   Z = b + sum_{i=1..t} Y_i B_i -- the row-parallel GEMM; the t shard partials
  *                                  are summed in order on chip, then b is added.
  * X[T,h], A[h,F], a[F], B[F,h], b[h] are inputs; Z[T,h] is the output; saved->Y
- * (and saved->H unless NULL) receive the activations.  GeLU is the tanh form
+ * (and saved->H unless NULL) receive the activations.  saved == NULL is
+ * inference: H is not stored and Y goes to the workspace's dY region (which
+ * only the backward pass uses), so nothing is kept for a backward pass.  GeLU is the tanh form
  * 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
- * Errors: INVALID_ARG for NULL shape/pointers (saved->H excepted), bad sizes;
+ * Errors: INVALID_ARG for NULL shape/pointers (saved and saved->H excepted), bad sizes;
  * UNSUPPORTED on the tensor-core path when a pointer is not 16-byte aligned,
  * h or F is not a multiple of 8, or t > 1 and F/t is not a multiple of 64;
  * CUDA when a launch fails.  Nothing is launched when an error is returned. */

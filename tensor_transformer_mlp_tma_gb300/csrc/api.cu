@@ -337,8 +337,11 @@ namespace {
 tpmlp_status validate_forward(const tpmlp_shape *s, const void *X, const void *A, const void *a, const void *B,
                               const void *b, const void *Z, const tpmlp_saved *saved, const void *workspace) {
     if (!shape_valid(s)) return invalid("tpmlp_forward: invalid shape");
-    if (!saved || !workspace) return invalid("tpmlp_forward: saved or workspace is NULL");
+    if (!workspace) return invalid("tpmlp_forward: workspace is NULL");
     if (!aligned16(workspace)) return TPMLP_ERR_UNSUPPORTED;
+    // Inference (saved == NULL): nothing is kept; Y goes to the workspace.
+    if (!saved)
+        return s->tokens == 0 ? check_ptrs(s, {A, a, B, b}, {X, Z}) : check_ptrs(s, {X, A, a, B, b, Z}, {});
     // With no tokens the [T, .] tensors are empty and may have NULL data pointers.
     // Under recomputation H is the saved activation and Y lives in the workspace.
     const bool rec = recompute(s);
@@ -371,9 +374,11 @@ tpmlp_status tpmlp_forward(const tpmlp_shape *s, const void *X, const void *A, c
     tpmlp_status rc = validate_forward(s, X, A, a, B, b, Z, saved, workspace);
     if (rc != TPMLP_OK) return rc;
     const bool rec = recompute(s);
-    saved->X = X;
-    saved->A = A;
-    saved->B = B;
+    if (saved) {
+        saved->X = X;
+        saved->A = A;
+        saved->B = B;
+    }
     const int64_t T = s->tokens, h = s->hidden, F = s->ffn;
     if (T == 0) return TPMLP_OK;
     const int sms = num_sms_current();
@@ -381,14 +386,18 @@ tpmlp_status tpmlp_forward(const tpmlp_shape *s, const void *X, const void *A, c
     if (use_tc(s) && sms < 0) return TPMLP_ERR_DEVICE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint32_t *status = static_cast<uint32_t *>(workspace);
-    void *Y = rec ? static_cast<void *>(static_cast<uint8_t *>(workspace) + y_offset(s)) : saved->Y;
+    // Y: the caller's buffer; under recomputation the workspace's Y region; for
+    // inference (saved == NULL) the workspace's dY region, which only the
+    // backward pass uses.
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *Y = !saved ? static_cast<void *>(ws + dy_offset(s)) : (rec ? static_cast<void *>(ws + y_offset(s)) : saved->Y);
 
     // Column-parallel GEMM of all shards, bias and GeLU fused: H = X A + a, Y = GeLU(H).
     GemmArgs g1 = base_args(status);
     g1.a = X, g1.a_mn = false;  // X[T,h]: K-major
     g1.b = A, g1.b_mn = true;   // A[h,F]: N contiguous, MN-major
     g1.M = T, g1.N = F, g1.K = h, g1.kshard = h;
-    g1.out0 = saved->H, g1.out1 = Y, g1.bias = a;
+    g1.out0 = saved ? saved->H : nullptr, g1.out1 = Y, g1.bias = a;
     pick_raster(g1);
     cudaError_t e = gemm(s, "fc1_bias_gelu", tpmlp::EPI_BIAS_GELU, g1, sms, st);
     if (e != cudaSuccess) return from_cuda(e);

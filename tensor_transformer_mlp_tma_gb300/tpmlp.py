@@ -222,8 +222,10 @@ class Context:
         return self._ws_view(WS_DY)
 
 
-def forward(ctx: Context, X, A, a, B, b, Z=None, stream=None):
-    """Z = GeLU(X A + a) B + b with the t-shard fold; fills ctx.H, ctx.Y."""
+def forward(ctx: Context, X, A, a, B, b, Z=None, stream=None, inference=False):
+    """Z = GeLU(X A + a) B + b with the t-shard fold; fills ctx.H, ctx.Y.
+    inference=True passes no saved record: nothing is kept for backward (Y goes
+    to the workspace's dY region, H is not stored)."""
     s = ctx.shape
     T, h, F = s.tokens, s.hidden, s.ffn
     for x, n, shp in ((X, "X", (T, h)), (A, "A", (h, F)), (a, "a", (F,)), (B, "B", (F, h)), (b, "b", (h,))):
@@ -233,7 +235,7 @@ def forward(ctx: Context, X, A, a, B, b, Z=None, stream=None):
     _need(Z, "Z", ctx.dtype, (T, h))
     ctx._keep = [X, A, B]
     st = lib.tpmlp_forward(ctypes.byref(s), _ptr(X), _ptr(A), _ptr(a), _ptr(B), _ptr(b), _ptr(Z),
-                           ctypes.byref(ctx.saved), _ptr(ctx.workspace), _stream(stream))
+                           None if inference else ctypes.byref(ctx.saved), _ptr(ctx.workspace), _stream(stream))
     _check(st, "tpmlp_forward")
     return Z
 

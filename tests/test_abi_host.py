@@ -92,6 +92,24 @@ def _fwd(tp, shape, ptrs=None, saved=None, ws=FAKE):
                                 ctypes.byref(sv), ws, None)
 
 
+def _fwd_inference(tp, shape, ptrs=None, ws=FAKE):
+    p = ptrs or [FAKE] * 6
+    return tp.lib.tpmlp_forward(ctypes.byref(shape), *p, None, ws, None)
+
+
+def test_forward_inference_validation(tp):
+    """saved == NULL (inference) is accepted by validation; the inputs are still checked."""
+    good = tp.make_shape(256, 256, 1024, 2, tp.BF16)
+    for i in range(6):
+        p = [FAKE] * 6
+        p[i] = None
+        assert _fwd_inference(tp, good, ptrs=p) == tp.ERR_INVALID_ARG
+    p = [FAKE] * 6
+    p[0] = FAKE + 2
+    assert _fwd_inference(tp, good, ptrs=p) == tp.ERR_UNSUPPORTED
+    assert _fwd_inference(tp, good, ws=None) == tp.ERR_INVALID_ARG
+
+
 def _bwd(tp, shape, ptrs=None, saved=None, ws=FAKE):
     p = ptrs or [FAKE] * 6
     sv = saved if saved is not None else tp.Saved(FAKE, FAKE, FAKE, FAKE, FAKE)

@@ -142,6 +142,24 @@ def test_misaligned_pointer_is_rejected():
     assert e.value.status == tpmlp.ERR_UNSUPPORTED
 
 
+def test_inference_forward_without_saved():
+    """tpmlp_forward with saved == NULL: Z is bit-identical to the training
+    forward, and Y is left in the workspace's dY region."""
+    from tensor_transformer_mlp_tma_gb300 import tpmlp
+    T, h, F, t = 300, 384, 1280, 2
+    inp = inputs.make(T, h, F, "bf16", seed=77, std=STD)
+    d = {k: v.cuda() for k, v in inp.items()}
+    ctx = tpmlp.Context(T, h, F, t, torch.bfloat16)
+    Z_train = tpmlp.forward(ctx, d["X"], d["A"], d["a"], d["B"], d["b"]).clone()
+    Y_train = ctx.Y.clone()
+    ctx2 = tpmlp.Context(T, h, F, t, torch.bfloat16)
+    Z_inf = tpmlp.forward(ctx2, d["X"], d["A"], d["a"], d["B"], d["b"], inference=True)
+    torch.cuda.synchronize()
+    assert tpmlp.check_device_status(ctx2) == tpmlp.OK
+    assert torch.equal(Z_inf, Z_train)
+    assert torch.equal(ctx2.dY, Y_train)
+
+
 def test_inference_forward_without_H():
     from tensor_transformer_mlp_tma_gb300 import tpmlp
     T, h, F, t = 300, 384, 1280, 2
