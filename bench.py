@@ -173,6 +173,25 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def host_cpu() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
 # ------------------------------------------------------------------ oracle leg
 def oracle_sample(w, tokens: int):
     """Time the fp64 oracle on the first `tokens` rows of the workload (full
@@ -227,7 +246,7 @@ def run_reference(args, rank, world):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(w, t, world),
             "cpu_baseline": {"value": val, "unit": UNIT, "cores": oracle.num_threads(lib), "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "cpu": host_cpu()},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -574,6 +593,7 @@ def main():
             w = WORKLOADS[args.workload]
             secs, fl, cores = oracle_sample(w, args.oracle_tokens)
             line["cpu_baseline"] = {"value": fl / secs / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                    "cpu": host_cpu(),
                                     "sample": "first %d of %d token rows of %s, full weights, fp64 (%.1f s)"
                                               % (args.oracle_tokens, w.tokens, w.name, secs)}
         print(json.dumps(line), flush=True)
