@@ -748,16 +748,13 @@ tpmlp_shape attn_route(const tpmlp_attn_shape *s) {
     return m;
 }
 
-tpmlp::HeadLayout head_layout(const tpmlp_attn_shape *s, bool qkv) {
+tpmlp::HeadLayout head_layout(const tpmlp_attn_shape *s) {
     tpmlp::HeadLayout L;
     L.nb = s->batch;
     L.S = s->seq;
     L.h = s->hidden;
     L.heads = s->heads;
     L.d = s->hidden / s->heads;
-    L.t = s->t;
-    L.qkv = qkv;
-    L.nmat = qkv ? 3 : 1;
     return L;
 }
 
@@ -1004,7 +1001,7 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
 
     {
         Timed timed("attn_bwd_rowdot", st);
-        e = tpmlp::launch_rowdot(head_layout(s, false), dO, saved->O, D, st);
+        e = tpmlp::launch_rowdot(head_layout(s), dO, saved->O, D, st);
         if (e != cudaSuccess) return from_cuda(e);
         g_launches.fetch_add(1);
     }

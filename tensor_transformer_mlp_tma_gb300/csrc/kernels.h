@@ -117,14 +117,10 @@ int64_t ln_partial_floats(int64_t rows, int64_t h);
 cudaError_t launch_ln_forward(bool is_bf16, const LnArgs &a, cudaStream_t st);
 cudaError_t launch_ln_backward(bool is_bf16, const LnArgs &a, cudaStream_t st, int *launches);
 
-// Attention support.  Problem z = b*heads + g; token-major data is QKV [T, 3h]
-// with shard-major columns (qkv = true, nmat = 3: Q, K, V) or O [T, h] (qkv =
-// false, nmat = 1).
+// Attention support.  Problem z = b*heads + g over `nb` sequences of S tokens;
+// token-major O and dO are [T, h] with head g at columns [g*d, (g+1)*d).
 struct HeadLayout {
     int64_t nb, S, h, heads, d;
-    int t;
-    bool qkv;
-    int nmat;
 };
 cudaError_t launch_softmax(const float *S, void *P, int64_t rows, int64_t cols, bool causal, cudaStream_t st);
 // D[z*S + s] = row dot of dO and O over head g's columns of token b*S + s (token-major inputs).
