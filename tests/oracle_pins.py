@@ -18,6 +18,9 @@ What pins what:
                  (Z = Y_1 B_1 + Y_2 B_2 for t = 2).
   * backward  -- central finite differences of L = sum(dZ * Z) for every element
                  of X, A, a, B and b; the dX shard partials against numpy.
+  * worked example -- tests/golden/worked_example_t2.txt: the two-shard split of
+                 section 4.1 with pre-activations of exactly 10, -10 and 0, every
+                 forward, backward and shard-partial value worked by hand.
   * closed forms -- X = 0 gives Z = gelu(a) B + b and dA = 0; A = 0, a = 0 give
                  Z = b, dY = dZ B^T / 2, dX = 0; db is the column sum of dZ.
   * slices    -- the exact row/column slices equal the full result.
@@ -36,6 +39,8 @@ What pins what:
 from __future__ import annotations
 
 import math
+
+import os
 
 import numpy as np
 
@@ -141,6 +146,46 @@ def check_worked_example_t2(lib):
         f.append("t=2 worked example: partials differ")
     if _rel(out["Y"], np.concatenate([Y1, Y2], axis=1)) > 1e-12:
         f.append("t=2 worked example: Y is not [Y_1, Y_2]")
+    return f
+
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def read_golden(name: str) -> dict:
+    """A tests/golden fixture: scalars as 'name value', matrices as 'name rows
+    cols' followed by the rows; '#' starts a comment line."""
+    out, lines = {}, [ln.split() for ln in open(os.path.join(GOLDEN, name))
+                      if ln.strip() and not ln.lstrip().startswith("#")]
+    i = 0
+    while i < len(lines):
+        f = lines[i]
+        if len(f) == 2:
+            out[f[0]] = int(f[1])
+            i += 1
+        else:
+            r, c = int(f[1]), int(f[2])
+            out[f[0]] = np.array([[float(x) for x in lines[i + 1 + k]] for k in range(r)]).reshape(r, c)
+            i += 1 + r
+    return out
+
+
+def check_golden_worked_example_t2(lib):
+    """The hand-worked two-shard example of tests/golden/worked_example_t2.txt
+    (report section 4.1's two-GPU split, pre-activations of exactly 10, -10 and
+    0): forward, backward and both sets of shard partials."""
+    g = read_golden("worked_example_t2.txt")
+    t = g["t"]
+    fw = oracle.forward(g["X"], g["A"], g["a"].ravel(), g["B"], g["b"].ravel(), t, parts=True, lib=lib)
+    bw = oracle.backward(g["X"], g["A"], g["B"], fw["H"], fw["Y"], g["dZ"], t, parts=True, lib=lib)
+    got = {"H": fw["H"], "Y": fw["Y"], "Z": fw["Z"], "Z1": fw["Zpart"][0], "Z2": fw["Zpart"][1],
+           "dY": bw["dY"], "da": bw["da"][None, :], "db": bw["db"][None, :], "dB": bw["dB"], "dA": bw["dA"],
+           "dX": bw["dX"], "dX1": bw["dXpart"][0], "dX2": bw["dXpart"][1]}
+    f = []
+    for k, v in got.items():
+        err = float(np.max(np.abs(v - g[k])))
+        if err > 1e-12 * max(1.0, float(np.max(np.abs(g[k])))):
+            f.append("golden t=2 example: %s differs by %.3e" % (k, err))
     return f
 
 
@@ -468,7 +513,7 @@ def check_attn_fd(lib, eps_fd=1e-6, tol=1e-6):
 
 
 ALL = [check_gelu_vs_erf, check_gelu_identities, check_gelu_prime_fd, check_forward_numpy,
-       check_worked_example_t2, check_backward_fd, check_backward_partials,
+       check_worked_example_t2, check_golden_worked_example_t2, check_backward_fd, check_backward_partials,
        check_closed_forms, check_slice_vs_full, check_layernorm_numpy, check_layernorm_invariants,
        check_layernorm_backward_fd, check_sp_composition_fd, check_attn_numpy, check_attn_sharding,
        check_attn_causal, check_attn_fd]
