@@ -142,6 +142,27 @@ def test_misaligned_pointer_is_rejected():
     assert e.value.status == tpmlp.ERR_UNSUPPORTED
 
 
+def test_golden_worked_example_fp32():
+    """The hand-worked two-shard example of tests/golden/worked_example_t2.txt on
+    the fp32 FFMA path: every output matches the hand-derived values to fp32
+    rounding (they are small integers and halves)."""
+    from tensor_transformer_mlp_tma_gb300 import tpmlp
+    from oracle_pins import read_golden
+    g = read_golden("worked_example_t2.txt")
+    d = {k: torch.tensor(g[k], dtype=torch.float32, device="cuda") for k in ("X", "A", "B", "dZ")}
+    a = torch.tensor(g["a"].ravel(), dtype=torch.float32, device="cuda")
+    b = torch.tensor(g["b"].ravel(), dtype=torch.float32, device="cuda")
+    ctx = tpmlp.Context(g["T"], g["h"], g["F"], g["t"], torch.float32)
+    Z = tpmlp.forward(ctx, d["X"], d["A"], a, d["B"], b)
+    out = tpmlp.backward(ctx, d["dZ"])
+    torch.cuda.synchronize()
+    assert tpmlp.check_device_status(ctx) == tpmlp.OK
+    got = {"H": ctx.H, "Y": ctx.Y, "Z": Z, "dY": ctx.dY, "dA": out["dA"], "dB": out["dB"], "dX": out["dX"],
+           "da": out["da"][None, :], "db": out["db"][None, :]}
+    for k, v in got.items():
+        assert np.allclose(to_np(v), g[k], rtol=0, atol=1e-5), (k, to_np(v), g[k])
+
+
 def test_inference_forward_without_saved():
     """tpmlp_forward with saved == NULL: Z is bit-identical to the training
     forward, and Y is left in the workspace's dY region."""
