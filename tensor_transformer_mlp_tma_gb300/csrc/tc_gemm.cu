@@ -90,6 +90,7 @@ struct Params {
     const float *rowvec;
     int causal_k;    // K range of an M-tile: 0 all; 1 k < end of the tile's rows; 2 k >= start of its rows
     int skip_upper;  // tiles wholly above the diagonal (every column past every row) are not computed
+    int flip_odd;    // odd problems walk their M-tiles in reverse order (load balance under causal ranges)
     int a_mn4, b_mn4;  // MN-major operand mapped as 4-D (all of a stage's 64-wide blocks in one copy)
     // Bias gradient from the MMA (EPI_STORE with MN-major A): one extra M-tile
     // whose A is a 64 x 64 block of ones (map tmO2), so its first accumulator
@@ -186,6 +187,13 @@ __device__ __forceinline__ void tile_coords(int tile, const Params &p, int &mb, 
     const int slow = local / gsize;
     mb = p.raster_n ? slow : fast;
     nb = p.raster_n ? fast : slow;
+    // Under causal K ranges (or skipped upper tiles) an M-tile's work grows or
+    // shrinks with its index.  A unit takes every num_units-th tile, so problems
+    // walked in order hand each unit the same few M-tile indices again and again
+    // (76 units and 8 M-tiles: two indices per unit).  Walking the M-tiles of
+    // every odd problem backwards gives each unit a mix of heavy and light
+    // tiles, and the tiles of one problem stay adjacent (sharing operands in L2).
+    if (p.flip_odd && (zb & 1)) mb = p.m_tiles - 1 - mb;
 }
 
 // Records a timeout once in the status word (detail = which role gave up).
@@ -1198,6 +1206,11 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     p.bias_grad = g.bias_grad;
     if (bias_tile) p.m_tiles += 1;  // the ones tile, after every row of the output
     p.skip_upper = g.skip_upper ? 1 : 0;
+    // TPMLP_FLIP_ODD=0 keeps every problem's M-tiles in order (a tuning knob, read per call).
+    {
+        const char *flip = std::getenv("TPMLP_FLIP_ODD");
+        p.flip_odd = (g.causal_k != 0 || g.skip_upper) && !(flip && flip[0] == '0') ? 1 : 0;
+    }
     // The causal ranges are defined for square per-head problems in one shard.
     if ((g.causal_k != 0 || g.skip_upper) && (g.nshards != 1 || (g.causal_k != 0 && g.M != g.K))) {
         set_last_error("causal K ranges need one shard and M = K (M=%lld K=%lld, %d shards)",
