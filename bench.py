@@ -42,12 +42,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, with the hash of the kernel source they were taken at.  A kernel whose
 # source has changed since reports traffic null.
 NCU_TRAFFIC = {  # profiles/dram_traffic_h8192_gemms.md (h8192 workload)
-    "fc1_bias_gelu": (2.189950e9 + 0.519356e9, "bf58902d685d"),
-    "fc2_shard_fold": (2.767711e9 + 0.108464e9, "bf58902d685d"),
-    "bwd_dY_dgelu": (3.167461e9 + 0.275350e9, "bf58902d685d"),
-    "bwd_dB": (1.156275e9 + 0.520084e9, "bf58902d685d"),
-    "bwd_dA": (1.074235e9 + 0.518396e9, "bf58902d685d"),
-    "bwd_dX_shard_fold": (3.496686e9 + 0.106172e9, "bf58902d685d"),
+    "fc1_bias_gelu": (1.988987e9 + 0.519648e9, "57a2ba7513ad"),
+    "fc2_shard_fold": (2.295506e9 + 0.092963e9, "57a2ba7513ad"),
+    "bwd_dY_dgelu": (2.646548e9 + 0.274623e9, "57a2ba7513ad"),
+    "bwd_dB": (1.007968e9 + 0.517005e9, "57a2ba7513ad"),
+    "bwd_dA": (0.979500e9 + 0.516222e9, "57a2ba7513ad"),
+    "bwd_dX_shard_fold": (2.528508e9 + 0.090992e9, "57a2ba7513ad"),
 }
 
 
