@@ -5,14 +5,16 @@
 // Tiles are 256 x 256 on CTA pairs (a 2-CTA cluster, tcgen05 cta_group::2: each
 // CTA loads its 128 rows of A and 128 of B's 256 columns, the even CTA issues the
 // MMAs, each CTA's TMEM holds its 128 rows of the accumulator) or 128 x 256 on
-// single CTAs.  One persistent CTA per SM, 10 warps:
-//   warp 0      TMA producer (one elected lane): fills a 4-stage ring of
-//               128x64 A tiles and 256x64 B tiles, 128-byte swizzled.
+// single CTAs.  Outputs at most 128 wide take 256 x 128 tiles on CTA pairs.
+// One persistent CTA per SM, 10 warps:
+//   warp 0      TMA producer (one elected lane): fills a ring of stages (4 to 8)
+//               of 128x64 A tiles and B tiles of the CTA's columns, 128-byte
+//               swizzled.
 //   warp 1      MMA issuer (one elected lane) and owner of the 512 TMEM columns:
-//               two 128x256 fp32 accumulators, used alternately per
-//               "accumulation unit" (one K range of one output tile).
+//               two fp32 accumulators (128 lanes x tile width), used alternately
+//               per "accumulation unit" (one K range of one output tile).
 //   warps 2..9  epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (its rows) and
-//               columns 128*((w-2)/4)..+127 of the accumulator.
+//               one half of the accumulator's columns, (w-2)/4.
 //
 // The all-reduce of the t shard partials ("Megatron-LM" report, section 4.1,
 // Z = sum_i Y_i B_i; section 4.2 for dX in the backward direction) becomes the
@@ -42,7 +44,7 @@ namespace tpmlp {
 namespace tc {
 
 constexpr int BM = 128;   // accumulator rows per CTA (TMEM lanes)
-constexpr int BN = 256;   // accumulator columns
+constexpr int BN = 256;   // accumulator columns of the wide tile (the narrow one has 128)
 constexpr int BK = 64;    // 64 bf16 = one 128-byte swizzle row
 constexpr int NUM_THREADS = 320;
 constexpr int EPI_THREADS = 256;
@@ -57,17 +59,22 @@ constexpr int STG_PER_WARP = 2 * STG_BOX;
 // all of B's 256 columns.  CG = 2: a CTA pair computes a 256 x 256 tile with
 // CTA-pair MMAs; each CTA loads its own 128 rows of A and 128 of B's columns, so
 // a stage is 32 KB instead of 48 KB and six stages fit.
-template <int CG>
+//
+// TILE_N = 128 (CTA pairs only) is the narrow tile for outputs at most 128 wide
+// (the per-head products with N = d): each CTA loads 64 of B's columns, a stage
+// is 24 KB and eight stages fit.
+template <int CG, int TILE_N_ = BN>
 struct Cfg {
     static constexpr int TILE_M = BM * CG;
-    static constexpr int B_ROWS = BN / CG;
+    static constexpr int TILE_N = TILE_N_;
+    static constexpr int B_ROWS = TILE_N / CG;
     static constexpr int A_STAGE = BM * BK * 2;
     static constexpr int B_STAGE = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-    static constexpr int STAGES = CG == 1 ? 4 : 6;
+    static constexpr int STAGES = CG == 1 ? 4 : (TILE_N == BN ? 6 : 8);
     static constexpr int SMEM_DYN = STAGES * STAGE_BYTES + (EPI_THREADS / 32) * STG_PER_WARP + 1024;
 };
-constexpr int MAX_STAGES = 6;
+constexpr int MAX_STAGES = 8;
 
 constexpr uint32_t STATUS_TIMEOUT = 4;  // TPMLP_ERR_TIMEOUT
 
@@ -164,9 +171,9 @@ __device__ __forceinline__ void k_range(const Params &p, int mb, int &kb0, int &
 
 // Scores and dS are not needed above the diagonal: a tile whose first column lies
 // past its last row is skipped by every role (none of its outputs is read).
-template <int TILE_M>
+template <int TILE_M, int TILE_N = BN>
 __device__ __forceinline__ bool tile_active(const Params &p, int mb, int nb) {
-    return !p.skip_upper || nb * BN <= mb * TILE_M + TILE_M - 1;
+    return !p.skip_upper || nb * TILE_N <= mb * TILE_M + TILE_M - 1;
 }
 
 // Tile order: super-rows of `group` tiles along one dimension; inside a
@@ -502,15 +509,18 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
     }
 }
 
-template <int EPI, bool A_MN, bool B_MN, int CG, bool HEADS>
+template <int EPI, bool A_MN, bool B_MN, int CG, bool HEADS, int TILE_N>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
                 const __grid_constant__ CUtensorMap tmO2, const Params p) {
-    using C = Cfg<CG>;
+    using C = Cfg<CG, TILE_N>;
     constexpr bool PAIR = CG == 2;
     constexpr bool FOLD = (EPI == EPI_FOLD_BIAS || EPI == EPI_FOLD);
-    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(C::TILE_M, BN, A_MN, B_MN);
+    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(C::TILE_M, TILE_N, A_MN, B_MN);
+    // each epilogue warp finishes TILE_N / 2 columns of its 32 rows, in 32-column chunks
+    constexpr int CHUNKS = TILE_N / 64;
+    static_assert(TILE_N == BN || (TILE_N == 128 && CG == 2 && EPI == EPI_STORE), "narrow tile: CTA pairs, plain store");
     constexpr int STAGES = C::STAGES;
 
     extern __shared__ uint8_t smem_raw[];
@@ -591,9 +601,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
                 int mb, nb, zb;
                 tile_coords(tile, p, mb, nb, zb);
-                if (!tile_active<C::TILE_M>(p, mb, nb)) continue;
+                if (!tile_active<C::TILE_M, C::TILE_N>(p, mb, nb)) continue;
                 const int m0 = mb * C::TILE_M + BM * static_cast<int>(rank);
-                const int n0 = nb * BN + C::B_ROWS * static_cast<int>(rank);
+                const int n0 = nb * TILE_N + C::B_ROWS * static_cast<int>(rank);
                 int kb0, kb1;
                 k_range<C::TILE_M>(p, mb, kb0, kb1);
                 if constexpr (EPI == EPI_STORE && A_MN && B_MN && !HEADS) {
@@ -746,7 +756,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
                 int mb, nb, zb;
                 tile_coords(tile, p, mb, nb, zb);
-                if (!tile_active<C::TILE_M>(p, mb, nb)) continue;
+                if (!tile_active<C::TILE_M, C::TILE_N>(p, mb, nb)) continue;
                 int kb0, kb1;
                 k_range<C::TILE_M>(p, mb, kb0, kb1);
                 // one shard: the tile's k-block range; several: kb_per_shard blocks each
@@ -759,7 +769,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + buf * BN;
+                    const uint32_t d_tmem = tmem_base + buf * TILE_N;
                     // Stages are taken two at a time: wait for both, then issue their
                     // eight MMAs back to back.  Measured on GB300 this issues 2-7% faster
                     // per clock than one stage at a time (MN/MN GEMMs gain once their
@@ -826,12 +836,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int ew = warp - 2;                         // 0..7
         const int quarter = warp & 3;                    // TMEM lanes this warp may read
-        const int half = ew >> 2;                        // column half of the 256-wide tile
+        const int half = ew >> 2;                        // column half of the tile
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t stg = smem_base + STAGES * C::STAGE_BYTES + ew * STG_PER_WARP;
         uint32_t unit = 0;
         bool ok = true;
-        float sum[FOLD ? 128 : 1];
+        float sum[FOLD ? TILE_N / 2 : 1];
         (void)sum;
         AuxLoad aux{ptx::smem_u32(&bar_aux[ew]), 0u, false};
         // After every lane's tcgen05.ld of the buffer has completed, one arrival
@@ -855,10 +865,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (tile + num_units >= num_tiles) ptx::griddep_launch_dependents();
             int mb, nb, zb;
             tile_coords(tile, p, mb, nb, zb);
-            if (!tile_active<C::TILE_M>(p, mb, nb)) continue;
+            if (!tile_active<C::TILE_M, C::TILE_N>(p, mb, nb)) continue;
             const int row0 = mb * C::TILE_M + BM * static_cast<int>(rank) + quarter * 32;
             const int64_t row = static_cast<int64_t>(row0) + lane;
-            const int col0 = nb * BN + half * 128;
+            const int col0 = nb * TILE_N + half * (TILE_N / 2);
             if constexpr (EPI == EPI_DGELU || EPI == EPI_ATTN_DS)
                 aux_issue(&tmO1, aux, stg + STG_BOX, col0, row0, zb, lane);
             for (int s = 0; s < p.nshards; ++s, ++unit) {
@@ -871,10 +881,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t taddr = tmem_base + lane_off + buf * BN + half * 128;
+                const uint32_t taddr = tmem_base + lane_off + buf * TILE_N + half * (TILE_N / 2);
                 if constexpr (FOLD) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < CHUNKS; ++c) {
                         uint32_t r[32];
                         ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
                         ptx::tmem_ld_wait(r);
@@ -887,7 +897,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     release(buf);
                     if (s == p.nshards - 1) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
+                        for (int c = 0; c < CHUNKS; ++c) {
                             float v[32];
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = sum[c * 32 + i];
@@ -898,11 +908,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (EPI == EPI_STORE && A_MN && B_MN && p.bias_tile && mb == p.m_tiles - 1) {
                         // The ones tile: its row 0 holds the column sums of B; it has no
                         // rows of the output (all of them lie past M).
-                        for (int c = 0; c < 4; ++c) {
+                        for (int c = 0; c < CHUNKS; ++c) {
                             uint32_t r[32];
                             ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
                             ptx::tmem_ld_wait(r);
-                            if (c == 3) release(buf);
+                            if (c == CHUNKS - 1) release(buf);
                             if (rank == 0 && quarter == 0 && lane == 0) {
                                 float v[32];
 #pragma unroll
@@ -913,17 +923,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         continue;
                     }
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < CHUNKS; ++c) {
                         uint32_t r[32];
                         ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
                         ptx::tmem_ld_wait(r);
                         // the whole accumulator slice is in registers: release the buffer
-                        if (c == 3) release(buf);
+                        if (c == CHUNKS - 1) release(buf);
                         float v[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
                         finish_chunk<EPI, HEADS>(p, &tmO0, &tmO1, &tmO2, v, row, row0, col0 + c * 32, zb, lane, stg, &aux,
-                                          c < 3 ? col0 + (c + 1) * 32 : -1, row0, &abort_sh);
+                                          c < CHUNKS - 1 ? col0 + (c + 1) * 32 : -1, row0, &abort_sh);
                     }
                 }
             }
@@ -1060,10 +1070,10 @@ static bool make_map_view(CUtensorMap *m, const void *ptr, const HeadView &v, ui
     return r == CUDA_SUCCESS;
 }
 
-template <int EPI, bool A_MN, bool B_MN, int CG, bool HEADS = false>
+template <int EPI, bool A_MN, bool B_MN, int CG, bool HEADS = false, int TILE_N = BN>
 static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
-    using C = Cfg<CG>;
-    auto kern = gemm_kernel<EPI, A_MN, B_MN, CG, HEADS>;
+    using C = Cfg<CG, TILE_N>;
+    auto kern = gemm_kernel<EPI, A_MN, B_MN, CG, HEADS, TILE_N>;
     // Per-device, once: the shared-memory opt-in, and for CTA pairs the number of
     // 2-CTA clusters that can be resident at once (the persistent grid size).
     static std::mutex mu;
@@ -1172,7 +1182,7 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     p.M = static_cast<int>(g.M);
     p.N = static_cast<int>(g.N);
     p.m_tiles = static_cast<int>((g.M + C::TILE_M - 1) / C::TILE_M);
-    p.n_tiles = static_cast<int>((g.N + BN - 1) / BN);
+    p.n_tiles = static_cast<int>((g.N + TILE_N - 1) / TILE_N);
     p.raster_n = g.raster_n ? 1 : 0;
     {
         const int fast_tiles = p.raster_n ? p.n_tiles : p.m_tiles;
@@ -1253,9 +1263,18 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
 template <int EPI, bool A_MN, bool B_MN>
 static cudaError_t launch_cg(const GemmArgs &g, int num_sms, cudaStream_t st) {
     if constexpr (EPI == EPI_ATTN_SCORE || EPI == EPI_ATTN_DS || EPI == EPI_STORE) {
-        if (g.heads_layout)
+        if (g.heads_layout) {
+            // Outputs at most 128 wide (the per-head products with N = d) take the
+            // narrow tile: the wide one would spend half its MMA work on columns
+            // past N.  TPMLP_NARROW=0 keeps the wide tile (a tuning knob, read per call).
+            if constexpr (EPI == EPI_STORE) {
+                const char *nar = std::getenv("TPMLP_NARROW");
+                if (g.cta_pair && g.N <= 128 && !(nar && nar[0] == '0'))
+                    return launch_t<EPI, A_MN, B_MN, 2, true, 128>(g, num_sms, st);
+            }
             return g.cta_pair ? launch_t<EPI, A_MN, B_MN, 2, true>(g, num_sms, st)
                               : launch_t<EPI, A_MN, B_MN, 1, true>(g, num_sms, st);
+        }
     }
     return g.cta_pair ? launch_t<EPI, A_MN, B_MN, 2>(g, num_sms, st) : launch_t<EPI, A_MN, B_MN, 1>(g, num_sms, st);
 }

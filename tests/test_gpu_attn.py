@@ -227,3 +227,15 @@ def test_tile_order_does_not_change_results(tp, monkeypatch):
     _, inorder, _ = run_attn(tp, nb, S, h, heads, t, seed=21)
     for k in TOL:
         assert torch.equal(fwd[k], inorder[k]), k
+
+
+def test_wide_tiles_match_oracle(tp, monkeypatch):
+    """The per-head products with N = d take 256 x 128 tiles by default;
+    TPMLP_NARROW=0 runs them on the 256 x 256 tiles, with the same results."""
+    monkeypatch.setenv("TPMLP_NARROW", "0")
+    nb, S, h, heads, t = 1, 520, 512, 8, 4
+    inp, out, _ = run_attn(tp, nb, S, h, heads, t, seed=10)
+    ref = oracle_ref(inp, nb, heads, t)
+    errs = {k: rel(to_np(out[k]), ref[k]) for k in TOL}
+    bad = {k: v for k, v in errs.items() if not (v <= TOL[k])}
+    assert not bad, "outside tolerance: %s (all: %s)" % (bad, errs)
