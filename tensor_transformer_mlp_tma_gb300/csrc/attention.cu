@@ -102,9 +102,57 @@ __global__ void __launch_bounds__(256)
         out[c] = __float2bfloat16_rn(c <= last ? expf(in[c] - mx) * inv : 0.0f);
 }
 
-// One warp per (token r, head g): D[z*S + s] = sum_e dO[r, g*d + e] * O[r, g*d + e]
-// over the token-major [T, h] arrays, written in per-head order (z = b*heads + g,
-// r = b*S + s).  d is a multiple of 8.
+// D[z*S + s] = sum_e dO[r, g*d + e] * O[r, g*d + e] over the token-major [T, h]
+// arrays, written in per-head order (z = b*heads + g, r = b*S + s).  d is a
+// multiple of 8; a lane takes 8 consecutive elements (one 16-byte load of each
+// array) and its dot product is 4 fused pairs in element order.
+__device__ __forceinline__ float dot8(const uint4 va, const uint4 vb) {
+    const uint32_t ua[4] = {va.x, va.y, va.z, va.w}, ub[4] = {vb.x, vb.y, vb.z, vb.w};
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&ua[i]);
+        const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162 *>(&ub[i]);
+        s += __low2float(x) * __low2float(y) + __high2float(x) * __high2float(y);
+    }
+    return s;
+}
+
+// One block per token row, for d / 8 a power of two up to 32: thread j takes the
+// row's 8-element chunks j, j + 256, ..., four of them in flight at once, and
+// the d / 8 lanes that hold one head's chunks add them by shuffles (butterfly).
+constexpr int ROWDOT_UNROLL = 4;
+__global__ void __launch_bounds__(256)
+    rowdot_row_kernel(const HeadLayout L, const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ b,
+                      float *__restrict__ D) {
+    const int64_t r = blockIdx.x;
+    const int64_t chunks = L.h / 8;
+    const int G = static_cast<int>(L.d / 8);
+    const int64_t bi = r / L.S, s = r % L.S;
+    const uint4 *pa = reinterpret_cast<const uint4 *>(a + r * L.h);
+    const uint4 *pb = reinterpret_cast<const uint4 *>(b + r * L.h);
+    for (int64_t j0 = 0; j0 < chunks; j0 += 256 * ROWDOT_UNROLL) {
+        uint4 va[ROWDOT_UNROLL], vb[ROWDOT_UNROLL];
+#pragma unroll
+        for (int u = 0; u < ROWDOT_UNROLL; ++u) {
+            const int64_t j = j0 + u * 256 + threadIdx.x;
+            va[u] = vb[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (j < chunks) {
+                va[u] = __ldg(pa + j);
+                vb[u] = __ldg(pb + j);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < ROWDOT_UNROLL; ++u) {
+            float v = dot8(va[u], vb[u]);
+            for (int off = G / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            const int64_t j = j0 + u * 256 + threadIdx.x;
+            if (j < chunks && threadIdx.x % G == 0) D[(bi * L.heads + j / G) * L.S + s] = v;
+        }
+    }
+}
+
+// One warp per (token r, head g), for any d that is a multiple of 8.
 __global__ void __launch_bounds__(256)
     rowdot_kernel(const HeadLayout L, const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ b,
                   float *__restrict__ D) {
@@ -114,17 +162,8 @@ __global__ void __launch_bounds__(256)
     const int64_t r = row / L.heads, g = row % L.heads;
     const int64_t base = r * L.h + g * L.d;
     float s = 0.0f;
-    for (int64_t e = static_cast<int64_t>(lane) * 8; e < L.d; e += 256) {
-        const uint4 va = __ldg(reinterpret_cast<const uint4 *>(a + base + e));
-        const uint4 vb = __ldg(reinterpret_cast<const uint4 *>(b + base + e));
-        const uint32_t ua[4] = {va.x, va.y, va.z, va.w}, ub[4] = {vb.x, vb.y, vb.z, vb.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&ua[i]);
-            const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162 *>(&ub[i]);
-            s += __low2float(x) * __low2float(y) + __high2float(x) * __high2float(y);
-        }
-    }
+    for (int64_t e = static_cast<int64_t>(lane) * 8; e < L.d; e += 256)
+        s += dot8(__ldg(reinterpret_cast<const uint4 *>(a + base + e)), __ldg(reinterpret_cast<const uint4 *>(b + base + e)));
     s = warp_sum(s);
     if (lane == 0) D[((r / L.S) * L.heads + g) * L.S + r % L.S] = s;
 }
@@ -152,6 +191,12 @@ cudaError_t launch_softmax(const float *S, void *P, int64_t rows, int64_t cols, 
 cudaError_t launch_rowdot(const HeadLayout &L, const void *a, const void *b, float *D, cudaStream_t st) {
     const int64_t rows = L.nb * L.S * L.heads;
     if (rows <= 0) return cudaSuccess;
+    const int64_t G = L.d / 8;
+    if (G >= 1 && G <= 32 && (G & (G - 1)) == 0) {
+        attn::rowdot_row_kernel<<<static_cast<unsigned>(L.nb * L.S), 256, 0, st>>>(
+            L, static_cast<const __nv_bfloat16 *>(a), static_cast<const __nv_bfloat16 *>(b), D);
+        return cudaGetLastError();
+    }
     attn::rowdot_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
         L, static_cast<const __nv_bfloat16 *>(a), static_cast<const __nv_bfloat16 *>(b), D);
     return cudaGetLastError();
