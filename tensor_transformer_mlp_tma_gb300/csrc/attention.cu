@@ -118,24 +118,27 @@ __device__ __forceinline__ float dot8(const uint4 va, const uint4 vb) {
     return s;
 }
 
-// One block per token row, for d / 8 a power of two up to 32: thread j takes the
-// row's 8-element chunks j, j + 256, ..., four of them in flight at once, and
-// the d / 8 lanes that hold one head's chunks add them by shuffles (butterfly).
-constexpr int ROWDOT_UNROLL = 4;
-__global__ void __launch_bounds__(256)
+// One block of ROWDOT_THREADS per token row, for d / 8 a power of two up to 32:
+// thread j takes the row's 8-element chunks j, j + ROWDOT_THREADS, ..., two of
+// them in flight at once, and the d / 8 lanes that hold one head's chunks add
+// them by shuffles (butterfly).  40 registers: 12 blocks (8 KB of loads in
+// flight each) stay resident per SM.
+constexpr int ROWDOT_THREADS = 128;
+constexpr int ROWDOT_UNROLL = 2;
+__global__ void __launch_bounds__(ROWDOT_THREADS)
     rowdot_row_kernel(const HeadLayout L, const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ b,
                       float *__restrict__ D) {
-    const int64_t r = blockIdx.x;
-    const int64_t chunks = L.h / 8;
+    const int r = static_cast<int>(blockIdx.x), S = static_cast<int>(L.S);
+    const int chunks = static_cast<int>(L.h / 8);
     const int G = static_cast<int>(L.d / 8);
-    const int64_t bi = r / L.S, s = r % L.S;
-    const uint4 *pa = reinterpret_cast<const uint4 *>(a + r * L.h);
-    const uint4 *pb = reinterpret_cast<const uint4 *>(b + r * L.h);
-    for (int64_t j0 = 0; j0 < chunks; j0 += 256 * ROWDOT_UNROLL) {
+    const uint4 *pa = reinterpret_cast<const uint4 *>(a + static_cast<int64_t>(r) * L.h);
+    const uint4 *pb = reinterpret_cast<const uint4 *>(b + static_cast<int64_t>(r) * L.h);
+    float *out = D + static_cast<int64_t>(r / S) * L.heads * S + r % S;  // + head * S
+    for (int j0 = 0; j0 < chunks; j0 += ROWDOT_THREADS * ROWDOT_UNROLL) {
         uint4 va[ROWDOT_UNROLL], vb[ROWDOT_UNROLL];
 #pragma unroll
         for (int u = 0; u < ROWDOT_UNROLL; ++u) {
-            const int64_t j = j0 + u * 256 + threadIdx.x;
+            const int j = j0 + u * ROWDOT_THREADS + static_cast<int>(threadIdx.x);
             va[u] = vb[u] = make_uint4(0u, 0u, 0u, 0u);
             if (j < chunks) {
                 va[u] = __ldg(pa + j);
@@ -146,8 +149,8 @@ __global__ void __launch_bounds__(256)
         for (int u = 0; u < ROWDOT_UNROLL; ++u) {
             float v = dot8(va[u], vb[u]);
             for (int off = G / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            const int64_t j = j0 + u * 256 + threadIdx.x;
-            if (j < chunks && threadIdx.x % G == 0) D[(bi * L.heads + j / G) * L.S + s] = v;
+            const int j = j0 + u * ROWDOT_THREADS + static_cast<int>(threadIdx.x);
+            if (j < chunks && threadIdx.x % G == 0) out[static_cast<int64_t>(j / G) * S] = v;
         }
     }
 }
@@ -193,7 +196,7 @@ cudaError_t launch_rowdot(const HeadLayout &L, const void *a, const void *b, flo
     if (rows <= 0) return cudaSuccess;
     const int64_t G = L.d / 8;
     if (G >= 1 && G <= 32 && (G & (G - 1)) == 0) {
-        attn::rowdot_row_kernel<<<static_cast<unsigned>(L.nb * L.S), 256, 0, st>>>(
+        attn::rowdot_row_kernel<<<static_cast<unsigned>(L.nb * L.S), attn::ROWDOT_THREADS, 0, st>>>(
             L, static_cast<const __nv_bfloat16 *>(a), static_cast<const __nv_bfloat16 *>(b), D);
         return cudaGetLastError();
     }
