@@ -52,27 +52,37 @@ def test_sp_block_matches_oracle(T, h, F, t, algo):
     compare_full(out, ref, TOL)
 
 
-def test_layernorm_alone_matches_oracle():
-    """Vector path (h % 8 == 0) at a full-size row length, and the scalar path on
-    a ragged row length; the input has a large common offset per row."""
+# (T, h, dtype): every LayerNorm kernel path.  bf16 rows of 8-element chunks take
+# the block-per-row kernels with 1 (h = 200), 2 (3000), 4 (8192) or 8 (12288)
+# chunks per thread; longer rows (20000) the warp-per-row vector kernels; rows
+# that are not whole 16-byte chunks (203) the scalar ones.  fp32 rows of
+# 4-element chunks: 1 chunk (1000) and 8 chunks (8100).
+LN_CASES = [(257, 8192, "bf16"), (33, 200, "bf16"), (9, 3000, "bf16"), (5, 12288, "bf16"), (3, 20000, "bf16"),
+            (7, 203, "bf16"), (11, 1000, "f32"), (4, 8100, "f32")]
+
+
+@pytest.mark.parametrize("T,h,dt", LN_CASES)
+def test_layernorm_alone_matches_oracle(T, h, dt):
+    """LayerNorm forward and backward on rows with a large common offset."""
     from tensor_transformer_mlp_tma_gb300 import tpmlp
-    for T, h in ((257, 8192), (33, 200)):
-        g = torch.Generator().manual_seed(h)
-        X = (torch.randn(T, h, generator=g) * 2 + 3).to(torch.bfloat16)
-        dXn = torch.randn(T, h, generator=g).to(torch.bfloat16)
-        gamma, beta = _ln_params(h, 11)
-        ctx = tpmlp.Context(T, h, 64, 1, torch.bfloat16, tpmlp.ALGO_SIMT, layernorm=True, eps=EPS)
-        tpmlp.ln_forward(ctx, X.cuda(), gamma.cuda(), beta.cuda())
-        bw = tpmlp.ln_backward(ctx, dXn.cuda())
-        torch.cuda.synchronize()
-        fw_ref = oracle.layernorm_forward(X, gamma, beta, EPS)
-        bw_ref = oracle.layernorm_backward(dXn, X, gamma, EPS)
-        assert rel(to_np(ctx.Xn), fw_ref["Y"]) <= 1e-2
-        assert rel(to_np(ctx.mean), fw_ref["mean"]) <= 1e-5
-        assert rel(to_np(ctx.rstd), fw_ref["rstd"]) <= 1e-5
-        for k in ("dX_in", "dgamma", "dbeta"):
-            ref = bw_ref["dX" if k == "dX_in" else k]
-            assert rel(to_np(bw[k]), ref) <= 2e-2, k
+    dtype = torch.bfloat16 if dt == "bf16" else torch.float32
+    tol_y, tol_g = (1e-2, 2e-2) if dt == "bf16" else (1e-5, 1e-5)
+    g = torch.Generator().manual_seed(h)
+    X = (torch.randn(T, h, generator=g) * 2 + 3).to(dtype)
+    dXn = torch.randn(T, h, generator=g).to(dtype)
+    gamma, beta = _ln_params(h, 11, dtype)
+    ctx = tpmlp.Context(T, h, 64, 1, dtype, tpmlp.ALGO_SIMT, layernorm=True, eps=EPS)
+    tpmlp.ln_forward(ctx, X.cuda(), gamma.cuda(), beta.cuda())
+    bw = tpmlp.ln_backward(ctx, dXn.cuda())
+    torch.cuda.synchronize()
+    fw_ref = oracle.layernorm_forward(X, gamma, beta, EPS)
+    bw_ref = oracle.layernorm_backward(dXn, X, gamma, EPS)
+    assert rel(to_np(ctx.Xn), fw_ref["Y"]) <= tol_y
+    assert rel(to_np(ctx.mean), fw_ref["mean"]) <= 1e-5
+    assert rel(to_np(ctx.rstd), fw_ref["rstd"]) <= 1e-5
+    for k in ("dX_in", "dgamma", "dbeta"):
+        ref = bw_ref["dX" if k == "dX_in" else k]
+        assert rel(to_np(bw[k]), ref) <= tol_g, k
 
 
 def test_sp_block_repeatable():
