@@ -206,6 +206,22 @@ def oracle_sample(w, tokens: int):
     return dt, 12.0 * tokens * w.hidden * w.ffn, oracle.num_threads(lib)
 
 
+def attn_oracle_sample(w, tokens: int, seed: int):
+    """Time the fp64 attention oracle on one sequence of `tokens` tokens with the
+    workload's h, heads and t (full weights); returns (seconds, flops, threads)."""
+    import dataclasses
+    import oracle
+    sw = dataclasses.replace(w, batch=1, seq=tokens)
+    inp = inputs.make_attn(tokens, w.hidden, seed, {"Wqkv": w.std_W, "Wo": w.std_W, "bqkv": w.std_b, "bo": w.std_b})
+    lib = oracle.load()
+    f64 = {k: oracle._f64(v) for k, v in inp.items()}
+    t0 = time.perf_counter()
+    oracle.attn_forward_backward(f64["X"], f64["Wqkv"], f64["bqkv"], f64["Wo"], f64["bo"], f64["dZ"], 1, w.heads,
+                                 w.t, lib=lib)
+    dt = time.perf_counter() - t0
+    return dt, sw.flops_fwd_bwd, oracle.num_threads(lib)
+
+
 def run_reference(args, rank, world):
     """The reference arm: the fp64 CPU oracle as it stands, on host cores."""
     if rank != 0:
@@ -259,6 +275,96 @@ def config_of(w, t, world, fwd_only=False, recompute=False, sp=False):
             "dtype": w.dtype, "parallelism": "replicas x%d" % world if world > 1 else "single GPU",
             "l2": "inputs larger than L2 (A, B 537 MB each; ~3.2 GB touched per step)"
             if w.name == "h8192" else "per-step working set larger than L2"}
+
+
+# ------------------------------------------------------------------ end to end
+def overlapped_e2e(dev, stream, world, steps, warmup, host_in, dev_out, copy_out, fwd, bwd):
+    """Times `steps` steps end to end: every step copies `host_in` (pinned host
+    tensors) to the device, runs fwd (and bwd, if given) on `stream`, and copies
+    the `copy_out` outputs back to pinned host memory.  The copies run on their
+    own streams, overlapped with compute: step i+1's inputs are copied in while
+    step i computes, and step i's results are copied out while step i+1
+    computes (device inputs and outputs double-buffered).  The timed region
+    opens before the first step's input copy and closes after the last step's
+    results have reached host memory.
+
+    dev_out: name -> (shape, dtype) of the device outputs; copy_out: (names
+    copied after the forward, names copied after the backward); fwd(ins, outs)
+    and bwd(ins, outs) launch one step's work.  Returns (max over ranks of the
+    ms per step, host-to-device bytes per step, device-to-host bytes per step)."""
+    hin = {k: v.pin_memory() for k, v in host_in.items()}
+    din = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in hin.items()} for _ in range(2)]
+    dout = [{k: torch.empty(shape, dtype=dt, device=dev) for k, (shape, dt) in dev_out.items()} for _ in range(2)]
+    out_fwd, out_bwd = copy_out
+    hout = [{k: torch.empty(dout[0][k].shape, dtype=dout[0][k].dtype).pin_memory() for k in out_fwd + out_bwd}
+            for _ in range(2)]
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    fwd_done = [torch.cuda.Event() for _ in range(2)]
+    step_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    pend = {"done": [False, False], "out": [False, False]}
+
+    def copy_in(b):
+        if pend["done"][b]:  # the step that last read buffer b has finished
+            s_in.wait_event(step_done[b])
+        with torch.cuda.stream(s_in):
+            for k, v in hin.items():
+                din[b][k].copy_(v, non_blocking=True)
+        in_ready[b].record(s_in)
+
+    def one_step(i, last):
+        b = i % 2
+        stream.wait_event(in_ready[b])
+        if pend["out"][b]:  # results of step i-2 have left buffer b
+            stream.wait_event(out_done[b])
+        fwd(din[b], dout[b])
+        fwd_done[b].record(stream)
+        if bwd is not None:
+            bwd(din[b], dout[b])
+        step_done[b].record(stream)
+        pend["done"][b] = True
+        if not last:
+            copy_in(b ^ 1)
+        s_out.wait_event(fwd_done[b])
+        with torch.cuda.stream(s_out):
+            for k in out_fwd:
+                hout[b][k].copy_(dout[b][k], non_blocking=True)
+        if out_bwd:
+            s_out.wait_event(step_done[b])
+            with torch.cuda.stream(s_out):
+                for k in out_bwd:
+                    hout[b][k].copy_(dout[b][k], non_blocking=True)
+        out_done[b].record(s_out)
+        pend["out"][b] = True
+
+    def run_steps(n, start_event=None, end_event=None):
+        if start_event is not None:
+            start_event.record(stream)
+            s_in.wait_event(start_event)
+        copy_in(0)
+        for i in range(n):
+            one_step(i, i == n - 1)
+        for b in range(2):
+            if pend["out"][b]:
+                stream.wait_event(out_done[b])
+        if end_event is not None:
+            end_event.record(stream)
+        torch.cuda.synchronize(dev)
+        pend["done"] = [False, False]
+        pend["out"] = [False, False]
+
+    run_steps(max(1, warmup))
+    barrier(world)
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    run_steps(steps, f0, f1)
+    barrier(world)
+    ems = max_over_ranks(f0.elapsed_time(f1) / steps, world)
+    h2d = sum(v.numel() * v.element_size() for v in hin.values())
+    d2h = sum(v.numel() * v.element_size() for v in hout[0].values())
+    return ems, h2d, d2h
 
 
 # ------------------------------------------------------------------ GPU leg
@@ -350,101 +456,34 @@ def run_ours(args, rank, world, local, w=None, quiet=False):
         roof = {"bound": "hbm", "kernel": name, "achieved": None, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": None, "traffic": None}
 
-    # ---- end to end: pinned host inputs in, results out, every step.  The copies
-    # run on their own streams, overlapped with compute: step i+1's inputs are
-    # copied in while step i computes, and step i's results are copied out while
-    # step i+1 computes (device inputs and outputs double-buffered).  The timed
-    # region opens before the first step's input copy and closes after the last
-    # step's results have reached host memory.
+    # ---- end to end: pinned host inputs in, results out, every step, on copy
+    # streams overlapped with the neighbouring steps' compute.
     e2e = None
     if not args.no_e2e:
-        hX = host["X"].pin_memory()
-        hdZ = host["dZ"].pin_memory()
-        Xd = [torch.empty_like(d["X"]) for _ in range(2)]
-        dZd = [torch.empty_like(d["dZ"]) for _ in range(2)]
-        Zd = [torch.empty((T, h), dtype=dt, device=dev) for _ in range(2)]
-        gd = [{k: torch.empty_like(v) for k, v in g.items()} for _ in range(2)]
-        oZ = [torch.empty((T, h), dtype=dt).pin_memory() for _ in range(2)]
-        odX = [torch.empty((T, h), dtype=dt).pin_memory() for _ in range(2)]
-        oda = [torch.empty((F,), dtype=dt).pin_memory() for _ in range(2)]
-        odb = [torch.empty((h,), dtype=dt).pin_memory() for _ in range(2)]
-        s_in = torch.cuda.Stream(device=dev)
-        s_out = torch.cuda.Stream(device=dev)
-        in_ready = [torch.cuda.Event() for _ in range(2)]
-        fwd_done = [torch.cuda.Event() for _ in range(2)]
-        step_done = [torch.cuda.Event() for _ in range(2)]
-        out_done = [torch.cuda.Event() for _ in range(2)]
-        pend = {"done": [False, False], "out": [False, False]}
+        host_in = {"X": host["X"]} if args.fwd_only else {"X": host["X"], "dZ": host["dZ"]}
+        dev_out = {"Z": ((T, h), dt)}
+        if not args.fwd_only:
+            dev_out.update({k: (tuple(v.shape), v.dtype) for k, v in g.items()})
 
-        def copy_in(b):
-            if pend["done"][b]:  # the step that last read buffer b has finished
-                s_in.wait_event(step_done[b])
-            with torch.cuda.stream(s_in):
-                Xd[b].copy_(hX, non_blocking=True)
-                if not args.fwd_only:
-                    dZd[b].copy_(hdZ, non_blocking=True)
-            in_ready[b].record(s_in)
-
-        def e2e_step(i, last):
-            b = i % 2
-            stream.wait_event(in_ready[b])
-            if pend["out"][b]:  # results of step i-2 have left buffer b
-                stream.wait_event(out_done[b])
+        def fwd(ins, outs):
             if args.sp:
-                tpmlp.sp_forward(ctx, Xd[b], gamma, beta, d["A"], d["a"], d["B"], d["b"], Z=Zd[b], stream=stream)
+                tpmlp.sp_forward(ctx, ins["X"], gamma, beta, d["A"], d["a"], d["B"], d["b"], Z=outs["Z"],
+                                 stream=stream)
             else:
-                tpmlp.forward(ctx, Xd[b], d["A"], d["a"], d["B"], d["b"], Z=Zd[b], stream=stream)
-            fwd_done[b].record(stream)
-            if not args.fwd_only:
-                if args.sp:
-                    tpmlp.sp_backward(ctx, dZd[b], stream=stream, dX_in=gd[b]["dX"], dgamma=sp_dg, dbeta=sp_db,
-                                      dA=gd[b]["dA"], da=gd[b]["da"], dB=gd[b]["dB"], db=gd[b]["db"])
-                else:
-                    tpmlp.backward(ctx, dZd[b], stream=stream, **gd[b])
-            step_done[b].record(stream)
-            pend["done"][b] = True
-            if not last:
-                copy_in(b ^ 1)
-            s_out.wait_event(fwd_done[b])
-            with torch.cuda.stream(s_out):
-                oZ[b].copy_(Zd[b], non_blocking=True)
-            if not args.fwd_only:
-                s_out.wait_event(step_done[b])
-                with torch.cuda.stream(s_out):
-                    odX[b].copy_(gd[b]["dX"], non_blocking=True)
-                    oda[b].copy_(gd[b]["da"], non_blocking=True)
-                    odb[b].copy_(gd[b]["db"], non_blocking=True)
-            out_done[b].record(s_out)
-            pend["out"][b] = True
+                tpmlp.forward(ctx, ins["X"], d["A"], d["a"], d["B"], d["b"], Z=outs["Z"], stream=stream)
 
-        def run_steps(n, start_event=None, end_event=None):
-            if start_event is not None:
-                start_event.record(stream)
-                s_in.wait_event(start_event)
-            copy_in(0)
-            for i in range(n):
-                e2e_step(i, i == n - 1)
-            for b in range(2):
-                if pend["out"][b]:
-                    stream.wait_event(out_done[b])
-            if end_event is not None:
-                end_event.record(stream)
-            torch.cuda.synchronize(dev)
-            pend["done"] = [False, False]
-            pend["out"] = [False, False]
+        def bwd(ins, outs):
+            if args.sp:
+                tpmlp.sp_backward(ctx, ins["dZ"], stream=stream, dX_in=outs["dX"], dgamma=sp_dg, dbeta=sp_db,
+                                  dA=outs["dA"], da=outs["da"], dB=outs["dB"], db=outs["db"])
+            else:
+                tpmlp.backward(ctx, ins["dZ"], stream=stream, **{k: outs[k] for k in g})
 
-        run_steps(max(1, args.warmup))
-        barrier(world)
-        f0 = torch.cuda.Event(enable_timing=True)
-        f1 = torch.cuda.Event(enable_timing=True)
-        run_steps(args.steps, f0, f1)
-        barrier(world)
-        ems = max_over_ranks(f0.elapsed_time(f1) / args.steps, world)
-        esz = hX.element_size()
-        h2d = hX.numel() + (0 if args.fwd_only else hdZ.numel())
-        d2h = oZ[0].numel() + (0 if args.fwd_only else odX[0].numel() + oda[0].numel() + odb[0].numel())
+        ems, h2d, d2h = overlapped_e2e(dev, stream, world, args.steps, args.warmup, host_in, dev_out,
+                                       (["Z"], [] if args.fwd_only else ["dX", "da", "db"]), fwd,
+                                       None if args.fwd_only else bwd)
         e2e = {"value": flops * world / (ems * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ems,
-               "h2d_bytes_per_step": h2d * esz, "d2h_bytes_per_step": d2h * esz,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "what": "X and dZ copied in from pinned host memory, Z, dX, da, db copied out, every "
                        "step, on copy streams overlapped with the neighbouring steps' compute; weights "
                        "and weight gradients stay resident"}
@@ -529,6 +568,26 @@ def run_attn_bench(args, rank, world, local):
     roof = {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": peak, "unit": UNIT,
             "frac": achieved / peak if achieved else None, "traffic": None, "peak_source": peak_bf16_src}
     total = sum(v[1] for v in kernels.values())
+
+    e2e = None
+    if not args.no_e2e:
+        dev_out = {"Z": ((T, h), torch.bfloat16)}
+        dev_out.update({k: (tuple(v.shape), v.dtype) for k, v in g.items()})
+
+        def fwd(ins, outs):
+            tpmlp.attn_forward(ctx, ins["X"], d["Wqkv"], d["bqkv"], d["Wo"], d["bo"], Z=outs["Z"], stream=stream)
+
+        def bwd(ins, outs):
+            tpmlp.attn_backward(ctx, ins["dZ"], stream=stream, **{k: outs[k] for k in g})
+
+        ems, h2d, d2h = overlapped_e2e(dev, stream, world, args.steps, args.warmup,
+                                       {"X": host["X"], "dZ": host["dZ"]}, dev_out,
+                                       (["Z"], ["dX", "dbqkv", "dbo"]), fwd, bwd)
+        e2e = {"value": w.flops_fwd_bwd * world / (ems * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ems,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "what": "X and dZ copied in from pinned host memory, Z, dX, dbqkv, dbo copied out, every "
+                       "step, on copy streams overlapped with the neighbouring steps' compute; weights "
+                       "and weight gradients stay resident"}
     return {"metric": "TP self-attention fwd+bwd TFLOP/s (bf16, 1×GB300)", "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -539,7 +598,8 @@ def run_attn_bench(args, rank, world, local):
                        "flops_note": "projections 24*T*h^2 + per-head products 6*T*h*(seq+1) (the causal "
                                      "lower triangle only; tiles above the diagonal are skipped)",
                        "l2": "per-step working set larger than L2"},
-            "frac_of_peak": value / world / peak, "roofline": roof, "gpu_launches": int(sum_over_ranks(launches, world)),
+            "frac_of_peak": value / world / peak, "roofline": roof, "e2e": e2e,
+            "gpu_launches": int(sum_over_ranks(launches, world)),
             "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
             "kernels": {k: {"launches": n, "ms_per_launch": t_ / n, "share": t_ / total,
                             "tflops": (gemm_flops[k] / (t_ / n * 1e-3) / 1e12) if k in gemm_flops else None}
@@ -579,6 +639,15 @@ def main():
     if args.attn:
         line = run_attn_bench(args, rank, world, local)
         if rank == 0:
+            if not args.no_cpu_baseline:
+                from tensor_transformer_mlp_tma_gb300.workloads import ATTN_WORKLOADS
+                w = ATTN_WORKLOADS[args.attn_workload]
+                secs, fl, cores = attn_oracle_sample(w, args.oracle_tokens, args.seed)
+                line["cpu_baseline"] = {"value": fl / secs / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                        "cpu": host_cpu(),
+                                        "sample": "one sequence of %d tokens with the full weights of %s "
+                                                  "(h %d, %d heads, t %d), fp64 (%.1f s)"
+                                                  % (args.oracle_tokens, w.name, w.hidden, w.heads, w.t, secs)}
             print(json.dumps(line), flush=True)
         return
     if args.sweep:
