@@ -52,8 +52,10 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int MN_BLOCK_BYTES = 64 * BK * 2;             // one 64(MN) x 64(K) TMA box
 // Epilogue staging: each epilogue warp owns two 32 x 32 bf16 boxes (2 KB each,
 // 64-byte swizzled) that it fills from registers and writes out with TMA stores.
+// The dS epilogue owns two 32 x 64 bf16 boxes (4 KB each, 128-byte swizzled):
+// one for the dS it stores, one for the P it loads.
 constexpr int STG_BOX = 32 * 32 * 2;
-constexpr int STG_PER_WARP = 2 * STG_BOX;
+constexpr int STG_BOX_WIDE = 32 * 64 * 2;
 
 // Per-CTA pipeline geometry.  CG = 1: one CTA computes a 128 x 256 tile and loads
 // all of B's 256 columns.  CG = 2: a CTA pair computes a 256 x 256 tile with
@@ -63,7 +65,7 @@ constexpr int STG_PER_WARP = 2 * STG_BOX;
 // TILE_N = 128 (CTA pairs only) is the narrow tile for outputs at most 128 wide
 // (the per-head products with N = d): each CTA loads 64 of B's columns, a stage
 // is 24 KB and eight stages fit.
-template <int CG, int TILE_N_ = BN>
+template <int CG, int TILE_N_ = BN, int EPI_ = EPI_STORE>
 struct Cfg {
     static constexpr int TILE_M = BM * CG;
     static constexpr int TILE_N = TILE_N_;
@@ -71,7 +73,11 @@ struct Cfg {
     static constexpr int A_STAGE = BM * BK * 2;
     static constexpr int B_STAGE = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-    static constexpr int STAGES = CG == 1 ? 4 : (TILE_N == BN ? 6 : 8);
+    static constexpr bool DS = EPI_ == EPI_ATTN_DS;
+    static constexpr int STG_PER_WARP = DS ? 2 * STG_BOX_WIDE : 2 * STG_BOX;
+    // dS: the K extent is one head dimension (two K blocks per tile), so fewer
+    // stages make room for its wider staging boxes
+    static constexpr int STAGES = CG == 1 ? (DS ? 3 : 4) : (TILE_N == BN ? (DS ? 5 : 6) : 8);
     static constexpr int SMEM_DYN = STAGES * STAGE_BYTES + (EPI_THREADS / 32) * STG_PER_WARP + 1024;
 };
 constexpr int MAX_STAGES = 8;
@@ -278,6 +284,30 @@ __device__ __forceinline__ void unstage_row(uint32_t box, int r, float (&v)[32])
     }
 }
 
+// Column half hf (32 of the 64 bf16 columns) of row r of a 32 x 64 bf16 box in
+// the 128-byte-swizzled layout: 16-byte chunk j of the 128-byte row sits at
+// chunk j ^ (r & 7).  stage_half_row128 fills it for a TMA store;
+// unstage_half_row128 reads what a TMA load with SWIZZLE_128B left.
+__device__ __forceinline__ void stage_half_row128(uint32_t box, int r, int hf, const uint32_t (&w)[16]) {
+    const uint32_t row = box + static_cast<uint32_t>(r) * 128u;
+    const int x = r & 7;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        ptx::st_shared_v4(row + (static_cast<uint32_t>((4 * hf + j) ^ x) << 4), w[4 * j], w[4 * j + 1],
+                          w[4 * j + 2], w[4 * j + 3]);
+}
+__device__ __forceinline__ void unstage_half_row128(uint32_t box, int r, int hf, float (&v)[32]) {
+    const uint32_t row = box + static_cast<uint32_t>(r) * 128u;
+    const int x = r & 7;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t w[4];
+        ptx::ld_shared_v4(row + (static_cast<uint32_t>((4 * hf + j) ^ x) << 4), w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) unpack_bf16(w[i], v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+    }
+}
+
 // Row r of a 32 x 32 fp32 box (4 KB, both staging boxes of a warp) staged for a
 // 128-byte-swizzled TMA store: 16-byte chunk j of the 128-byte row sits at
 // chunk j ^ (r & 7).
@@ -365,12 +395,12 @@ struct AuxLoad {
 };
 
 __device__ __forceinline__ void aux_issue(const CUtensorMap *tm, AuxLoad &a, uint32_t box, int col, int row0,
-                                          int z, int lane) {
+                                          int z, int lane, uint32_t bytes = STG_BOX) {
     __syncwarp();  // every lane has read the previous chunk out of the box
     if (lane == 0) {
-        ptx::bulk_wait_read0();  // a store staged in this box (rebuilt Y) has been read
+        ptx::bulk_wait_read0();  // a store staged in this box (rebuilt Y) or the previous one has been read
         ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive_expect_tx(a.bar, STG_BOX);
+        ptx::mbar_arrive_expect_tx(a.bar, bytes);
         ptx::tma_load_3d(box, tm, a.bar, col, row0, z);  // out-of-range parts read as zero
     }
     a.pending = true;
@@ -458,22 +488,6 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
             if (row0 < p.M && col + lane < p.N)
                 p.colsum_part[static_cast<int64_t>(row0 >> 5) * p.N + col + lane] = cs;
         }
-    } else if constexpr (EPI == EPI_ATTN_DS) {
-        // dS = P * (dP - D) * scale: P read through the second staging box (TMA,
-        // one chunk ahead), D one fp32 per row.
-        float pv[32];
-        bool got = ptx::mbar_wait(aux->bar, aux->phase, p.wait_ns, abort_flag);
-        aux->phase ^= 1u;
-        aux->pending = false;
-        if (!__all_sync(0xffffffffu, got)) {
-            if (lane == 0) record_timeout(p, abort_flag, 6);
-        }
-        unstage_row(stg + STG_BOX, lane, pv);
-        if (next_col >= 0) aux_issue(tm1, *aux, stg + STG_BOX, next_col, next_row0, z, lane);
-        const float D = row < p.M ? p.rowvec[static_cast<int64_t>(z) * p.M + row] : 0.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = pv[i] * (v[i] - D) * p.scale;
-        pack32(v, w0);
     } else if constexpr (EPI == EPI_FOLD_BIAS) {
         float bias[32];
         load32(p.bias, col, col, p.N, true, bias);
@@ -509,12 +523,27 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
     }
 }
 
+// dS = P * (dP - D) * scale for column half hf of a 64-column pair of chunks:
+// P comes from the warp's P box (128-byte rows, loaded by TMA), D is one fp32
+// per row, and the result is staged in the same half of the store box.
+__device__ __forceinline__ void ds_half(const Params &p, float (&v)[32], int64_t row, int z, int lane,
+                                        uint32_t sbox, uint32_t pbox, int hf) {
+    float pv[32];
+    unstage_half_row128(pbox, lane, hf, pv);
+    const float D = row < p.M ? p.rowvec[static_cast<int64_t>(z) * p.M + row] : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = pv[i] * (v[i] - D) * p.scale;
+    uint32_t w[16];
+    pack32(v, w);
+    stage_half_row128(sbox, lane, hf, w);
+}
+
 template <int EPI, bool A_MN, bool B_MN, int CG, bool HEADS, int TILE_N>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
                 const __grid_constant__ CUtensorMap tmO2, const Params p) {
-    using C = Cfg<CG, TILE_N>;
+    using C = Cfg<CG, TILE_N, EPI>;
     constexpr bool PAIR = CG == 2;
     constexpr bool FOLD = (EPI == EPI_FOLD_BIAS || EPI == EPI_FOLD);
     constexpr uint32_t IDESC = ptx::idesc_bf16_f32(C::TILE_M, TILE_N, A_MN, B_MN);
@@ -838,7 +867,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int quarter = warp & 3;                    // TMEM lanes this warp may read
         const int half = ew >> 2;                        // column half of the tile
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t stg = smem_base + STAGES * C::STAGE_BYTES + ew * STG_PER_WARP;
+        const uint32_t stg = smem_base + STAGES * C::STAGE_BYTES + ew * C::STG_PER_WARP;
         uint32_t unit = 0;
         bool ok = true;
         float sum[FOLD ? TILE_N / 2 : 1];
@@ -869,8 +898,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int row0 = mb * C::TILE_M + BM * static_cast<int>(rank) + quarter * 32;
             const int64_t row = static_cast<int64_t>(row0) + lane;
             const int col0 = nb * TILE_N + half * (TILE_N / 2);
-            if constexpr (EPI == EPI_DGELU || EPI == EPI_ATTN_DS)
-                aux_issue(&tmO1, aux, stg + STG_BOX, col0, row0, zb, lane);
+            if constexpr (EPI == EPI_DGELU) aux_issue(&tmO1, aux, stg + STG_BOX, col0, row0, zb, lane);
+            if constexpr (EPI == EPI_ATTN_DS) aux_issue(&tmO1, aux, stg + STG_BOX_WIDE, col0, row0, zb, lane, STG_BOX_WIDE);
             for (int s = 0; s < p.nshards; ++s, ++unit) {
                 const uint32_t buf = unit & 1u, use = unit >> 1;
                 bool got = ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_tfull[buf]), use & 1u, p.wait_ns,
@@ -922,6 +951,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                         continue;
                     }
+                    if constexpr (EPI == EPI_ATTN_DS) {
+                        // Chunks in pairs: one P load and one dS store per 64 columns.
+                        const uint32_t sbox = stg, pbox = stg + STG_BOX_WIDE;
+#pragma unroll
+                        for (int q = 0; q < CHUNKS / 2; ++q) {
+                            const int colq = col0 + 64 * q;
+                            const bool landed = ptx::mbar_wait(aux.bar, aux.phase, p.wait_ns, &abort_sh);
+                            aux.phase ^= 1u;
+                            aux.pending = false;
+                            if (!__all_sync(0xffffffffu, landed) && lane == 0) record_timeout(p, &abort_sh, 6);
+#pragma unroll
+                            for (int hf = 0; hf < 2; ++hf) {
+                                const int c = 2 * q + hf;
+                                uint32_t r[32];
+                                ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+                                ptx::tmem_ld_wait(r);
+                                if (c == CHUNKS - 1) release(buf);
+                                float v[32];
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                                if (hf == 0) {
+                                    // the previous pair's store has left the store box
+                                    if (lane == 0) ptx::bulk_wait_read0();
+                                    __syncwarp();
+                                }
+                                ds_half(p, v, row, zb, lane, sbox, pbox, hf);
+                            }
+                            ptx::fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0 && row0 < p.M && colq < p.N) {
+                                ptx::tma_store_3d(&tmO0, sbox, colq, row0, zb);
+                                ptx::bulk_commit();
+                            }
+                            // the P box is free: the next pair's P, once this store has left its box
+                            if (q + 1 < CHUNKS / 2)
+                                aux_issue(&tmO1, aux, pbox, colq + 64, row0, zb, lane, STG_BOX_WIDE);
+                        }
+                    } else {
 #pragma unroll
                     for (int c = 0; c < CHUNKS; ++c) {
                         uint32_t r[32];
@@ -935,11 +1002,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         finish_chunk<EPI, HEADS>(p, &tmO0, &tmO1, &tmO2, v, row, row0, col0 + c * 32, zb, lane, stg, &aux,
                                           c < CHUNKS - 1 ? col0 + (c + 1) * 32 : -1, row0, &abort_sh);
                     }
+                    }
                 }
             }
         }
         if (!ok) record_timeout(p, &abort_sh, 5);
-        // an H load still in flight (only after an abort) must land before the CTA exits
+        // an H or P load still in flight (only after an abort) must land before the CTA exits
         if (aux.pending && !ptx::mbar_wait(aux.bar, aux.phase, p.wait_ns, nullptr) && lane == 0)
             record_timeout(p, &abort_sh, 7);
         // every TMA store of this warp must be complete before the CTA exits
@@ -1072,7 +1140,7 @@ static bool make_map_view(CUtensorMap *m, const void *ptr, const HeadView &v, ui
 
 template <int EPI, bool A_MN, bool B_MN, int CG, bool HEADS = false, int TILE_N = BN>
 static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
-    using C = Cfg<CG, TILE_N>;
+    using C = Cfg<CG, TILE_N, EPI>;
     auto kern = gemm_kernel<EPI, A_MN, B_MN, CG, HEADS, TILE_N>;
     // Per-device, once: the shared-memory opt-in, and for CTA pairs the number of
     // 2-CTA clusters that can be resident at once (the persistent grid size).
@@ -1161,19 +1229,27 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     CUtensorMap mo0, mo1, mo2;
     const void *o0 = g.out0 ? g.out0 : g.out1;
     // The attention scores are fp32 (32 x 32 box, 128-byte swizzle, see stage_row_f32);
-    // dS reads P through the second map.
+    // dS reads P through the second map; both of its maps have 32 x 64 boxes with
+    // 128-byte swizzle (see stage_half_row128).
     const void *o1 = (EPI == EPI_BIAS_GELU) ? g.out1 : ((EPI == EPI_DGELU || EPI == EPI_ATTN_DS) ? g.aux : o0);
     const void *o2 = (EPI == EPI_DGELU && g.out1) ? g.out1 : o0;
     const bool f32out = EPI == EPI_ATTN_SCORE;
-    const CUtensorMapSwizzle so = f32out ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const bool wide = EPI == EPI_ATTN_DS;
+    const uint32_t obox = wide ? 64 : 32;
+    const CUtensorMapSwizzle so = (f32out || wide) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (wide && (o_rank > 3 || g.nshards != 1)) {
+        set_last_error("dS epilogue: a plain [problems][M][N] output and one shard only");
+        return cudaErrorInvalidValue;
+    }
     // The bias-gradient tile takes its A from a 64 x 64 block of ones (third map).
     const bool bias_tile = EPI == EPI_STORE && A_MN && B_MN && g.bias_grad != nullptr;
     if (bias_tile && (g.ones == nullptr || nb != 1 || g.nshards != 1 || g.causal_k != 0 || g.skip_upper)) {
         set_last_error("bias-gradient tile: needs the ones block, one problem, one shard, no causal ranges");
         return cudaErrorInvalidValue;
     }
-    if (!(o_rank > 3 ? make_map_view(&mo0, o0, g.o_view, 32, 32, so) : make_map(&mo0, o0, g.M, g.N, 32, 32, so, nb, f32out)) ||
-        !make_map(&mo1, o1, g.M, g.N, 32, 32, so, nb, f32out) ||
+    if (!(o_rank > 3 ? make_map_view(&mo0, o0, g.o_view, 32, 32, so)
+                     : make_map(&mo0, o0, g.M, g.N, obox, 32, so, nb, f32out)) ||
+        !make_map(&mo1, o1, g.M, g.N, obox, 32, so, nb, f32out) ||
         !(bias_tile ? make_map(&mo2, g.ones, 64, 64, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B, 1)
                     : make_map(&mo2, o2, g.M, g.N, 32, 32, so, nb, f32out)))
         return cudaErrorInvalidValue;
