@@ -42,12 +42,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, with the hash of the kernel source they were taken at.  A kernel whose
 # source has changed since reports traffic null.
 NCU_TRAFFIC = {  # profiles/dram_traffic_h8192_gemms.md (h8192 workload)
-    "fc1_bias_gelu": (1.988987e9 + 0.519648e9, "57a2ba7513ad"),
-    "fc2_shard_fold": (2.295506e9 + 0.092963e9, "57a2ba7513ad"),
-    "bwd_dY_dgelu": (2.646548e9 + 0.274623e9, "57a2ba7513ad"),
-    "bwd_dB": (1.007968e9 + 0.517005e9, "57a2ba7513ad"),
-    "bwd_dA": (0.979500e9 + 0.516222e9, "57a2ba7513ad"),
-    "bwd_dX_shard_fold": (2.528508e9 + 0.090992e9, "57a2ba7513ad"),
+    "fc1_bias_gelu": (1.943519e9 + 0.519111e9, "32d5816d0a52"),
+    "fc2_shard_fold": (2.203810e9 + 0.081232e9, "32d5816d0a52"),
+    "bwd_dY_dgelu": (2.517340e9 + 0.274451e9, "32d5816d0a52"),
+    "bwd_dB": (0.998947e9 + 0.515716e9, "32d5816d0a52"),
+    "bwd_dA": (0.982707e9 + 0.515046e9, "32d5816d0a52"),
+    "bwd_dX_shard_fold": (2.210045e9 + 0.076435e9, "32d5816d0a52"),
 }
 
 
