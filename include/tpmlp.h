@@ -239,8 +239,17 @@ typedef struct {
     int32_t heads;  /* h % heads == 0, heads % t == 0, d = h/heads a multiple of 64 */
     int32_t t;      /* shards, 1..16 */
     int32_t dtype;  /* TPMLP_BF16 */
-    int32_t flags;  /* 0 */
+    int32_t flags;  /* tpmlp_attn_flags, 0 for the plain pass */
 } tpmlp_attn_shape;
+
+/* TPMLP_ATTN_P_UPPER_ZERO: the caller's P buffer already holds zeros in every
+ * 256 x 256 tile that lies wholly above the diagonal (each key of the tile past
+ * each query), so the forward does not write those tiles: row s of a head
+ * writes columns [0, min(seq, (s/256 + 1)*256)).  No kernel reads them.  A
+ * caller that keeps one P buffer across steps and zeroes it once can set it; the
+ * values of P are then the same as without it.  Without the flag every row of P
+ * is written in full. */
+typedef enum { TPMLP_ATTN_P_UPPER_ZERO = 1 } tpmlp_attn_flags;
 
 /* What the forward pass keeps for the backward pass (caller-owned except the
  * weights, which tpmlp_attn_forward records): QKV [T,3h], P [batch*heads, seq,

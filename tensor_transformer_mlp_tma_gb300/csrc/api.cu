@@ -693,7 +693,7 @@ bool attn_shape_valid(const tpmlp_attn_shape *s) {
     if (!s) return false;
     if (s->batch < 0 || s->seq <= 0 || s->hidden <= 0 || s->heads <= 0) return false;
     if (s->t < 1 || s->t > 16 || s->heads % s->t != 0 || s->hidden % s->heads != 0) return false;
-    if (s->flags != 0) return false;
+    if ((s->flags & ~TPMLP_ATTN_P_UPPER_ZERO) != 0) return false;
     // int32 tile and grid arithmetic inside the kernels
     if (s->hidden > (1LL << 28) || s->seq > (1LL << 20) || s->batch * s->seq > (1LL << 30)) return false;
     if (static_cast<int64_t>(s->batch) * s->heads > (1LL << 24)) return false;
@@ -906,7 +906,11 @@ tpmlp_status tpmlp_attn_forward(const tpmlp_attn_shape *s, const void *X, const 
 
     {
         Timed timed("attn_softmax", st);
-        e = tpmlp::launch_softmax(scores, saved->P, nz * S, S, true, st);
+        // With TPMLP_ATTN_P_UPPER_ZERO the 256 x 256 tiles of P wholly above the
+        // diagonal (never read: P V and dS K stop at the tile's keys, P^T dO starts
+        // at its queries, dS skips them) already hold zeros and are not written.
+        const int64_t wtile = (s->flags & TPMLP_ATTN_P_UPPER_ZERO) ? 256 : 0;
+        e = tpmlp::launch_softmax(scores, saved->P, nz * S, S, true, wtile, st);
         if (e != cudaSuccess) return from_cuda(e);
         g_launches.fetch_add(1);
     }

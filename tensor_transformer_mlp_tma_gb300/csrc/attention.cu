@@ -25,18 +25,27 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
+// Columns of P that row r of a head (r = row % S) writes: all S, or with
+// wtile > 0 only up to the end of the row's wtile-wide tile (the tiles wholly
+// above the diagonal, which no later kernel reads, are left as they are).
+__device__ __forceinline__ int64_t write_end(int64_t row, int64_t S, int64_t wtile) {
+    return wtile > 0 ? min(S, (row % S / wtile + 1) * wtile) : S;
+}
+
 // One warp per score row.  Row r of a head (r = row % S) sees columns 0..r; the
-// others are written as exact zeros.  Max-subtracted exponentials, fp32 sum.
-// The row is read once, 16 bytes per lane at a time, into V float4 registers per
-// lane (S <= 128 V); only the columns up to the diagonal are read.
+// others are written as exact zeros (up to write_end).  Max-subtracted
+// exponentials (the fast __expf), fp32 sum.  The row is read once, 16 bytes per lane at a time,
+// into V float4 registers per lane (S <= 128 V); only the columns up to the
+// diagonal are read.
 template <int V>
 __global__ void __launch_bounds__(256)
     softmax_reg_kernel(const float *__restrict__ S_, __nv_bfloat16 *__restrict__ P, int64_t rows, int64_t S,
-                       bool causal) {
+                       bool causal, int64_t wtile) {
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     if (row >= rows) return;
     const int64_t last = causal ? row % S : S - 1;
+    const int64_t wend = write_end(row, S, wtile);
     const float4 *in = reinterpret_cast<const float4 *>(S_ + row * S);
     float4 x[V];
     float mx = -INFINITY;
@@ -57,10 +66,12 @@ __global__ void __launch_bounds__(256)
     float sum = 0.0f;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-        x[v].x = expf(x[v].x - mx);  // exp(-inf) = 0 for the masked columns
-        x[v].y = expf(x[v].y - mx);
-        x[v].z = expf(x[v].z - mx);
-        x[v].w = expf(x[v].w - mx);
+        // the fast exponential (its error is far below P's bf16 rounding);
+        // exp(-inf) = 0 for the masked columns
+        x[v].x = __expf(x[v].x - mx);
+        x[v].y = __expf(x[v].y - mx);
+        x[v].z = __expf(x[v].z - mx);
+        x[v].w = __expf(x[v].w - mx);
         sum += (x[v].x + x[v].y) + (x[v].z + x[v].w);
     }
     sum = warp_sum(sum);
@@ -69,7 +80,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int64_t c = 4 * (lane + 32 * v);
-        if (c < S) {
+        if (c < wend) {  // wend is a multiple of 4
             __nv_bfloat162 lo = __floats2bfloat162_rn(x[v].x * inv, x[v].y * inv);
             __nv_bfloat162 hi = __floats2bfloat162_rn(x[v].z * inv, x[v].w * inv);
             uint2 w;
@@ -84,7 +95,7 @@ __global__ void __launch_bounds__(256)
 // passes over the row (max, sum, write).
 __global__ void __launch_bounds__(256)
     softmax_kernel(const float *__restrict__ S_, __nv_bfloat16 *__restrict__ P, int64_t rows, int64_t S,
-                   bool causal) {
+                   bool causal, int64_t wtile) {
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     if (row >= rows) return;
@@ -95,11 +106,12 @@ __global__ void __launch_bounds__(256)
     for (int64_t c = lane; c <= last; c += 32) mx = fmaxf(mx, in[c]);
     mx = warp_max(mx);
     float sum = 0.0f;
-    for (int64_t c = lane; c <= last; c += 32) sum += expf(in[c] - mx);
+    for (int64_t c = lane; c <= last; c += 32) sum += __expf(in[c] - mx);
     sum = warp_sum(sum);
     const float inv = 1.0f / sum;
-    for (int64_t c = lane; c < S; c += 32)
-        out[c] = __float2bfloat16_rn(c <= last ? expf(in[c] - mx) * inv : 0.0f);
+    const int64_t wend = write_end(row, S, wtile);
+    for (int64_t c = lane; c < wend; c += 32)
+        out[c] = __float2bfloat16_rn(c <= last ? __expf(in[c] - mx) * inv : 0.0f);
 }
 
 // D[z*S + s] = sum_e dO[r, g*d + e] * O[r, g*d + e] over the token-major [T, h]
@@ -173,21 +185,22 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace attn
 
-cudaError_t launch_softmax(const float *S, void *P, int64_t rows, int64_t cols, bool causal, cudaStream_t st) {
+cudaError_t launch_softmax(const float *S, void *P, int64_t rows, int64_t cols, bool causal, int64_t wtile,
+                           cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
     const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(P);
     // 16-byte row starts (cols a multiple of 4) for the vector loads
     if (cols % 4 != 0 || cols > 128 * 32)
-        attn::softmax_kernel<<<grid, 256, 0, st>>>(S, out, rows, cols, causal);
+        attn::softmax_kernel<<<grid, 256, 0, st>>>(S, out, rows, cols, causal, wtile);
     else if (cols <= 128 * 4)
-        attn::softmax_reg_kernel<4><<<grid, 256, 0, st>>>(S, out, rows, cols, causal);
+        attn::softmax_reg_kernel<4><<<grid, 256, 0, st>>>(S, out, rows, cols, causal, wtile);
     else if (cols <= 128 * 8)
-        attn::softmax_reg_kernel<8><<<grid, 256, 0, st>>>(S, out, rows, cols, causal);
+        attn::softmax_reg_kernel<8><<<grid, 256, 0, st>>>(S, out, rows, cols, causal, wtile);
     else if (cols <= 128 * 16)
-        attn::softmax_reg_kernel<16><<<grid, 256, 0, st>>>(S, out, rows, cols, causal);
+        attn::softmax_reg_kernel<16><<<grid, 256, 0, st>>>(S, out, rows, cols, causal, wtile);
     else
-        attn::softmax_reg_kernel<32><<<grid, 256, 0, st>>>(S, out, rows, cols, causal);
+        attn::softmax_reg_kernel<32><<<grid, 256, 0, st>>>(S, out, rows, cols, causal, wtile);
     return cudaGetLastError();
 }
 

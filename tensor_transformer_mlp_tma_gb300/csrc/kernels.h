@@ -122,7 +122,9 @@ cudaError_t launch_ln_backward(bool is_bf16, const LnArgs &a, cudaStream_t st, i
 struct HeadLayout {
     int64_t nb, S, h, heads, d;
 };
-cudaError_t launch_softmax(const float *S, void *P, int64_t rows, int64_t cols, bool causal, cudaStream_t st);
+// wtile > 0: each row writes P only up to the end of its wtile-wide column tile.
+cudaError_t launch_softmax(const float *S, void *P, int64_t rows, int64_t cols, bool causal, int64_t wtile,
+                           cudaStream_t st);
 // D[z*S + s] = row dot of dO and O over head g's columns of token b*S + s (token-major inputs).
 cudaError_t launch_rowdot(const HeadLayout &L, const void *dO, const void *O, float *D, cudaStream_t st);
 

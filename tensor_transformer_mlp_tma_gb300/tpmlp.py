@@ -20,6 +20,7 @@ F32, BF16 = 0, 1
 ALGO_DEFAULT, ALGO_SIMT = 0, 1
 WS_STATUS, WS_PARTIALS, WS_DY, WS_Y, WS_DXN = 0, 1, 2, 3, 4
 FLAG_RECOMPUTE, FLAG_LAYERNORM = 1, 2
+ATTN_P_UPPER_ZERO = 1
 
 _DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -322,10 +323,16 @@ def ln_backward(ctx: Context, dXn, stream=None):
 class AttnContext:
     """Buffers of one tensor-parallel self-attention layer between forward and
     backward: the saved QKV [T,3h], P [batch*heads, seq, seq], O [T,h] and the
-    workspace (bf16 only)."""
+    workspace (bf16 only).
 
-    def __init__(self, batch, seq, hidden, heads, t, device=None):
-        self.shape = AttnShape(int(batch), int(seq), int(hidden), int(heads), int(t), BF16, 0)
+    p_upper_zero=True (the default) allocates P zeroed and sets
+    ATTN_P_UPPER_ZERO: the tiles of P wholly above the diagonal keep those
+    zeros and the forward does not rewrite them.  False: P is allocated
+    uninitialised and every row is written in full."""
+
+    def __init__(self, batch, seq, hidden, heads, t, device=None, p_upper_zero=True):
+        flags = ATTN_P_UPPER_ZERO if p_upper_zero else 0
+        self.shape = AttnShape(int(batch), int(seq), int(hidden), int(heads), int(t), BF16, flags)
         n = int(lib.tpmlp_attn_workspace_bytes(ctypes.byref(self.shape)))
         if n == 0:
             raise ValueError("invalid attention shape (batch=%d seq=%d hidden=%d heads=%d t=%d)"
@@ -334,7 +341,8 @@ class AttnContext:
         T, h = batch * seq, hidden
         self.dtype = torch.bfloat16
         self.QKV = torch.empty((T, 3 * h), dtype=self.dtype, device=dev)
-        self.P = torch.empty((batch * heads, seq, seq), dtype=self.dtype, device=dev)
+        alloc = torch.zeros if p_upper_zero else torch.empty
+        self.P = alloc((batch * heads, seq, seq), dtype=self.dtype, device=dev)
         self.O = torch.empty((T, h), dtype=self.dtype, device=dev)
         self.workspace = torch.zeros(n, dtype=torch.uint8, device=dev)
         self.saved = AttnSaved(None, None, None, _ptr(self.QKV), _ptr(self.P), _ptr(self.O))

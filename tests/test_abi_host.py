@@ -201,11 +201,17 @@ def test_attention_size_queries(tp):
                 tp.AttnShape(1, 64, 256, 2, 0, tp.BF16, 0),    # t < 1
                 tp.AttnShape(1, 0, 256, 2, 1, tp.BF16, 0),     # seq = 0
                 tp.AttnShape(-1, 64, 256, 2, 1, tp.BF16, 0),   # batch < 0
-                tp.AttnShape(1, 64, 256, 2, 1, tp.BF16, 1),    # flags
+                tp.AttnShape(1, 64, 256, 2, 1, tp.BF16, 2),    # unknown flag
+                tp.AttnShape(1, 64, 256, 2, 1, tp.BF16, -1),   # unknown flags
                 tp.AttnShape(1 << 10, 1 << 20, 1024, 8, 1, tp.BF16, 0)):  # scores past 2^48 elements
         assert tp.lib.tpmlp_attn_saved_bytes(ctypes.byref(bad)) == 0
         assert tp.lib.tpmlp_attn_workspace_bytes(ctypes.byref(bad)) == 0
     assert tp.lib.tpmlp_attn_workspace_bytes(ctypes.byref(tp.AttnShape(0, 64, 256, 2, 2, tp.BF16, 0))) > 0
+    # TPMLP_ATTN_P_UPPER_ZERO changes which tiles of P are written, not any size
+    up = tp.AttnShape(1, 64, 256, 2, 1, tp.BF16, tp.ATTN_P_UPPER_ZERO)
+    plain = tp.AttnShape(1, 64, 256, 2, 1, tp.BF16, 0)
+    assert tp.lib.tpmlp_attn_saved_bytes(ctypes.byref(up)) == tp.lib.tpmlp_attn_saved_bytes(ctypes.byref(plain)) > 0
+    assert tp.lib.tpmlp_attn_workspace_bytes(ctypes.byref(up)) == tp.lib.tpmlp_attn_workspace_bytes(ctypes.byref(plain)) > 0
 
 
 def test_attention_invalid_and_unsupported_arguments(tp):

@@ -239,3 +239,34 @@ def test_wide_tiles_match_oracle(tp, monkeypatch):
     errs = {k: rel(to_np(out[k]), ref[k]) for k in TOL}
     bad = {k: v for k, v in errs.items() if not (v <= TOL[k])}
     assert not bad, "outside tolerance: %s (all: %s)" % (bad, errs)
+
+
+@pytest.mark.parametrize("pair", ["1", "0"])
+def test_p_upper_tiles_flag(tp, pair, monkeypatch):
+    """TPMLP_ATTN_P_UPPER_ZERO leaves the 256 x 256 tiles of P wholly above the
+    diagonal as they were and writes everything else as without the flag; no
+    later kernel reads those tiles (CTA-pair 256-row or single-CTA 128-row
+    tiles), so every output is bit-identical.  Without the flag every row of P
+    is written in full (sentinel values overwritten)."""
+    from tensor_transformer_mlp_tma_gb300 import inputs
+    monkeypatch.setenv("TPMLP_CTA_PAIR", pair)
+    nb, S, h, heads, t = 2, 520, 512, 4, 2   # 3 tile rows of 256, ragged last
+    inp = inputs.make_attn(nb * S, h, 31, STD)
+    d = {k: v.cuda() for k, v in inp.items()}
+    res = {}
+    for flag in (False, True):
+        ctx = tp.AttnContext(nb, S, h, heads, t, p_upper_zero=flag)
+        ctx.P.fill_(7.0)  # a sentinel in every entry
+        Z = tp.attn_forward(ctx, d["X"], d["Wqkv"], d["bqkv"], d["Wo"], d["bo"])
+        g = tp.attn_backward(ctx, d["dZ"])
+        torch.cuda.synchronize()
+        assert tp.check_device_status(ctx) == tp.OK
+        res[flag] = dict(g, Z=Z, P=ctx.P.clone(), O=ctx.O.clone(), QKV=ctx.QKV.clone())
+    s = torch.arange(S, device="cuda")
+    upper = (s[None, :] // 256) > (s[:, None] // 256)  # [S, S]: tile column past the tile row
+    P0, P1 = res[False]["P"], res[True]["P"]
+    assert torch.count_nonzero(P0[:, upper]) == 0                   # written as zeros
+    assert bool((P1[:, upper] == 7.0).all())                        # left as they were
+    assert torch.equal(P0[:, ~upper], P1[:, ~upper])
+    for k in ("Z", "O", "QKV", "dX", "dWqkv", "dbqkv", "dWo", "dbo"):
+        assert torch.equal(res[False][k], res[True][k]), k
