@@ -253,7 +253,8 @@ typedef enum { TPMLP_ATTN_P_UPPER_ZERO = 1 } tpmlp_attn_flags;
 
 /* What the forward pass keeps for the backward pass (caller-owned except the
  * weights, which tpmlp_attn_forward records): QKV [T,3h], P [batch*heads, seq,
- * seq] (bf16 probabilities of every head), O [T,h]. */
+ * seq] (bf16 probabilities of every head; with TPMLP_ATTN_P_UPPER_ZERO the tiles
+ * wholly above the diagonal are left as the caller holds them), O [T,h]. */
 typedef struct {
     const void *X;
     const void *Wqkv;
