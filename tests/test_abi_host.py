@@ -32,6 +32,17 @@ def test_header_declares_the_entry_points():
         assert n in names
 
 
+def test_binding_constants_match_the_header(tp):
+    """Every enumerator the header declares has the same value in the binding
+    (TPMLP_X in C is X in Python), so the two cannot drift apart."""
+    src = open(os.path.join(ROOT, "include", "tpmlp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    enums = dict((k, int(v)) for k, v in re.findall(r"\bTPMLP_([A-Z0-9_]+)\s*=\s*(-?\d+)", src))
+    assert len(enums) >= 18, enums  # status, dtype, algo, flags, workspace regions, attention flags
+    for name, value in enums.items():
+        assert getattr(tp, name) == value, name
+
+
 def test_every_declared_symbol_is_exported(tp):
     lib = ctypes.CDLL(tp.LIB_PATH)
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
