@@ -85,6 +85,26 @@ def test_layernorm_alone_matches_oracle(T, h, dt):
         assert rel(to_np(bw[k]), ref) <= tol_g, k
 
 
+@pytest.mark.parametrize("algo", ["tc", "simt"])
+def test_sp_block_with_recompute(algo):
+    """Recomputation (only H kept) with the LayerNorm in front: against the
+    oracle, and bit-identical to the plain sequence-parallel block in every
+    output but dB, which uses Y rebuilt from the stored bf16 H."""
+    from tensor_transformer_mlp_tma_gb300 import tpmlp
+    a = tpmlp.ALGO_SIMT if algo == "simt" else None
+    inp = inputs.make(300, 384, 1280, "bf16", seed=41, std=STD)
+    gamma, beta = _ln_params(384, 13)
+    rec, ctx = run_sp(inp, gamma, beta, 2, algo=a, recompute=True)
+    assert tpmlp.saved_bytes(ctx.shape) == 300 * 1280 * 2
+    ref = oracle.sp_forward_backward(inp["X"], gamma, beta, EPS, inp["A"], inp["a"], inp["B"], inp["b"],
+                                     inp["dZ"], 2)
+    compare_full(rec, ref, TOL)
+    plain, _ = run_sp(inp, gamma, beta, 2, algo=a)
+    for k in ("Xn", "Z", "H", "dY", "dX", "dX_in", "dgamma", "dbeta", "dA", "da", "db"):
+        assert torch.equal(rec[k].view(torch.int16), plain[k].view(torch.int16)), k
+    compare_full({"dB": rec["dB"]}, {"dB": to_np(plain["dB"])}, {"dB": 2e-2})
+
+
 def test_sp_block_repeatable():
     inp = inputs.make(300, 384, 1280, "bf16", seed=5, std=STD)
     gamma, beta = _ln_params(384, 3)
