@@ -512,11 +512,33 @@ def check_attn_fd(lib, eps_fd=1e-6, tol=1e-6):
     return f
 
 
+def check_golden_attention_worked_example(lib):
+    """The hand-worked attention example of tests/golden/attention_worked_example.txt
+    (one sequence of two tokens, one head of d = 4, equal keys so that the second
+    row's probabilities are exactly 1/2): forward and every gradient.  Equal
+    logits make the softmax blind to the 1/sqrt(d) scale of the scores; the
+    numpy and finite-difference pins cover that."""
+    g = read_golden("attention_worked_example.txt")
+    nb, heads, t = g["nb"], g["heads"], g["t"]
+    fw = oracle.attn_forward(g["X"], g["Wqkv"], g["bqkv"].ravel(), g["Wo"], g["bo"].ravel(), nb, heads, t, lib=lib)
+    bw = oracle.attn_backward(g["X"], g["Wqkv"], g["Wo"], fw["QKV"], fw["P"], fw["O"], g["dZ"], nb, heads, t,
+                              lib=lib)
+    got = {"QKV": fw["QKV"], "P": fw["P"].reshape(g["P"].shape), "O": fw["O"], "Z": fw["Z"],
+           "dbo": bw["dbo"][None, :], "dWo": bw["dWo"], "dWqkv": bw["dWqkv"], "dbqkv": bw["dbqkv"][None, :],
+           "dX": bw["dX"]}
+    f = []
+    for k, v in got.items():
+        err = float(np.max(np.abs(v - g[k])))
+        if err > 1e-12 * max(1.0, float(np.max(np.abs(g[k])))):
+            f.append("golden attention example: %s differs by %.3e" % (k, err))
+    return f
+
+
 ALL = [check_gelu_vs_erf, check_gelu_identities, check_gelu_prime_fd, check_forward_numpy,
        check_worked_example_t2, check_golden_worked_example_t2, check_backward_fd, check_backward_partials,
        check_closed_forms, check_slice_vs_full, check_layernorm_numpy, check_layernorm_invariants,
        check_layernorm_backward_fd, check_sp_composition_fd, check_attn_numpy, check_attn_sharding,
-       check_attn_causal, check_attn_fd]
+       check_attn_causal, check_attn_fd, check_golden_attention_worked_example]
 
 
 def run_all(lib) -> list:
