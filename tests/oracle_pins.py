@@ -512,6 +512,32 @@ def check_attn_fd(lib, eps_fd=1e-6, tol=1e-6):
     return f
 
 
+def check_layernorm_worked_example(lib):
+    """LayerNorm worked by hand (the sequence-parallel block's first step), eps = 0:
+      x = [1, 3, 1, 3]: mean 2, population variance 1, rstd 1, xhat = [-1, 1, -1, 1]
+      x = [0, 0, 4, 4]: mean 2, variance 4, rstd 1/2, xhat = [-1, -1, 1, 1]
+    With gamma = [1, 2, 1/2, -1], beta = [0, 1, -1, 1/2]: y = gamma xhat + beta.
+    Backward for dY = [[1, 0, 2, -1], [0, 1, 1, 2]]: g = dY gamma,
+      dx = rstd (g - mean(g) - xhat mean(g xhat)),  dgamma = sum dY xhat,
+      dbeta = sum dY."""
+    X = np.array([[1.0, 3, 1, 3], [0, 0, 4, 4]])
+    gamma = np.array([1.0, 2, 0.5, -1])
+    beta = np.array([0.0, 1, -1, 0.5])
+    dY = np.array([[1.0, 0, 2, -1], [0, 1, 1, 2]])
+    want = {"Y": [[-1, 3, -1.5, -0.5], [-1, -1, -0.5, -0.5]], "mean": [2, 2], "rstd": [1, 0.5],
+            "dX": [[0, -0.5, 0, 0.5], [-0.5, 0.5, 0.625, -0.625]], "dgamma": [-1, -1, -1, 1],
+            "dbeta": [1, 1, 3, 1]}
+    fw = oracle.layernorm_forward(X, gamma, beta, 0.0, lib=lib)
+    bw = oracle.layernorm_backward(dY, X, gamma, 0.0, lib=lib)
+    got = dict(fw, **bw)
+    f = []
+    for k, v in want.items():
+        err = float(np.max(np.abs(np.asarray(got[k]) - np.asarray(v))))
+        if err > 1e-14:
+            f.append("LayerNorm worked example: %s differs by %.3e" % (k, err))
+    return f
+
+
 def check_golden_attention_worked_example(lib):
     """The hand-worked attention example of tests/golden/attention_worked_example.txt
     (one sequence of two tokens, one head of d = 4, equal keys so that the second
@@ -538,7 +564,7 @@ ALL = [check_gelu_vs_erf, check_gelu_identities, check_gelu_prime_fd, check_forw
        check_worked_example_t2, check_golden_worked_example_t2, check_backward_fd, check_backward_partials,
        check_closed_forms, check_slice_vs_full, check_layernorm_numpy, check_layernorm_invariants,
        check_layernorm_backward_fd, check_sp_composition_fd, check_attn_numpy, check_attn_sharding,
-       check_attn_causal, check_attn_fd, check_golden_attention_worked_example]
+       check_attn_causal, check_attn_fd, check_golden_attention_worked_example, check_layernorm_worked_example]
 
 
 def run_all(lib) -> list:
