@@ -56,6 +56,18 @@ MUTANTS = {
                      "const double ds = Pg[r * S + c] * dP[c] * scale;"),
     # dK built from K instead of Q
     "attn_dk_operand": ("dk[e] += ds * qr[e];", "dk[e] += ds * kr[e];"),
+    # dV from the transposed probability (P[c][r] instead of P[r][c])
+    "attn_dv_transposed_p": ("dv[e] += Pg[r * S + c] * dor[e];", "dv[e] += Pg[c * S + r] * dor[e];"),
+    # dQ built from Q instead of K
+    "attn_dq_operand": ("dq[e] += ds * kr[e];", "dq[e] += ds * qr[e];"),
+    # dbqkv summed over the wrong column
+    "attn_dbqkv_column": ("for (int64_t r = 0; r < T; ++r) sb += dQKV[r * H3 + c];",
+                          "for (int64_t r = 0; r < T; ++r) sb += dQKV[r * H3 + (c + 1) % H3];"),
+    # the softmax row term D = rowsum(dP * P) without the P
+    "attn_D_without_p": ("D += s * Pg[r * S + c];", "D += s;"),
+    # dO read at the head's offset within its shard instead of its global offset
+    "attn_head_offset": ("const double *dor = dO + (b * S + r) * h + g * d;",
+                         "const double *dor = dO + (b * S + r) * h + (g % hpt) * d;"),
     # output projection: a shard's partial added twice
     "attn_fold": ("                for (int64_t c = 0; c < h; ++c) Z[r * h + c] += part[c];\n            }\n            for (int64_t c = 0; c < h; ++c) Z[r * h + c] += bo[c];",
                   "                for (int64_t c = 0; c < h; ++c) Z[r * h + c] += (i == 0 ? 2.0 : 1.0) * part[c];\n            }\n            for (int64_t c = 0; c < h; ++c) Z[r * h + c] += bo[c];"),
