@@ -47,6 +47,11 @@ MUTANTS = {
                          "dX[r * h + j] = rstd * (dy[j] * gamma[j] - mg);"),
     # dgamma without xhat
     "ln_dgamma": ("sg += dY[r * h + j] * (X[r * h + j] - mu[r]) * rs[r];", "sg += dY[r * h + j];"),
+    # LayerNorm forward: eps added outside the square root
+    "ln_eps_outside": ("const double rs = 1.0 / sqrt(v + eps);", "const double rs = 1.0 / sqrt(v) + eps;"),
+    # LayerNorm forward: beta added before the gamma scale
+    "ln_beta_inside": ("Y[r * h + j] = (x[j] - mu) * rs * gamma[j] + beta[j];",
+                       "Y[r * h + j] = ((x[j] - mu) * rs + beta[j]) * gamma[j];"),
     # attention without the causal mask on the scores
     "attn_no_mask": ("const int64_t last = r; /* causal", "const int64_t last = S - 1; /* causal"),
     # scores without the 1/sqrt(d) scale
