@@ -194,8 +194,9 @@ def host_cpu() -> str:
 
 # ------------------------------------------------------------------ oracle leg
 def oracle_sample(w, tokens: int):
-    """Time the fp64 oracle on the first `tokens` rows of the workload (full
-    weights); returns (seconds, flops, threads)."""
+    """Time the fp64 oracle on a `tokens`-token instance of the workload: its
+    recipe with fewer token rows (same h, F, t and value distributions, weights
+    of full size, drawn after the smaller X); returns (seconds, flops, threads)."""
     import oracle
     inp = inputs.for_workload(w, tokens=tokens)
     lib = oracle.load()
@@ -256,7 +257,8 @@ def run_reference(args, rank, world):
     dt = (time.perf_counter() - t0) / args.steps
     flops = 12.0 * args.oracle_tokens * w.hidden * w.ffn
     val = flops / dt / 1e12
-    sample = "first %d of %d token rows of %s per step, full weights, fp64" % (args.oracle_tokens, w.tokens, w.name)
+    sample = ("%d of %d token rows of %s per step (the workload's recipe with fewer tokens; full-size weights), "
+              "fp64" % (args.oracle_tokens, w.tokens, w.name))
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -664,7 +666,8 @@ def main():
             secs, fl, cores = oracle_sample(w, args.oracle_tokens)
             line["cpu_baseline"] = {"value": fl / secs / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
                                     "cpu": host_cpu(),
-                                    "sample": "first %d of %d token rows of %s, full weights, fp64 (%.1f s)"
+                                    "sample": "%d of %d token rows of %s (the workload's recipe with fewer "
+                                              "tokens; full-size weights), fp64 (%.1f s)"
                                               % (args.oracle_tokens, w.tokens, w.name, secs)}
         print(json.dumps(line), flush=True)
 

@@ -6,7 +6,8 @@ For every named workload (and its shard counts) it prints one JSON line with:
   exact slice oracle on sampled token rows and ffn columns;
 - whether three repeated runs are bit-identical;
 - the oracle's fp64 wall time on this host: measured in full for the small
-  workloads; for the large ones, measured on the first `--tokens` token rows and
+  workloads; for the large ones, measured on a `--tokens`-token instance of the
+  workload (its recipe with fewer tokens, full-size weights) and
   scaled to the full token count (marked "extrapolated": the oracle's work is
   linear in the tokens at a fixed h and F).
 
