@@ -13,9 +13,13 @@ section 4.1, for the MLP block Y = f(XA)B with A split by columns and B by rows)
     dB = Y^T dZ,  dA = X^T dY,  dX = sum_i dY[:, S_i] A[:, S_i]^T
 
 with shard i owning the ffn columns [i*F/t, (i+1)*F/t).  Every function here is
-pinned by ``tests/test_oracle_pins.py`` against closed forms, identities, a
-library routine (numpy) in the special case t = 1, mpmath brute force on tiny
-inputs, and central finite differences for the backward pass.
+pinned by ``tests/test_oracle_pins.py`` (pins in ``tests/oracle_pins.py``):
+closed forms and identities (GeLU's odd-part identity and asymptotes, the
+sharded sum equal to the unsharded product, X = 0 and A = 0), numpy matmuls in
+the special case t = 1 and per shard block, examples worked by hand (two
+shards and attention under ``tests/golden/``, LayerNorm in the pins), central finite
+differences of the loss for every gradient, and 24 planted one-line mistakes
+that the pins must catch (``tests/test_oracle_mutants.py``).
 """
 from __future__ import annotations
 
