@@ -307,10 +307,14 @@ void tpmlp_set_wait_limit_ns(uint64_t ns);
 tpmlp_status tpmlp_debug_timeout_probe(void *workspace, uint64_t wait_ns, void *stream);
 
 /* Column sums out[c] = sum_r x[r, c] of a row-major [rows, cols] device matrix
- * of the given dtype -- the kernel behind the bias gradients db = 1^T dZ and
- * da = 1^T dY of tpmlp_backward, same summation order, same results -- for callers
- * that cannot allocate device memory.  The pages have no counterpart to this
- * entry point; it exists for the caller, not the method.
+ * of the given dtype, for callers that cannot allocate device memory.  It runs
+ * the two-pass column-sum kernels that tpmlp_backward's FFMA path (fp32, or
+ * TPMLP_ALGO_SIMT) uses for db = 1^T dZ and da = 1^T dY, and gives the same bits
+ * as that path.  tpmlp_backward's tensor-core path sums in other orders (db in
+ * the dB GEMM's ones tile, da in per-32-row block sums of the dY epilogue), so
+ * against it the results agree to within bf16 rounding, not bit for bit.  The
+ * pages have no counterpart to this entry point; it exists for the caller, not
+ * the method.
  *
  * Who needs it: code that must not call cudaMalloc, e.g. a runtime whose device
  * memory is one pre-reserved arena owned by another component, or a caller on a
@@ -323,12 +327,14 @@ tpmlp_status tpmlp_debug_timeout_probe(void *workspace, uint64_t wait_ns, void *
  * process exits.  A call needs chunks*cols floats, where chunks depends only on
  * (rows, cols) and is at most ceil(1024 / ceil(cols/256)); requests that need
  * more (for instance cols > 1,048,576) return TPMLP_ERR_UNSUPPORTED with the
- * reason in tpmlp_last_error().  The first call on a device looks up the array's
- * device address (cudaGetSymbolAddress) for that device; make that first call
- * before any stream capture.  Every call uses the same array and leaves its
- * partials there; nothing in it needs to start at zero.  Calls that can overlap
- * on the GPU (other streams, other host threads) race on the array: serialise
- * them.  rows = 0 writes zeros.
+ * reason in tpmlp_last_error().  The first call on a device (and the first call
+ * after that device's context has been destroyed and recreated, e.g. by
+ * cudaDeviceReset) looks up the array's device address in the current context
+ * (cudaGetSymbolAddress); make that call before any stream capture.  Every call
+ * uses the same array and leaves its partials there; pass 1 writes every
+ * partial that pass 2 reads, so nothing in it needs to start at zero.  Calls
+ * that can overlap on the GPU (other streams, other host threads) race on the
+ * array: serialise them.  rows = 0 writes zeros.
  * Errors: INVALID_ARG for an unknown dtype, rows < 0, cols <= 0 or a NULL
  * pointer; UNSUPPORTED beyond the scratch limit; CUDA when a launch fails. */
 tpmlp_status tpmlp_colsum_noalloc(int32_t dtype, const void *x, int64_t rows, int64_t cols, void *out,

@@ -12,6 +12,7 @@
 //
 // Also here: the timeout probe, a kernel whose only job is to run a bounded wait
 // to its limit and report it.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -257,21 +258,52 @@ namespace noalloc {
 constexpr int64_t SCRATCH_FLOATS = int64_t(1) << 20;  // 4 MiB of fp32 partials
 static __device__ __align__(256) float g_scratch[SCRATCH_FLOATS];
 
-// Device address of g_scratch on the current device, looked up once per device.
+// Identifier of the current CUDA context, 0 when it cannot be read.  An address
+// looked up with cudaGetSymbolAddress belongs to the context it was looked up in;
+// after cudaDeviceReset the device's primary context is a new one.
+static unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_scratch on the current device, looked up once per device
+// and context (again if the context has changed since, or cannot be identified).
 // Host code must not use the symbol itself: on the host it is only a stand-in.
 static cudaError_t scratch_ptr(float **out) {
     static std::mutex mu;
     static float *ptrs[64] = {};
+    static unsigned long long ctx_ids[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(mu);
-    if (!ptrs[dev]) {
+    const unsigned long long id = current_context_id();
+    if (!ptrs[dev] || id == 0 || id != ctx_ids[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_scratch);
         if (e != cudaSuccess) return e;
         ptrs[dev] = static_cast<float *>(p);
+        ctx_ids[dev] = current_context_id();
     }
     *out = ptrs[dev];
     return cudaSuccess;
