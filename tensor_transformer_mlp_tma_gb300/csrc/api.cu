@@ -253,7 +253,7 @@ GemmArgs base_args(uint32_t *status) {
     return g;
 }
 
-// Raster order of the tensor-core GEMM tiles (128 x 256).  Tiles are walked in
+// Raster order of the tensor-core GEMM tiles (256 x 256, 256 x 512 or 128 x 256).  Tiles are walked in
 // super-rows of G tiles along M (or N); the G operand panels of the grouped
 // dimension (each spans all of K) are re-read while the super-row lasts, so
 // they should stay in L2, and each panel of the other operand is read once per
@@ -261,9 +261,10 @@ GemmArgs base_args(uint32_t *status) {
 // or  B + A * ceil(n_tiles / G)  (along N); G is the largest group whose panels
 // fit in the L2 budget, and the cheaper direction wins.
 // TPMLP_RASTER=m:G or n:G overrides the choice (a tuning knob, read per call).
-void pick_raster(GemmArgs &g) {
+void pick_raster(GemmArgs &g, Epi epi = tpmlp::EPI_FOLD) {
     const int64_t tile_m = g.cta_pair ? 256 : 128;
-    const int64_t m_tiles = (g.M + tile_m - 1) / tile_m, n_tiles = (g.N + 255) / 256;
+    const int64_t tile_n = tpmlp::tc_wide_tile(epi, g) ? 512 : 256;
+    const int64_t m_tiles = (g.M + tile_m - 1) / tile_m, n_tiles = (g.N + tile_n - 1) / tile_n;
     const char *env = std::getenv("TPMLP_RASTER");
     if (env && (env[0] == 'm' || env[0] == 'n') && env[1] == ':') {
         g.raster_n = env[0] == 'n';
@@ -272,7 +273,7 @@ void pick_raster(GemmArgs &g) {
     }
     const char *bud = std::getenv("TPMLP_L2_PANEL_MB");
     const double budget = (bud ? std::atof(bud) : 24.0) * 1048576.0;
-    const double a_panel = static_cast<double>(tile_m) * g.K * 2, b_panel = 256.0 * g.K * 2;
+    const double a_panel = static_cast<double>(tile_m) * g.K * 2, b_panel = static_cast<double>(tile_n) * g.K * 2;
     const double a_total = static_cast<double>(g.M) * g.K * 2, b_total = static_cast<double>(g.N) * g.K * 2;
     int64_t gm = static_cast<int64_t>(budget / a_panel), gn = static_cast<int64_t>(budget / b_panel);
     // Very long K makes panels too big for the budget; tiles that run in the same
@@ -398,7 +399,7 @@ tpmlp_status tpmlp_forward(const tpmlp_shape *s, const void *X, const void *A, c
     g1.b = A, g1.b_mn = true;   // A[h,F]: N contiguous, MN-major
     g1.M = T, g1.N = F, g1.K = h, g1.kshard = h;
     g1.out0 = saved ? saved->H : nullptr, g1.out1 = Y, g1.bias = a;
-    pick_raster(g1);
+    pick_raster(g1, tpmlp::EPI_BIAS_GELU);
     cudaError_t e = gemm(s, "fc1_bias_gelu", tpmlp::EPI_BIAS_GELU, g1, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
@@ -462,7 +463,7 @@ tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_sa
     g3.out1 = rec ? Y : nullptr;
     // On tensor cores the epilogue also sums dY's columns per 32-row block.
     g3.colsum_part = use_tc(s) ? partials : nullptr;
-    pick_raster(g3);
+    pick_raster(g3, tpmlp::EPI_DGELU);
     e = gemm(s, "bwd_dY_dgelu", tpmlp::EPI_DGELU, g3, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
@@ -484,7 +485,7 @@ tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_sa
     g4.M = F, g4.N = h, g4.K = T, g4.kshard = T;
     g4.out0 = dB;
     if (use_tc(s)) g4.ones = ones, g4.bias_grad = db;  // db = 1^T dZ from an extra ones tile
-    pick_raster(g4);
+    pick_raster(g4, tpmlp::EPI_STORE);
     e = gemm(s, "bwd_dB", tpmlp::EPI_STORE, g4, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
@@ -494,7 +495,7 @@ tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_sa
     g5.b = dY, g5.b_mn = true;        // dY[T,F] as [K=T, N=F]: MN-major
     g5.M = h, g5.N = F, g5.K = T, g5.kshard = T;
     g5.out0 = dA;
-    pick_raster(g5);
+    pick_raster(g5, tpmlp::EPI_STORE);
     e = gemm(s, "bwd_dA", tpmlp::EPI_STORE, g5, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
@@ -999,7 +1000,7 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
     g2.M = h, g2.N = h, g2.K = T, g2.kshard = T;
     g2.out0 = dWo;
     g2.ones = ones, g2.bias_grad = dbo;
-    pick_raster(g2);
+    pick_raster(g2, tpmlp::EPI_STORE);
     e = gemm(&ms, "attn_bwd_dWo", tpmlp::EPI_STORE, g2, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
@@ -1046,7 +1047,7 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
     g7.M = h, g7.N = 3 * h, g7.K = T, g7.kshard = T;
     g7.out0 = dWqkv;
     g7.ones = ones, g7.bias_grad = dbqkv;
-    pick_raster(g7);
+    pick_raster(g7, tpmlp::EPI_STORE);
     e = gemm(&ms, "attn_bwd_dWqkv", tpmlp::EPI_STORE, g7, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 

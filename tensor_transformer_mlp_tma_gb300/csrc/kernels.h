@@ -81,6 +81,11 @@ cudaError_t launch_fill_ones_bf16(void *p, int64_t n, cudaStream_t st);
 // Tensor-core path: bf16 operands, fp32 accumulation in TMEM (tcgen05).
 cudaError_t launch_tc_gemm(Epi epi, const GemmArgs &g, int num_sms, cudaStream_t st);
 
+// Whether launch_tc_gemm runs this product on 256 x 512 tiles (CTA pairs; the
+// store, bias + GeLU and GeLU' epilogues of one shard on plain operands) rather
+// than 256 x 256.  TPMLP_WIDE=0 keeps 256 x 256 (a tuning knob, read per call).
+bool tc_wide_tile(Epi epi, const GemmArgs &g);
+
 // FFMA path: element type fp32 (is_bf16 = false) or bf16, fp32 accumulation.
 cudaError_t launch_simt_gemm(Epi epi, bool is_bf16, const GemmArgs &g, cudaStream_t st);
 

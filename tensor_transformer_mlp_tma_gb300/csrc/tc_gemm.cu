@@ -5,7 +5,10 @@
 // Tiles are 256 x 256 on CTA pairs (a 2-CTA cluster, tcgen05 cta_group::2: each
 // CTA loads its 128 rows of A and 128 of B's 256 columns, the even CTA issues the
 // MMAs, each CTA's TMEM holds its 128 rows of the accumulator) or 128 x 256 on
-// single CTAs.  Outputs at most 128 wide take 256 x 128 tiles on CTA pairs.
+// single CTAs.  Outputs at most 128 wide take 256 x 128 tiles on CTA pairs.  The
+// plain-store and GeLU epilogues (no shard fold) can take 256 x 512 tiles on CTA
+// pairs instead: two MMAs of N = 256 per k-step into the two halves of the 512
+// TMEM columns, which loads a quarter fewer operand bytes per FLOP (see Cfg).
 // One persistent CTA per SM, 10 warps:
 //   warp 0      TMA producer (one elected lane): fills a ring of stages (4 to 8)
 //               of 128x64 A tiles and B tiles of the CTA's columns, 128-byte
@@ -65,6 +68,16 @@ constexpr int STG_BOX_WIDE = 32 * 64 * 2;
 // TILE_N = 128 (CTA pairs only) is the narrow tile for outputs at most 128 wide
 // (the per-head products with N = d): each CTA loads 64 of B's columns, a stage
 // is 24 KB and eight stages fit.
+//
+// TILE_N = 512 (CTA pairs only) is the wide tile: each CTA loads 128 rows of A
+// and 256 of B's columns (a 48 KB stage, four of them), and one k-step is two
+// MMAs of 256 x 256 x 16, one per half of the tile's columns, into the two
+// 256-column halves of the CTA's TMEM.  Per SM that is 48 KB of operands per
+// 8.4 MFLOP instead of 32 KB per 4.2 MFLOP: 25% fewer bytes from L2 per FLOP,
+// and 15% less shared-memory traffic (TMA writes plus MMA reads) per FLOP.
+// The accumulator is no longer double-buffered; the MMA warp starts a tile's
+// first half as soon as the epilogue has drained that half of the previous
+// tile (see the MMA issuer).
 template <int CG, int TILE_N_ = BN, int EPI_ = EPI_STORE>
 struct Cfg {
     static constexpr int TILE_M = BM * CG;
@@ -77,12 +90,25 @@ struct Cfg {
     static constexpr int STG_PER_WARP = DS ? 2 * STG_BOX_WIDE : 2 * STG_BOX;
     // dS: the K extent is one head dimension (two K blocks per tile), so fewer
     // stages make room for its wider staging boxes
-    static constexpr int STAGES = CG == 1 ? (DS ? 3 : 4) : (TILE_N == BN ? (DS ? 5 : 6) : 8);
+    static constexpr int STAGES = CG == 1 ? (DS ? 3 : 4) : (TILE_N == BN ? (DS ? 5 : 6) : (TILE_N == 512 ? 4 : 8));
     static constexpr int SMEM_DYN = STAGES * STAGE_BYTES + (EPI_THREADS / 32) * STG_PER_WARP + 1024;
 };
 constexpr int MAX_STAGES = 8;
 
 constexpr uint32_t STATUS_TIMEOUT = 4;  // TPMLP_ERR_TIMEOUT
+constexpr uint32_t STATUS_DEVICE = 5;   // TPMLP_ERR_DEVICE: a bounds check of the TPMLP_DEBUG build failed
+
+// The TPMLP_DEBUG build (libtpmlp_debug.so) checks, before every TMA copy, MMA,
+// TMEM load and global store of the kernel, that the tile coordinates, k-block
+// range, shared-memory addresses, TMEM columns and partial-sum indices lie inside
+// what the launch set up.  A failed check records TPMLP_ERR_DEVICE and the check's
+// code in the status word, raises the CTA's abort flag and skips the access; the
+// kernel then winds down like after a timeout.  It stands in for a memory checker
+// on a machine where none can run.  In the normal build every check is a
+// constant true and compiles away.
+#ifndef TPMLP_DEBUG
+#define TPMLP_DEBUG 0
+#endif
 
 struct Params {
     int M, N;
@@ -116,6 +142,10 @@ struct Params {
     // problem z = b * heads + g and head g = i * hpt + j (hpt heads per shard).
     int a_rank, b_rank, o_rank;
     int heads, hpt;
+    // Wide tiles (TILE_N = 512): the last `wide_tail` tiles of the order are each
+    // split into their two 256-column halves, run as separate half-width tiles,
+    // so that a last partial wave of wide tiles is spread over twice the units.
+    int wide_tail;
 };
 
 // Coordinates after (x, y) of problem z in a map of the given rank.
@@ -209,6 +239,22 @@ __device__ __forceinline__ void tile_coords(int tile, const Params &p, int &mb, 
     if (p.flip_odd && (zb & 1)) mb = p.m_tiles - 1 - mb;
 }
 
+// Wide tiles: the tile order is that of tile_coords over the 256 x 512 tiles,
+// except that each of the last p.wide_tail of them is run as two half-width
+// tiles.  hm is the set of column halves the slot covers: 3 both, 1 the first
+// 256-column half (TMEM columns 0..255), 2 the second (TMEM columns 256..511).
+__device__ __forceinline__ void wide_coords(int tile, const Params &p, int &mb, int &nb, int &zb, int &hm) {
+    const int full = p.m_tiles * p.n_tiles * p.batch - p.wide_tail;
+    int wt = tile;
+    hm = 3;
+    if (tile >= full) {
+        const int j = tile - full;
+        wt = full + (j >> 1);
+        hm = 1 << (j & 1);
+    }
+    tile_coords(wt, p, mb, nb, zb);
+}
+
 // Records a timeout once in the status word (detail = which role gave up).
 __device__ __forceinline__ void record_timeout(const Params &p, volatile int *abort_flag,
                                                uint32_t role) {
@@ -216,6 +262,27 @@ __device__ __forceinline__ void record_timeout(const Params &p, volatile int *ab
     if (p.status) {
         if (atomicCAS(p.status, 0u, STATUS_TIMEOUT) == 0u) atomicExch(p.status + 1, role);
     }
+}
+
+// Debug-build bounds check (see TPMLP_DEBUG above): true if `cond` holds.
+// code = (check << 8) | role, role 1 producer, 2 MMA issuer, 3 epilogue.
+__device__ __forceinline__ bool dbg_ok(bool cond, const Params &p, volatile int *abort_flag, uint32_t code) {
+#if TPMLP_DEBUG
+    if (!cond) {
+        *abort_flag = 1;
+        if (p.status && atomicCAS(p.status, 0u, STATUS_DEVICE) == 0u) atomicExch(p.status + 1, code);
+    }
+    return cond;
+#else
+    (void)cond, (void)p, (void)abort_flag, (void)code;
+    return true;
+#endif
+}
+
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(n));
+    return n;
 }
 
 __device__ __forceinline__ float gelu_f(float x) {
@@ -542,14 +609,20 @@ template <int EPI, bool A_MN, bool B_MN, int CG, bool HEADS, int TILE_N>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
-                const __grid_constant__ CUtensorMap tmO2, const Params p) {
+                const __grid_constant__ CUtensorMap tmO2, const __grid_constant__ CUtensorMap tmB2,
+                const Params p) {
     using C = Cfg<CG, TILE_N, EPI>;
     constexpr bool PAIR = CG == 2;
     constexpr bool FOLD = (EPI == EPI_FOLD_BIAS || EPI == EPI_FOLD);
-    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(C::TILE_M, TILE_N, A_MN, B_MN);
+    constexpr bool WIDE = TILE_N == 512;
+    constexpr int MMA_N = WIDE ? 256 : TILE_N;  // N of one MMA instruction
+    constexpr uint32_t IDESC = ptx::idesc_bf16_f32(C::TILE_M, MMA_N, A_MN, B_MN);
     // each epilogue warp finishes TILE_N / 2 columns of its 32 rows, in 32-column chunks
     constexpr int CHUNKS = TILE_N / 64;
-    static_assert(TILE_N == BN || (TILE_N == 128 && CG == 2 && EPI == EPI_STORE), "narrow tile: CTA pairs, plain store");
+    static_assert(TILE_N == BN || TILE_N == 512 || (TILE_N == 128 && CG == 2 && EPI == EPI_STORE),
+                  "narrow tile: CTA pairs, plain store");
+    static_assert(!WIDE || (CG == 2 && !HEADS && (EPI == EPI_STORE || EPI == EPI_BIAS_GELU || EPI == EPI_DGELU)),
+                  "wide tile: CTA pairs, one shard, store / bias+GeLU / GeLU' epilogues");
     constexpr int STAGES = C::STAGES;
 
     extern __shared__ uint8_t smem_raw[];
@@ -593,6 +666,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB);
+        if constexpr (WIDE) ptx::prefetch_tensormap(&tmB2);
         ptx::prefetch_tensormap(&tmO0);
         ptx::prefetch_tensormap(&tmO1);
         ptx::prefetch_tensormap(&tmO2);
@@ -617,8 +691,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // and may overlap the previous kernel's tail; global memory is used only
     // after that kernel's grid has completed.
     ptx::griddep_wait();
+    // Debug build: the dynamic shared memory of the launch holds the aligned ring
+    // and the staging boxes, and the tile counts are positive.
+    const uint32_t ring_end = smem_base + STAGES * C::STAGE_BYTES;
+    const uint32_t stg_end = ring_end + (EPI_THREADS / 32) * C::STG_PER_WARP;
+    const bool launch_ok = dbg_ok(stg_end <= ptx::smem_u32(smem_raw) + dynamic_smem_bytes() && p.m_tiles > 0 &&
+                                      p.n_tiles > 0 && p.batch > 0 && p.nshards > 0 && p.kb_per_shard > 0,
+                                  p, &abort_sh, 0x0100u);
+    (void)ring_end, (void)stg_end;
 
-    const int num_tiles = p.m_tiles * p.n_tiles * p.batch;
+    const int num_tiles = p.m_tiles * p.n_tiles * p.batch + (WIDE ? p.wide_tail : 0);
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -626,7 +708,82 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             int64_t issued = 0;
-            bool ok = true;
+            bool ok = launch_ok;
+            if constexpr (WIDE) {
+            // Wide tiles: A as in the other tiles; B is this CTA's 256 of the tile's
+            // 512 columns (one copy, map tmB), or for a half-width slot the 128 of
+            // them in that half (map tmB2), placed where the MMA of that half reads.
+            for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
+                int mb, nb, zb, hm;
+                wide_coords(tile, p, mb, nb, zb, hm);
+                const int m0 = mb * C::TILE_M + BM * static_cast<int>(rank);
+                const int hs = hm == 2 ? 1 : 0;  // first half loaded
+                const bool both = hm == 3;
+                const int n0 = nb * TILE_N + C::B_ROWS * static_cast<int>(rank) + (C::B_ROWS / 2) * hs;
+                const uint32_t stage_bytes = CG * (C::A_STAGE + (both ? C::B_STAGE : C::B_STAGE / 2));
+                const int b_blocks = (both ? C::B_ROWS : C::B_ROWS / 2) / 64;
+                const CUtensorMap *bmap = both ? &tmB : &tmB2;
+                const bool ones_tile = EPI == EPI_STORE && A_MN && B_MN && p.bias_tile && mb == p.m_tiles - 1;
+                const int nkb = p.kb_per_shard;
+                if (!dbg_ok(mb >= 0 && mb < p.m_tiles && nb >= 0 && nb < p.n_tiles && zb >= 0 && zb < p.batch &&
+                                (hm == 1 || hm == 2 || hm == 3) && n0 % 64 == 0,
+                            p, &abort_sh, 0x0201u)) {
+                    ok = false;
+                    break;
+                }
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_empty[stage]), phase ^ 1u, p.wait_ns,
+                                                     &abort_sh)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full_local = ptx::smem_u32(&bar_full[stage]);
+                    const uint32_t full = ptx::mapa_shared(full_local, 0);
+                    const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
+                    const uint32_t sb = sa + C::A_STAGE + hs * (C::B_STAGE / 2);
+                    const int k0 = kb * BK;
+                    if (!dbg_ok(stage >= 0 && stage < STAGES && sb + b_blocks * MN_BLOCK_BYTES <= ring_end, p,
+                                &abort_sh, 0x0301u)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) ptx::mbar_arrive_expect_tx(full_local, stage_bytes);
+                    if (ones_tile) {
+                        // the bias-gradient tile: A is the 64 x 64 block of ones (rank 0,
+                        // block 0), the rest reads as zero (see the other tiles' loop)
+#pragma unroll
+                        for (int j = 0; j < BM / 64; ++j)
+                            ptx::tma_load_3d_pair(sa + j * MN_BLOCK_BYTES, &tmO2, full,
+                                                  BM * static_cast<int>(rank) + 64 * j, 0, 0);
+                    } else if constexpr (!A_MN) {
+                        ptx::tma_load_3d_pair(sa, &tmA, full, k0, m0, zb);
+                    } else {
+                        if (p.a_mn4) {
+                            ptx::tma_load_4d_pair(sa, &tmA, full, 0, k0, m0 / 64, zb);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < BM / 64; ++j)
+                                ptx::tma_load_3d_pair(sa + j * MN_BLOCK_BYTES, &tmA, full, m0 + 64 * j, k0, zb);
+                        }
+                    }
+                    if constexpr (!B_MN) {
+                        ptx::tma_load_3d_pair(sb, bmap, full, k0, n0, zb);
+                    } else {
+                        if (p.b_mn4) {
+                            ptx::tma_load_4d_pair(sb, bmap, full, 0, k0, n0 / 64, zb);
+                        } else {
+                            for (int j = 0; j < b_blocks; ++j)
+                                ptx::tma_load_3d_pair(sb + j * MN_BLOCK_BYTES, &tmB, full, n0 + 64 * j, k0, zb);
+                        }
+                    }
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            } else {
             for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
                 int mb, nb, zb;
                 tile_coords(tile, p, mb, nb, zb);
@@ -635,6 +792,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int n0 = nb * TILE_N + C::B_ROWS * static_cast<int>(rank);
                 int kb0, kb1;
                 k_range<C::TILE_M>(p, mb, kb0, kb1);
+                if (!dbg_ok(mb >= 0 && mb < p.m_tiles && nb >= 0 && nb < p.n_tiles && zb >= 0 && zb < p.batch &&
+                                kb0 >= 0 && kb0 <= kb1 && kb1 <= p.nshards * p.kb_per_shard && n0 % 64 == 0,
+                            p, &abort_sh, 0x0401u)) {
+                    ok = false;
+                    break;
+                }
                 if constexpr (EPI == EPI_STORE && A_MN && B_MN && !HEADS) {
                     if (p.bias_tile && mb == p.m_tiles - 1) {
                         // The ones tile (its own loop, so the main loop below is unchanged):
@@ -697,6 +860,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
                     const uint32_t sb = sa + C::A_STAGE;
                     const int k0 = kb * BK;
+                    if (!dbg_ok(stage >= 0 && stage < STAGES && sb + C::B_STAGE <= ring_end, p, &abort_sh, 0x0501u)) {
+                        ok = false;
+                        break;
+                    }
                     auto load = [&](uint32_t dst, const CUtensorMap *map, int x, int y) {
                         if constexpr (PAIR)
                             ptx::tma_load_3d_pair(dst, map, full, x, y, zb);
@@ -761,6 +928,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
+            }
             if (!ok) record_timeout(p, &abort_sh, 1);
             // Let every copy started for this CTA's stages land before the CTA can
             // exit.  In a pair the stage-full barriers live in the leader and count
@@ -781,7 +949,110 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t unit = 0;
-            bool ok = true;
+            bool ok = launch_ok;
+            if constexpr (WIDE) {
+            // Wide tiles: one accumulator of 512 columns, half h at TMEM columns
+            // [256h, 256h + 256), filled by the MMAs of half h (B columns at
+            // 16 KB * h in the stage).  A tile waits for the epilogue to drain each
+            // half of the previous tile separately: it issues the first half's MMAs
+            // for up to STAGES k-blocks (the stages already loaded) as soon as the
+            // first half is drained, while the epilogue still drains the second
+            // half, then the second half's MMAs of those k-blocks, then both halves
+            // per k-block.  One commit per tile tells the epilogue the whole
+            // accumulator is complete.
+            uint32_t use[2] = {0u, 0u};
+            auto issue_half = [&](int st, int hh, bool first) {
+                const uint32_t sa = smem_base + st * C::STAGE_BYTES;
+                const uint32_t sb = sa + C::A_STAGE + hh * (C::B_STAGE / 2);
+                const uint32_t d_tmem = tmem_base + hh * MMA_N;
+                if (!dbg_ok(st >= 0 && st < STAGES && (hh == 0 || hh == 1) && hh * MMA_N + MMA_N <= int(TMEM_COLS) &&
+                                sb + C::B_STAGE / 2 <= ring_end,
+                            p, &abort_sh, 0x0602u))
+                    return;
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k) {
+                    const uint64_t ad = A_MN ? ptx::sdesc_sw128(sa + k * 2048, MN_BLOCK_BYTES, 1024)
+                                             : ptx::sdesc_sw128(sa + k * 32, 16, 1024);
+                    const uint64_t bd = B_MN ? ptx::sdesc_sw128(sb + k * 2048, MN_BLOCK_BYTES, 1024)
+                                             : ptx::sdesc_sw128(sb + k * 32, 16, 1024);
+                    ptx::umma_f16_ss_pair(d_tmem, ad, bd, IDESC, (first && k == 0) ? 0u : 1u);
+                }
+            };
+            auto wait_drained = [&](int hh) -> bool {
+                const bool got = ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_tempty[hh]), (use[hh] & 1u) ^ 1u,
+                                                             p.wait_ns, &abort_sh);
+                ++use[hh];
+                ptx::tc_fence_after();
+                return got;
+            };
+            auto wait_loaded = [&](int st, uint32_t ph) -> bool {
+                const bool got = ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_full[st]), ph, p.wait_ns, &abort_sh);
+                ptx::tc_fence_after();
+                return got;
+            };
+            auto release_stage = [&]() {
+                ptx::umma_commit_pair_multicast(ptx::smem_u32(&bar_empty[stage]), 0x3);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            };
+            for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
+                int mb, nb, zb, hm;
+                wide_coords(tile, p, mb, nb, zb, hm);
+                const int nkb = p.kb_per_shard;
+                if (hm == 3) {
+                    if (!wait_drained(0)) {
+                        ok = false;
+                        break;
+                    }
+                    const int lead = nkb < STAGES ? nkb : STAGES;
+                    int st = stage;
+                    uint32_t ph = phase;
+                    for (int j = 0; j < lead; ++j) {
+                        if (!wait_loaded(st, ph)) {
+                            ok = false;
+                            break;
+                        }
+                        issue_half(st, 0, j == 0);
+                        if (++st == STAGES) st = 0, ph ^= 1u;
+                    }
+                    if (!ok || !wait_drained(1)) {
+                        ok = false;
+                        break;
+                    }
+                    for (int j = 0; j < lead; ++j) {
+                        issue_half(stage, 1, j == 0);
+                        release_stage();
+                    }
+                    for (int kb = lead; kb < nkb; ++kb) {
+                        if (!wait_loaded(stage, phase)) {
+                            ok = false;
+                            break;
+                        }
+                        issue_half(stage, 0, false);
+                        issue_half(stage, 1, false);
+                        release_stage();
+                    }
+                } else {
+                    const int hh = hm >> 1;  // the one half this slot computes
+                    if (!wait_drained(hh)) {
+                        ok = false;
+                        break;
+                    }
+                    for (int kb = 0; kb < nkb; ++kb) {
+                        if (!wait_loaded(stage, phase)) {
+                            ok = false;
+                            break;
+                        }
+                        issue_half(stage, hh, kb == 0);
+                        release_stage();
+                    }
+                }
+                if (!ok) break;
+                ptx::umma_commit_pair_multicast(ptx::smem_u32(&bar_tfull[0]), 0x3);
+            }
+            } else {
             for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
                 int mb, nb, zb;
                 tile_coords(tile, p, mb, nb, zb);
@@ -799,6 +1070,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * TILE_N;
+                    if (!dbg_ok(buf * TILE_N + TILE_N <= TMEM_COLS && kb0 >= 0 && kb0 <= kb1 &&
+                                    kb1 <= p.nshards * p.kb_per_shard,
+                                p, &abort_sh, 0x0702u)) {
+                        ok = false;
+                        break;
+                    }
                     // Stages are taken two at a time: wait for both, then issue their
                     // eight MMAs back to back.  Measured on GB300 this issues 2-7% faster
                     // per clock than one stage at a time (MN/MN GEMMs gain once their
@@ -853,6 +1130,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ptx::umma_commit(ptx::smem_u32(&bar_tfull[buf]));
                 }
             }
+            }
             if (!ok) record_timeout(p, &abort_sh, 3);
             // Retire every MMA this thread issued before TMEM can be freed.
             if constexpr (PAIR)
@@ -869,7 +1147,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t stg = smem_base + STAGES * C::STAGE_BYTES + ew * C::STG_PER_WARP;
         uint32_t unit = 0;
-        bool ok = true;
+        bool ok = launch_ok;
         float sum[FOLD ? TILE_N / 2 : 1];
         (void)sum;
         AuxLoad aux{ptx::smem_u32(&bar_aux[ew]), 0u, false};
@@ -886,6 +1164,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::mbar_arrive(a);
             }
         };
+        if constexpr (WIDE) {
+        // Wide tiles: this warp finishes TMEM columns [128 * half, 128 * half + 128)
+        // of each accumulator half hh; chunk q = 4 hh + c (c = 0..3) is output
+        // columns 512 nb + 256 half + 32 q.  (The pair MMA of half hh reads B
+        // columns 512 nb + 128 hh + [0, 128) in the even CTA and 512 nb + 256 +
+        // 128 hh + [0, 128) in the odd one.)  Each half is released as soon as its
+        // four chunks are in registers, so the next tile's MMAs of that half can
+        // start.
+        uint32_t tcount = 0;
+        for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
+            if (tile + num_units >= num_tiles) ptx::griddep_launch_dependents();
+            int mb, nb, zb, hm;
+            wide_coords(tile, p, mb, nb, zb, hm);
+            const int row0 = mb * C::TILE_M + BM * static_cast<int>(rank) + quarter * 32;
+            const int64_t row = static_cast<int64_t>(row0) + lane;
+            const int col0 = nb * TILE_N + half * (TILE_N / 2);
+            const int qa = hm == 2 ? 4 : 0, qb = hm == 1 ? 4 : 8;
+            const bool ones_tile = EPI == EPI_STORE && A_MN && B_MN && p.bias_tile && mb == p.m_tiles - 1;
+            if constexpr (EPI == EPI_DGELU) aux_issue(&tmO1, aux, stg + STG_BOX, col0 + 32 * qa, row0, zb, lane);
+            bool got = ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_tfull[0]), tcount & 1u, p.wait_ns, &abort_sh);
+            ++tcount;
+            got = __all_sync(0xffffffffu, got);
+            if (!got) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            for (int q = qa; q < qb; ++q) {
+                const uint32_t taddr = tmem_base + lane_off + (q >> 2) * MMA_N + half * 128 + (q & 3) * 32;
+                if (!dbg_ok((q >> 2) * MMA_N + half * 128 + (q & 3) * 32 + 32 <= int(TMEM_COLS) &&
+                                stg + C::STG_PER_WARP <= stg_end && (col0 + 32 * q) % 32 == 0 && row0 % 32 == 0,
+                            p, &abort_sh, 0x0803u)) {
+                    ok = false;
+                    break;
+                }
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(taddr, r);
+                ptx::tmem_ld_wait(r);
+                if ((q & 3) == 3) release(static_cast<uint32_t>(q >> 2));
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                if (ones_tile) {
+                    // row 0 of the ones tile holds the column sums of B; the tile
+                    // has no rows of the output
+                    if (rank == 0 && quarter == 0 && lane == 0) store_bias_grad(p, col0 + 32 * q, v);
+                    continue;
+                }
+                finish_chunk<EPI, false>(p, &tmO0, &tmO1, &tmO2, v, row, row0, col0 + 32 * q, zb, lane, stg, &aux,
+                                         q + 1 < qb ? col0 + 32 * (q + 1) : -1, row0, &abort_sh);
+            }
+        }
+        } else {
         for (int tile = unit_id; tile < num_tiles && ok; tile += num_units) {
             // On starting this CTA's last tile, allow the next kernel in the stream
             // to be scheduled: its CTAs take the SMs of CTAs that have finished.
@@ -911,6 +1242,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 ptx::tc_fence_after();
                 const uint32_t taddr = tmem_base + lane_off + buf * TILE_N + half * (TILE_N / 2);
+                if (!dbg_ok(buf * TILE_N + TILE_N <= TMEM_COLS && stg + C::STG_PER_WARP <= stg_end &&
+                                col0 % 32 == 0 && row0 % 32 == 0 && mb >= 0 && mb < p.m_tiles && nb >= 0 &&
+                                nb < p.n_tiles && zb >= 0 && zb < p.batch,
+                            p, &abort_sh, 0x0903u)) {
+                    ok = false;
+                    break;
+                }
                 if constexpr (FOLD) {
 #pragma unroll
                     for (int c = 0; c < CHUNKS; ++c) {
@@ -1005,6 +1343,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
+        }
         }
         if (!ok) record_timeout(p, &abort_sh, 5);
         // an H or P load still in flight (only after an abort) must land before the CTA exits
@@ -1208,9 +1547,12 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     const int b_rank = HEADS && g.b_view.rank > 3 ? g.b_view.rank : 3;
     const int o_rank = HEADS && g.o_view.rank > 3 ? g.o_view.rank : 3;
     // (HEADS kernels always copy MN-major operands block by block.)
+    constexpr bool WIDE = TILE_N == 512;
+    CUtensorMap mb2;  // wide tiles: B of one 256-column half of the tile (half the box)
     const bool a4 = !HEADS && A_MN && mn4 && g.M % 64 == 0 && make_map_mn4(&ma, g.a, g.K, g.M, BK, BM / 64, nb);
     const bool b4 = !HEADS && B_MN && mn4 && g.N % 64 == 0 &&
-                    make_map_mn4(&mb, g.b, g.K, g.N, BK, C::B_ROWS / 64, nb);
+                    make_map_mn4(&mb, g.b, g.K, g.N, BK, C::B_ROWS / 64, nb) &&
+                    (!WIDE || make_map_mn4(&mb2, g.b, g.K, g.N, BK, C::B_ROWS / 128, nb));
     bool oka, okb;
     if (a_rank > 3)
         oka = make_map_view(&ma, g.a, g.a_view, 64, A_MN ? BK : BM, sw);
@@ -1221,6 +1563,8 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     else
         okb = b4 || (B_MN ? make_map(&mb, g.b, g.K, g.N, 64, BK, sw, nb)
                           : make_map(&mb, g.b, g.N, g.K, BK, C::B_ROWS, sw, nb));
+    if (WIDE && !B_MN && okb) okb = make_map(&mb2, g.b, g.N, g.K, BK, C::B_ROWS / 2, sw, nb);
+    if (!WIDE || (B_MN && !b4)) mb2 = mb;  // unused, or the per-block maps serve both widths
     if (!oka || !okb) return cudaErrorInvalidValue;
     // Output maps: [M, N] row-major, 32 x 32 boxes, 64-byte swizzle (matches stage_row).
     // Bias + GeLU writes H (optional) and Y; GeLU' reads H through the second map;
@@ -1303,9 +1647,20 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
                        static_cast<long long>(g.M), static_cast<long long>(g.K), g.nshards);
         return cudaErrorInvalidValue;
     }
-    const int tiles = p.m_tiles * p.n_tiles * p.batch;
+    int tiles = p.m_tiles * p.n_tiles * p.batch;
     int resident = max_clusters[dev];
     if (const char *o = std::getenv("TPMLP_MAX_UNITS")) resident = std::atoi(o) > 0 ? std::atoi(o) : resident;
+    // Wide tiles: a last partial wave of r tiles is run as 2r half-width tiles
+    // when they fit in one wave (2r <= units): the wave then takes about half a
+    // wide tile's time.  TPMLP_WIDE_TAIL=0 keeps whole tiles (a tuning knob, read
+    // per call).
+    p.wide_tail = 0;
+    if (WIDE) {
+        const char *tail_env = std::getenv("TPMLP_WIDE_TAIL");
+        const int r = tiles % resident;
+        if (!(tail_env && tail_env[0] == '0') && 2 * r <= resident) p.wide_tail = r;
+        tiles += p.wide_tail;
+    }
     const int units = tiles < resident ? tiles : resident;
     if (std::getenv("TPMLP_DEBUG_LAUNCH"))
         std::fprintf(stderr, "tpmlp gemm epi=%d cg=%d M=%lld N=%lld K=%lld tiles=%d resident=%d grid=%d group=%d%c\n",
@@ -1322,7 +1677,7 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
             cfg.numAttrs = 1;
         }
     }
-    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo0, mo1, mo2, p);
+    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mo0, mo1, mo2, mb2, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         cudaFuncAttributes fa;
@@ -1338,6 +1693,9 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
 
 template <int EPI, bool A_MN, bool B_MN>
 static cudaError_t launch_cg(const GemmArgs &g, int num_sms, cudaStream_t st) {
+    if constexpr (EPI == EPI_BIAS_GELU || EPI == EPI_DGELU || (EPI == EPI_STORE && A_MN && B_MN)) {
+        if (tc_wide_tile(static_cast<Epi>(EPI), g)) return launch_t<EPI, A_MN, B_MN, 2, false, 512>(g, num_sms, st);
+    }
     if constexpr (EPI == EPI_ATTN_SCORE || EPI == EPI_ATTN_DS || EPI == EPI_STORE) {
         if (g.heads_layout) {
             // Outputs at most 128 wide (the per-head products with N = d) take the
@@ -1356,6 +1714,13 @@ static cudaError_t launch_cg(const GemmArgs &g, int num_sms, cudaStream_t st) {
 }
 
 }  // namespace tc
+
+bool tc_wide_tile(Epi epi, const GemmArgs &g) {
+    if (!g.cta_pair || g.heads_layout || g.nshards != 1 || g.causal_k != 0 || g.skip_upper) return false;
+    if (!(epi == EPI_BIAS_GELU || epi == EPI_DGELU || (epi == EPI_STORE && g.a_mn && g.b_mn))) return false;
+    const char *w = std::getenv("TPMLP_WIDE");
+    return !(w && w[0] == '0');
+}
 
 cudaError_t launch_tc_gemm(Epi epi, const GemmArgs &g, int num_sms, cudaStream_t st) {
     using namespace tc;

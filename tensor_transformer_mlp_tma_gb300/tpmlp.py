@@ -3,7 +3,9 @@ only.  Every step of the forward and backward pass runs in the library's CUDA
 kernels; PyTorch supplies device memory and the current stream.
 
 Importing this module loads the compiled library and raises if it is missing:
-there is no fallback implementation.
+there is no fallback implementation.  TPMLP_LIBRARY=debug (read at import)
+loads libtpmlp_debug.so instead, the build whose GEMM kernels bounds-check every
+tile access and report a failed check as ERR_DEVICE in the status word.
 """
 from __future__ import annotations
 
@@ -13,7 +15,8 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libtpmlp.so")
+LIB_PATH = os.path.join(_HERE, "libtpmlp_debug.so" if os.environ.get("TPMLP_LIBRARY") == "debug"
+                        else "libtpmlp.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(6)
 F32, BF16 = 0, 1
@@ -63,8 +66,9 @@ class TpmlpError(RuntimeError):
 
 def _load():
     if not os.path.exists(LIB_PATH):
-        raise ImportError("libtpmlp.so is not built (expected at %s); run "
-                          "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+        raise ImportError("%s is not built (expected at %s); run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`"
+                          % (os.path.basename(LIB_PATH), LIB_PATH))
     lib = ctypes.CDLL(LIB_PATH)
     vp, sz, i32, i64, u64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64
     SP = ctypes.POINTER(Shape)

@@ -49,6 +49,16 @@ def test_every_declared_symbol_is_exported(tp):
     assert not missing, missing
 
 
+def test_debug_build_exports_the_same_symbols(tp):
+    """libtpmlp_debug.so (the bounds-checked build, TPMLP_LIBRARY=debug) is built
+    beside the library and exports every declared entry point too."""
+    from tensor_transformer_mlp_tma_gb300 import build
+    assert os.path.exists(build.LIB_DEBUG)
+    lib = ctypes.CDLL(build.LIB_DEBUG)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
 def test_status_strings(tp):
     for s in range(6):
         assert tp.status_string(s)

@@ -40,18 +40,43 @@ def test_tensor_core_path_matches_oracle(T, h, F, t):
 
 
 @pytest.mark.parametrize("env", [{"TPMLP_CTA_PAIR": "0"}, {"TPMLP_MN4": "0"}, {"TPMLP_RASTER": "n:3"},
-                                 {"TPMLP_RASTER": "m:1", "TPMLP_CTA_PAIR": "0"}, {"TPMLP_PDL": "0"}])
+                                 {"TPMLP_RASTER": "m:1", "TPMLP_CTA_PAIR": "0"}, {"TPMLP_PDL": "0"},
+                                 {"TPMLP_WIDE": "0"}, {"TPMLP_WIDE_TAIL": "0"}, {"TPMLP_MAX_UNITS": "4"},
+                                 {"TPMLP_MAX_UNITS": "3", "TPMLP_RASTER": "n:2"},
+                                 {"TPMLP_MAX_UNITS": "2", "TPMLP_WIDE_TAIL": "0", "TPMLP_MN4": "0"}])
 @pytest.mark.parametrize("T,h,F,t", [(300, 384, 1280, 2), (257, 512, 1024, 4)])
 def test_tuning_knobs_keep_parity(T, h, F, t, env, monkeypatch):
     """The library's tuning knobs (single-CTA 128 x 256 tiles, per-block maps
     for MN-major operands, forced tile orders, launches without programmatic
-    dependence) change the schedule, not the result."""
+    dependence, 256 x 256 instead of 256 x 512 tiles, the wide tiles' last wave
+    kept whole, few persistent units so that each runs several wide tiles and
+    split half-width tiles in one launch) change the schedule, not the result."""
     for k, v in env.items():
         monkeypatch.setenv(k, v)
     inp = inputs.make(T, h, F, "bf16", seed=T + h + len(env), std=STD)
     out, _ = run_gpu(inp, t)
     ref = oracle.forward_backward(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], inp["dZ"], t)
     compare_full(out, ref, TOL_BF16)
+
+
+@pytest.mark.parametrize("T,h,F,t", [(300, 384, 1280, 2), (1000, 1024, 4096, 4)])
+def test_wide_and_square_tiles_agree(T, h, F, t, monkeypatch):
+    """256 x 512 tiles (default) against 256 x 256 tiles (TPMLP_WIDE=0): both
+    within tolerance of the oracle, and within bf16 rounding of each other.
+    The two accumulate every output element over k in the same order with the
+    same MMA shape, so they are expected to agree bit for bit; the test
+    reports whether they do but requires only the tolerance."""
+    inp = inputs.make(T, h, F, "bf16", seed=T + 5 * t, std=STD)
+    ref = oracle.forward_backward(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], inp["dZ"], t)
+    wide, _ = run_gpu(inp, t)
+    compare_full(wide, ref, TOL_BF16)
+    monkeypatch.setenv("TPMLP_WIDE", "0")
+    square, _ = run_gpu(inp, t)
+    compare_full(square, ref, TOL_BF16)
+    same = {k: bool(torch.equal(wide[k].view(torch.int16), square[k].view(torch.int16)))
+            for k in ("H", "Y", "Z", "dY", "dX", "dA", "da", "dB", "db")}
+    print("wide vs 256 x 256 bit-identical:", same)
+    compare_full(wide, {k: to_np(v) for k, v in square.items() if k in TOL_BF16}, TOL_BF16)
 
 
 def test_fp32_workload_matches_oracle():
@@ -214,7 +239,8 @@ def test_recompute_matches_oracle_and_plain_mode(T, h, F, t, algo):
     compare_full({"dB": rec["dB"]}, {"dB": to_np(plain["dB"])}, {"dB": 2e-2})
 
 
-FULL = [("h2048", 1), ("h2048", 2), ("h2048", 4), ("h4096", 8), ("h8192", 8), ("h12288-b1", 8)]
+FULL = [("h2048", 1), ("h2048", 2), ("h2048", 4), ("h4096", 8), ("h8192", 8), ("h12288-b1", 8),
+        ("h12288-b2", 8), ("h12288-b4", 8), ("h12288-b8", 8)]
 
 
 @pytest.mark.parametrize("name,t", [("h8192", 8)])
@@ -226,7 +252,8 @@ def test_full_size_recompute_slices(name, t):
     R = sample_indices(T, 32, seed=3, must=(0, T - 1))
     J = sample_indices(F, 96, seed=4, must=[0, F - 1] + [i * (F // t) for i in range(t)])
     ref = oracle.slice_(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], inp["dZ"], t, R, J)
-    compare_slices(out, ref, R, J, TOL_BF16)
+    errs = compare_slices(out, ref, R, J, TOL_BF16)
+    print("%s t=%d slice errors: %s" % (name, t, " ".join("%s=%.2e" % kv for kv in sorted(errs.items()))))
 
 
 @pytest.mark.parametrize("name,t", FULL)
@@ -244,4 +271,5 @@ def test_full_size_workload_slices(name, t):
     R = sample_indices(T, 48, seed=1, must=(0, 127, 128, T - 1))
     J = sample_indices(F, 192, seed=2, must=[0, 255, 256, F - 1] + [i * Fs for i in range(t)])
     ref = oracle.slice_(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], inp["dZ"], t, R, J)
-    compare_slices(out, ref, R, J, TOL_BF16)
+    errs = compare_slices(out, ref, R, J, TOL_BF16)
+    print("%s t=%d slice errors: %s" % (name, t, " ".join("%s=%.2e" % kv for kv in sorted(errs.items()))))
