@@ -441,18 +441,15 @@ tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_sa
     // Under recomputation the GeLU' epilogue rebuilds Y = GeLU(H) into the workspace.
     void *Y = rec ? static_cast<void *>(ws + y_offset(s)) : saved->Y;
 
-    // db = column sums of dZ: on tensor cores from the dB GEMM's ones tile (below),
-    // on the FFMA path a two-pass column sum.
+    // db = column sums of dZ: on tensor cores from the dB GEMM's ones tile (below,
+    // its block of ones is filled by the da pass), on the FFMA path a two-pass
+    // column sum.
     void *ones = ws + ones_offset(s);
     cudaError_t e = cudaSuccess;
-    if (use_tc(s)) {
-        Timed timed("fill_ones", st);
-        e = tpmlp::launch_fill_ones_bf16(ones, 64 * 64, st);
-        if (e == cudaSuccess) g_launches.fetch_add(1);
-    } else {
+    if (!use_tc(s)) {
         e = colsum(s, "colsum_db", dZ, T, h, partials, db, st);
+        if (e != cudaSuccess) return from_cuda(e);
     }
-    if (e != cudaSuccess) return from_cuda(e);
 
     // dY = (dZ B^T) * GeLU'(H)
     GemmArgs g3 = base_args(status);
@@ -471,7 +468,7 @@ tpmlp_status tpmlp_backward(const tpmlp_shape *s, const void *dZ, const tpmlp_sa
     // two-pass column sum of dY on the FFMA path.
     if (use_tc(s)) {
         Timed timed("da_block_sum", st);
-        e = tpmlp::launch_colsum_final(true, partials, (T + 31) / 32, F, da, st);
+        e = tpmlp::launch_colsum_final(true, partials, (T + 31) / 32, F, da, st, ones);
         if (e == cudaSuccess) g_launches.fetch_add(1);
     } else {
         e = colsum(s, "colsum_da", dY, T, F, partials, da, st);

@@ -16,6 +16,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "kernels.h"
@@ -124,9 +125,21 @@ __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16 *p, int64
 // The chunk partials of a column are added in ascending order.  They are loaded
 // 16 at a time before being added (same order), so a thread keeps 16 loads in
 // flight instead of waiting one memory round trip per chunk.
+//
+// `ones` (optional, 8 KiB, 16-byte aligned): block 0 also fills it with bf16 ones
+// (the A operand of the bias-gradient tile of the GEMM that follows), which
+// saves that GEMM's input its own launch.  Launched with programmatic stream
+// serialisation it waits for the previous kernel's grid before reading, and lets
+// the next kernel start its set-up at once.
 template <typename T>
 __global__ void __launch_bounds__(256) final_kernel(const float *__restrict__ part, int64_t chunks,
-                                                    int64_t cols, T *__restrict__ out) {
+                                                    int64_t cols, T *__restrict__ out, uint4 *__restrict__ ones) {
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+    if (ones && blockIdx.x == 0) {
+        const uint32_t two = 0x3F803F80u;  // two bf16 ones
+        for (int i = threadIdx.x; i < 64 * 64 * 2 / 16; i += blockDim.x) ones[i] = make_uint4(two, two, two, two);
+    }
     const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (c >= cols) return;
     constexpr int U = 16;
@@ -158,7 +171,7 @@ static cudaError_t launch_t(const T *x, int64_t rows, int64_t cols, float *part,
         partial_kernel<T, 1><<<grid, dim3(BX, BY), 0, st>>>(x, rows, cols, rpc, part);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    final_kernel<T><<<static_cast<unsigned>((cols + 255) / 256), 256, 0, st>>>(part, chunks, cols, out);
+    final_kernel<T><<<static_cast<unsigned>((cols + 255) / 256), 256, 0, st>>>(part, chunks, cols, out, nullptr);
     if (launches) *launches += 2;
     return cudaGetLastError();
 }
@@ -187,15 +200,25 @@ cudaError_t launch_colsum(bool is_bf16, const void *x, int64_t rows, int64_t col
 }
 
 cudaError_t launch_colsum_final(bool is_bf16, const float *partials, int64_t chunks, int64_t cols, void *out,
-                                cudaStream_t st) {
+                                cudaStream_t st, void *ones) {
     if (cols <= 0) return cudaSuccess;
-    const unsigned grid = static_cast<unsigned>((cols + 255) / 256);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((cols + 255) / 256), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    const char *pdl_env = std::getenv("TPMLP_PDL");
+    if (!(pdl_env && pdl_env[0] == '0')) {
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    uint4 *o = static_cast<uint4 *>(ones);
     if (is_bf16)
-        colsum::final_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(partials, chunks, cols,
-                                                                  static_cast<__nv_bfloat16 *>(out));
-    else
-        colsum::final_kernel<float><<<grid, 256, 0, st>>>(partials, chunks, cols, static_cast<float *>(out));
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, colsum::final_kernel<__nv_bfloat16>, partials, chunks, cols,
+                                  static_cast<__nv_bfloat16 *>(out), o);
+    return cudaLaunchKernelEx(&cfg, colsum::final_kernel<float>, partials, chunks, cols, static_cast<float *>(out), o);
 }
 
 // ---------------------------------------------------------------- ones block

@@ -96,8 +96,9 @@ cudaError_t launch_colsum(bool is_bf16, const void *x, int64_t rows, int64_t col
                           void *out, cudaStream_t st, int *launches);
 
 // Second pass alone: out[c] = sum over `chunks` rows of partials[k, c], in order.
+// `ones` (optional): an 8 KiB block the kernel also fills with bf16 ones.
 cudaError_t launch_colsum_final(bool is_bf16, const float *partials, int64_t chunks, int64_t cols, void *out,
-                                cudaStream_t st);
+                                cudaStream_t st, void *ones = nullptr);
 
 // A kernel that waits on a barrier nothing arrives on and reports the timeout.
 cudaError_t launch_timeout_probe(uint32_t *status, uint64_t wait_ns, cudaStream_t st);
