@@ -41,13 +41,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch of each tensor-core GEMM, from one ncu
 # capture, with the hash of the kernel source they were taken at.  A kernel whose
 # source has changed since reports traffic null.
-NCU_TRAFFIC = {  # profiles/dram_traffic_h8192_gemms.md (h8192 workload)
-    "fc1_bias_gelu": (1.943519e9 + 0.519111e9, "32d5816d0a52"),
-    "fc2_shard_fold": (2.203810e9 + 0.081232e9, "32d5816d0a52"),
-    "bwd_dY_dgelu": (2.517340e9 + 0.274451e9, "32d5816d0a52"),
-    "bwd_dB": (0.998947e9 + 0.515716e9, "32d5816d0a52"),
-    "bwd_dA": (0.982707e9 + 0.515046e9, "32d5816d0a52"),
-    "bwd_dX_shard_fold": (2.210045e9 + 0.076435e9, "32d5816d0a52"),
+NCU_TRAFFIC = {  # profiles/dram_traffic_h8192_gemms.md (h8192 workload, one kernel per capture)
+    "fc1_bias_gelu": (1.939918e9 + 0.520595e9, "ff4d7279796d"),
+    "fc2_shard_fold": (2.203393e9 + 0.085052e9, "ff4d7279796d"),
+    "bwd_dY_dgelu": (2.346733e9 + 0.278225e9, "ff4d7279796d"),
+    "bwd_dB": (1.139484e9 + 0.514869e9, "ff4d7279796d"),
+    "bwd_dA": (1.425699e9 + 0.515096e9, "ff4d7279796d"),
+    "bwd_dX_shard_fold": (2.198976e9 + 0.079511e9, "ff4d7279796d"),
 }
 
 
