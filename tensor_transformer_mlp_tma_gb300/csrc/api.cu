@@ -883,14 +883,15 @@ tpmlp_status tpmlp_attn_forward(const tpmlp_attn_shape *s, const void *X, const 
     const tpmlp::HeadView qv = qkv_view(s), tv = tok_view(s);
     const void *Qp = qkv_part(saved->QKV, s, 0), *Kp = qkv_part(saved->QKV, s, 1), *Vp = qkv_part(saved->QKV, s, 2);
 
-    // Column-parallel projection of all shards: QKV = X Wqkv + bqkv.
+    // Column-parallel projection of all shards: QKV = X Wqkv + bqkv (the bias
+    // epilogue without an activation, on 256 x 512 tiles).
     GemmArgs g1 = base_args(status);
     g1.a = X, g1.a_mn = false;     // X[T,h]: K-major
     g1.b = Wqkv, g1.b_mn = true;   // Wqkv[h,3h]: MN-major
     g1.M = T, g1.N = 3 * h, g1.K = h, g1.kshard = h;
-    g1.out0 = saved->QKV, g1.bias = bqkv;
-    pick_raster(g1);
-    cudaError_t e = gemm(&ms, "attn_qkv_proj", tpmlp::EPI_FOLD_BIAS, g1, sms, st);
+    g1.out0 = saved->QKV, g1.out1 = nullptr, g1.bias = bqkv;
+    pick_raster(g1, tpmlp::EPI_BIAS_GELU);
+    cudaError_t e = gemm(&ms, "attn_qkv_proj", tpmlp::EPI_BIAS_GELU, g1, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
     // Scores of every head: scale * Q K^T, causal; Q and K read in place in QKV.
@@ -970,15 +971,9 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
     const float scale = 1.0f / std::sqrt(static_cast<float>(d));
 
     // dbo = 1^T dZ and dbqkv = 1^T dQKV come from the ones tiles of the dWo and
-    // dWqkv GEMMs.
+    // dWqkv GEMMs; the row-dot pass, which runs before both, fills the ones.
     void *ones = ws + L.ones;
     cudaError_t e;
-    {
-        Timed timed("attn_fill_ones", st);
-        e = tpmlp::launch_fill_ones_bf16(ones, 64 * 64, st);
-        if (e != cudaSuccess) return from_cuda(e);
-        g_launches.fetch_add(1);
-    }
 
     // dO = dZ Wo^T (every shard's columns at once; no fold needed)
     GemmArgs g1 = base_args(status);
@@ -986,9 +981,17 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
     g1.b = saved->Wo, g1.b_mn = false;  // Wo[h,h] as [N, K]: K-major
     g1.M = T, g1.N = h, g1.K = h, g1.kshard = h;
     g1.out0 = dO;
-    pick_raster(g1);
-    e = gemm(&ms, "attn_bwd_dO", tpmlp::EPI_FOLD, g1, sms, st);
+    pick_raster(g1, tpmlp::EPI_STORE);
+    e = gemm(&ms, "attn_bwd_dO", tpmlp::EPI_STORE, g1, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
+
+    // D = rowsum(dO * O) per head (and the block of ones)
+    {
+        Timed timed("attn_bwd_rowdot", st);
+        e = tpmlp::launch_rowdot(head_layout(s), dO, saved->O, D, st, ones);
+        if (e != cudaSuccess) return from_cuda(e);
+        g_launches.fetch_add(1);
+    }
 
     // dWo = O^T dZ
     GemmArgs g2 = base_args(status);
@@ -1001,12 +1004,6 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
     e = gemm(&ms, "attn_bwd_dWo", tpmlp::EPI_STORE, g2, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
 
-    {
-        Timed timed("attn_bwd_rowdot", st);
-        e = tpmlp::launch_rowdot(head_layout(s), dO, saved->O, D, st);
-        if (e != cudaSuccess) return from_cuda(e);
-        g_launches.fetch_add(1);
-    }
 
     // dV_head = P^T dO_head
     GemmArgs g3 = head_gemm(status, saved->P, true, dO, true, S, d, S, nz, dVp);

@@ -32,25 +32,17 @@ __device__ __forceinline__ int64_t write_end(int64_t row, int64_t S, int64_t wti
     return wtile > 0 ? min(S, (row % S / wtile + 1) * wtile) : S;
 }
 
-// One warp per score row.  Row r of a head (r = row % S) sees columns 0..r; the
-// others are written as exact zeros (up to write_end).  Max-subtracted
-// exponentials (the fast __expf), fp32 sum.  The row is read once, 16 bytes per lane at a time,
-// into V float4 registers per lane (S <= 128 V); only the columns up to the
-// diagonal are read.
-template <int V>
-__global__ void __launch_bounds__(256)
-    softmax_reg_kernel(const float *__restrict__ S_, __nv_bfloat16 *__restrict__ P, int64_t rows, int64_t S,
-                       bool causal, int64_t wtile) {
-    const int lane = threadIdx.x & 31;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-    if (row >= rows) return;
-    const int64_t last = causal ? row % S : S - 1;
-    const int64_t wend = write_end(row, S, wtile);
-    const float4 *in = reinterpret_cast<const float4 *>(S_ + row * S);
-    float4 x[V];
+// One score row, held in U float4 registers per lane: row r of a head (r = row %
+// S) sees columns 0..last; the others are written as exact zeros (up to wend).
+// Max-subtracted exponentials (the fast __expf), fp32 sum.  The row is read once,
+// 16 bytes per lane at a time; only the columns up to the diagonal are read.
+template <int U>
+__device__ __forceinline__ void softmax_row(const float4 *__restrict__ in, uint2 *__restrict__ out, int64_t last,
+                                            int64_t wend, int lane) {
+    float4 x[U];
     float mx = -INFINITY;
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
+    for (int v = 0; v < U; ++v) {
         const int64_t c = 4 * (lane + 32 * v);
         if (c <= last) {
             x[v] = __ldcs(in + lane + 32 * v);  // streamed: read once
@@ -65,7 +57,7 @@ __global__ void __launch_bounds__(256)
     mx = warp_max(mx);
     float sum = 0.0f;
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
+    for (int v = 0; v < U; ++v) {
         // the fast exponential (its error is far below P's bf16 rounding);
         // exp(-inf) = 0 for the masked columns
         x[v].x = __expf(x[v].x - mx);
@@ -76,9 +68,8 @@ __global__ void __launch_bounds__(256)
     }
     sum = warp_sum(sum);
     const float inv = 1.0f / sum;
-    uint2 *out = reinterpret_cast<uint2 *>(P + row * S);
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
+    for (int v = 0; v < U; ++v) {
         const int64_t c = 4 * (lane + 32 * v);
         if (c < wend) {  // wend is a multiple of 4
             __nv_bfloat162 lo = __floats2bfloat162_rn(x[v].x * inv, x[v].y * inv);
@@ -89,6 +80,38 @@ __global__ void __launch_bounds__(256)
             out[lane + 32 * v] = w;
         }
     }
+    // columns past the U slots, all past the diagonal, up to wend: zeros
+    for (int64_t c = 4 * (lane + 32 * U); c < wend; c += 128) out[c / 4] = make_uint2(0u, 0u);
+}
+
+// One warp per score row, for rows of up to 128 V columns.  A causal row r needs
+// only its first r + 1 columns, so each warp runs the smallest of four unrolled
+// bodies (V/4, V/2, 3V/4 or V float4 registers per lane) that covers them: the
+// choice is uniform over the warp, and the slots it leaves out would only have
+// added exp(-inf) = +0.0 to the sum and -inf to the max, so P is the same, bit
+// for bit.  On average it halves the exponentials and the arithmetic of a causal
+// softmax.
+template <int V>
+__global__ void __launch_bounds__(256, V <= 16 ? 3 : 1)  // 24 warps per SM up to 2048 columns
+    softmax_reg_kernel(const float *__restrict__ S_, __nv_bfloat16 *__restrict__ P, int64_t rows, int64_t S,
+                       bool causal, int64_t wtile) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int64_t last = causal ? row % S : S - 1;
+    const int64_t wend = write_end(row, S, wtile);
+    const float4 *in = reinterpret_cast<const float4 *>(S_ + row * S);
+    uint2 *out = reinterpret_cast<uint2 *>(P + row * S);
+    const int64_t need = last / 128 + 1;  // float4 slots per lane up to the diagonal
+    constexpr int V1 = V / 4 > 0 ? V / 4 : 1, V2 = V / 2 > V1 ? V / 2 : V1, V3 = 3 * V / 4 > V2 ? 3 * V / 4 : V2;
+    if (need <= V1)
+        softmax_row<V1>(in, out, last, wend, lane);
+    else if (need <= V2)
+        softmax_row<V2>(in, out, last, wend, lane);
+    else if (need <= V3)
+        softmax_row<V3>(in, out, last, wend, lane);
+    else
+        softmax_row<V>(in, out, last, wend, lane);
 }
 
 // Rows longer than the register version holds: the same arithmetic with three
@@ -137,9 +160,18 @@ __device__ __forceinline__ float dot8(const uint4 va, const uint4 vb) {
 // flight each) stay resident per SM.
 constexpr int ROWDOT_THREADS = 128;
 constexpr int ROWDOT_UNROLL = 2;
+__device__ __forceinline__ void fill_ones_block(uint4 *ones) {
+    // the 64 x 64 bf16 ones (8 KiB) that the dWo and dWqkv GEMMs' bias-gradient
+    // tiles read, written by block 0 so that they need no launch of their own
+    if (ones && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < 64 * 64 * 2 / 16; i += blockDim.x)
+            ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+}
+
 __global__ void __launch_bounds__(ROWDOT_THREADS)
     rowdot_row_kernel(const HeadLayout L, const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ b,
-                      float *__restrict__ D) {
+                      float *__restrict__ D, uint4 *__restrict__ ones) {
+    fill_ones_block(ones);
     const int r = static_cast<int>(blockIdx.x), S = static_cast<int>(L.S);
     const int chunks = static_cast<int>(L.h / 8);
     const int G = static_cast<int>(L.d / 8);
@@ -170,7 +202,8 @@ __global__ void __launch_bounds__(ROWDOT_THREADS)
 // One warp per (token r, head g), for any d that is a multiple of 8.
 __global__ void __launch_bounds__(256)
     rowdot_kernel(const HeadLayout L, const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ b,
-                  float *__restrict__ D) {
+                  float *__restrict__ D, uint4 *__restrict__ ones) {
+    fill_ones_block(ones);
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     if (row >= L.nb * L.S * L.heads) return;
@@ -204,17 +237,19 @@ cudaError_t launch_softmax(const float *S, void *P, int64_t rows, int64_t cols, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_rowdot(const HeadLayout &L, const void *a, const void *b, float *D, cudaStream_t st) {
+cudaError_t launch_rowdot(const HeadLayout &L, const void *a, const void *b, float *D, cudaStream_t st, void *ones) {
     const int64_t rows = L.nb * L.S * L.heads;
     if (rows <= 0) return cudaSuccess;
     const int64_t G = L.d / 8;
     if (G >= 1 && G <= 32 && (G & (G - 1)) == 0) {
         attn::rowdot_row_kernel<<<static_cast<unsigned>(L.nb * L.S), attn::ROWDOT_THREADS, 0, st>>>(
-            L, static_cast<const __nv_bfloat16 *>(a), static_cast<const __nv_bfloat16 *>(b), D);
+            L, static_cast<const __nv_bfloat16 *>(a), static_cast<const __nv_bfloat16 *>(b), D,
+            static_cast<uint4 *>(ones));
         return cudaGetLastError();
     }
     attn::rowdot_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
-        L, static_cast<const __nv_bfloat16 *>(a), static_cast<const __nv_bfloat16 *>(b), D);
+        L, static_cast<const __nv_bfloat16 *>(a), static_cast<const __nv_bfloat16 *>(b), D,
+        static_cast<uint4 *>(ones));
     return cudaGetLastError();
 }
 

@@ -221,20 +221,6 @@ cudaError_t launch_colsum_final(bool is_bf16, const float *partials, int64_t chu
     return cudaLaunchKernelEx(&cfg, colsum::final_kernel<float>, partials, chunks, cols, static_cast<float *>(out), o);
 }
 
-// ---------------------------------------------------------------- ones block
-__global__ void fill_ones_kernel(uint4 *p, int64_t n16) {
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const uint32_t two = 0x3F803F80u;  // two bf16 ones
-    if (i < n16) p[i] = make_uint4(two, two, two, two);
-}
-
-cudaError_t launch_fill_ones_bf16(void *p, int64_t n, cudaStream_t st) {
-    const int64_t n16 = n / 8;
-    if (n16 <= 0) return cudaSuccess;
-    fill_ones_kernel<<<static_cast<unsigned>((n16 + 255) / 256), 256, 0, st>>>(static_cast<uint4 *>(p), n16);
-    return cudaGetLastError();
-}
-
 // ---------------------------------------------------------------- timeout probe
 // One warp allocates 32 TMEM columns (so the release path is exercised too),
 // waits on a barrier that never completes for at most wait_ns, records the

@@ -8,7 +8,7 @@ namespace tpmlp {
 
 // Epilogues of the GEMM kernels.  Each names the step of the MLP it finishes.
 enum Epi : int {
-    EPI_BIAS_GELU = 0,  // H = acc + a (optional store), Y = GeLU(H)        -- column-parallel GEMM
+    EPI_BIAS_GELU = 0,  // H = acc + a (optional store), Y = GeLU(H) (optional) -- column-parallel GEMM
     EPI_FOLD_BIAS = 1,  // Z = b + ((Z_1 + Z_2) + ...)                      -- row-parallel GEMM
     EPI_DGELU = 2,      // dY = acc * GeLU'(H)                              -- dZ B^T
     EPI_STORE = 3,      // out = acc                                       -- dB, dA
@@ -43,7 +43,7 @@ struct GemmArgs {
     int nshards;
     int64_t kshard;
     void *out0;        // H / Z / dY / dB / dA / dX
-    void *out1;        // Y for EPI_BIAS_GELU; Y rebuilt from H for EPI_DGELU (optional)
+    void *out1;        // Y for EPI_BIAS_GELU (null: no activation); Y rebuilt from H for EPI_DGELU (optional)
     const void *aux;   // H for EPI_DGELU
     const void *bias;  // a for EPI_BIAS_GELU, b for EPI_FOLD_BIAS
     uint32_t *status;  // device status word
@@ -75,15 +75,12 @@ struct GemmArgs {
     HeadView a_view, b_view, o_view;
 };
 
-// Fills n bf16 elements with 1.0 (n a multiple of 8, p 16-byte aligned).
-cudaError_t launch_fill_ones_bf16(void *p, int64_t n, cudaStream_t st);
-
 // Tensor-core path: bf16 operands, fp32 accumulation in TMEM (tcgen05).
 cudaError_t launch_tc_gemm(Epi epi, const GemmArgs &g, int num_sms, cudaStream_t st);
 
 // Whether launch_tc_gemm runs this product on 256 x 512 tiles (CTA pairs; the
-// store, bias + GeLU and GeLU' epilogues of one shard on plain operands) rather
-// than 256 x 256.  TPMLP_WIDE=0 keeps 256 x 256 (a tuning knob, read per call).
+// store (both operands MN-major or both K-major), bias + GeLU and GeLU'
+// epilogues of one shard on plain operands) rather than 256 x 256.  TPMLP_WIDE=0 keeps 256 x 256 (a tuning knob, read per call).
 bool tc_wide_tile(Epi epi, const GemmArgs &g);
 
 // FFMA path: element type fp32 (is_bf16 = false) or bf16, fp32 accumulation.
@@ -132,7 +129,9 @@ struct HeadLayout {
 cudaError_t launch_softmax(const float *S, void *P, int64_t rows, int64_t cols, bool causal, int64_t wtile,
                            cudaStream_t st);
 // D[z*S + s] = row dot of dO and O over head g's columns of token b*S + s (token-major inputs).
-cudaError_t launch_rowdot(const HeadLayout &L, const void *dO, const void *O, float *D, cudaStream_t st);
+// `ones` (optional): an 8 KiB block the kernel also fills with bf16 ones.
+cudaError_t launch_rowdot(const HeadLayout &L, const void *dO, const void *O, float *D, cudaStream_t st,
+                          void *ones = nullptr);
 
 // Records a description of the last failure of this host thread (read back by
 // tpmlp_last_error()).

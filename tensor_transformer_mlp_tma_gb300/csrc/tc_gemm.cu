@@ -509,17 +509,20 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
     bool two = false, store0 = true;
     const CUtensorMap *tm_second = tm1;  // map of the second staged box
     if constexpr (EPI == EPI_BIAS_GELU) {
+        // out0 = acc + bias (unless null); out1 = GeLU of it, or with out1 null
+        // no activation at all (a plain biased projection)
         float bias[32];
         load32(p.bias, col, col, p.N, true, bias);
-        float y[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            v[i] += bias[i];
-            y[i] = gelu_f(v[i]);
-        }
+        for (int i = 0; i < 32; ++i) v[i] += bias[i];
         pack32(v, w0);
-        pack32(y, w1);
-        two = true;
+        if (p.out1 != nullptr) {
+            float y[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) y[i] = gelu_f(v[i]);
+            pack32(y, w1);
+            two = true;
+        }
         store0 = p.out0 != nullptr;
     } else if constexpr (EPI == EPI_DGELU) {
         float hv[32];
@@ -1575,7 +1578,8 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     // The attention scores are fp32 (32 x 32 box, 128-byte swizzle, see stage_row_f32);
     // dS reads P through the second map; both of its maps have 32 x 64 boxes with
     // 128-byte swizzle (see stage_half_row128).
-    const void *o1 = (EPI == EPI_BIAS_GELU) ? g.out1 : ((EPI == EPI_DGELU || EPI == EPI_ATTN_DS) ? g.aux : o0);
+    const void *o1 = (EPI == EPI_BIAS_GELU) ? (g.out1 ? g.out1 : o0)
+                                            : ((EPI == EPI_DGELU || EPI == EPI_ATTN_DS) ? g.aux : o0);
     const void *o2 = (EPI == EPI_DGELU && g.out1) ? g.out1 : o0;
     const bool f32out = EPI == EPI_ATTN_SCORE;
     const bool wide = EPI == EPI_ATTN_DS;
@@ -1693,9 +1697,13 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
 
 template <int EPI, bool A_MN, bool B_MN>
 static cudaError_t launch_cg(const GemmArgs &g, int num_sms, cudaStream_t st) {
-    if constexpr (EPI == EPI_BIAS_GELU || EPI == EPI_DGELU || (EPI == EPI_STORE && A_MN && B_MN)) {
+    if constexpr (EPI == EPI_BIAS_GELU || EPI == EPI_DGELU || (EPI == EPI_STORE && A_MN == B_MN)) {
         if (tc_wide_tile(static_cast<Epi>(EPI), g)) return launch_t<EPI, A_MN, B_MN, 2, false, 512>(g, num_sms, st);
     }
+    if constexpr (EPI == EPI_STORE && !A_MN && !B_MN) {
+        // plain products of two K-major operands (the attention's dO = dZ Wo^T)
+        return g.cta_pair ? launch_t<EPI, false, false, 2>(g, num_sms, st) : launch_t<EPI, false, false, 1>(g, num_sms, st);
+    } else {
     if constexpr (EPI == EPI_ATTN_SCORE || EPI == EPI_ATTN_DS || EPI == EPI_STORE) {
         if (g.heads_layout) {
             // Outputs at most 128 wide (the per-head products with N = d) take the
@@ -1711,13 +1719,14 @@ static cudaError_t launch_cg(const GemmArgs &g, int num_sms, cudaStream_t st) {
         }
     }
     return g.cta_pair ? launch_t<EPI, A_MN, B_MN, 2>(g, num_sms, st) : launch_t<EPI, A_MN, B_MN, 1>(g, num_sms, st);
+    }
 }
 
 }  // namespace tc
 
 bool tc_wide_tile(Epi epi, const GemmArgs &g) {
     if (!g.cta_pair || g.heads_layout || g.nshards != 1 || g.causal_k != 0 || g.skip_upper) return false;
-    if (!(epi == EPI_BIAS_GELU || epi == EPI_DGELU || (epi == EPI_STORE && g.a_mn && g.b_mn))) return false;
+    if (!(epi == EPI_BIAS_GELU || epi == EPI_DGELU || (epi == EPI_STORE && g.a_mn == g.b_mn))) return false;
     const char *w = std::getenv("TPMLP_WIDE");
     return !(w && w[0] == '0');
 }
@@ -1735,9 +1744,11 @@ cudaError_t launch_tc_gemm(Epi epi, const GemmArgs &g, int num_sms, cudaStream_t
         case EPI_DGELU:  // dZ[T,h] (K-major) . B[F,h]^T (K-major)
             if (!g.a_mn && !g.b_mn) return launch_cg<EPI_DGELU, false, false>(g, num_sms, st);
             break;
-        case EPI_STORE:  // Y^T . dZ and X^T . dY: both operands MN-major; P . V: K-major . MN-major
+        case EPI_STORE:  // Y^T . dZ and X^T . dY: both operands MN-major; P . V: K-major . MN-major;
+                         // dZ . Wo^T: both K-major
             if (g.a_mn && g.b_mn) return launch_cg<EPI_STORE, true, true>(g, num_sms, st);
             if (!g.a_mn && g.b_mn) return launch_cg<EPI_STORE, false, true>(g, num_sms, st);
+            if (!g.a_mn && !g.b_mn) return launch_cg<EPI_STORE, false, false>(g, num_sms, st);
             break;
         case EPI_ATTN_SCORE:  // Q[S,d] (K-major) . K[S,d]^T (K-major), per head
             if (!g.a_mn && !g.b_mn) return launch_cg<EPI_ATTN_SCORE, false, false>(g, num_sms, st);

@@ -241,6 +241,24 @@ def test_wide_tiles_match_oracle(tp, monkeypatch):
     assert not bad, "outside tolerance: %s (all: %s)" % (bad, errs)
 
 
+def test_projections_on_square_tiles_match_wide(tp, monkeypatch):
+    """The QKV projection (bias, no activation), dO = dZ Wo^T (two K-major
+    operands), dWo and dWqkv run on 256 x 512 tiles by default; TPMLP_WIDE=0
+    runs them on 256 x 256 tiles.  Both match the oracle, and each output
+    element is accumulated over k in the same order by the same MMA shape, so
+    the two give the same bits."""
+    nb, S, h, heads, t = 2, 264, 1024, 8, 4
+    inp, wide, _ = run_attn(tp, nb, S, h, heads, t, seed=31)
+    ref = oracle_ref(inp, nb, heads, t)
+    for out in (wide,):
+        errs = {k: rel(to_np(out[k]), ref[k]) for k in TOL}
+        assert all(v <= TOL[k] for k, v in errs.items()), errs
+    monkeypatch.setenv("TPMLP_WIDE", "0")
+    _, square, _ = run_attn(tp, nb, S, h, heads, t, seed=31)
+    for k in TOL:
+        assert torch.equal(wide[k], square[k]), k
+
+
 @pytest.mark.parametrize("pair", ["1", "0"])
 def test_p_upper_tiles_flag(tp, pair, monkeypatch):
     """TPMLP_ATTN_P_UPPER_ZERO leaves the 256 x 256 tiles of P wholly above the
