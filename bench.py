@@ -42,12 +42,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, with the hash of the kernel source they were taken at.  A kernel whose
 # source has changed since reports traffic null.
 NCU_TRAFFIC = {  # profiles/dram_traffic_h8192_gemms.md (h8192 workload, one kernel per capture)
-    "fc1_bias_gelu": (1.939918e9 + 0.520595e9, "ff4d7279796d"),
-    "fc2_shard_fold": (2.203393e9 + 0.085052e9, "ff4d7279796d"),
-    "bwd_dY_dgelu": (2.346733e9 + 0.278225e9, "ff4d7279796d"),
-    "bwd_dB": (1.139484e9 + 0.514869e9, "ff4d7279796d"),
-    "bwd_dA": (1.425699e9 + 0.515096e9, "ff4d7279796d"),
-    "bwd_dX_shard_fold": (2.198976e9 + 0.079511e9, "ff4d7279796d"),
+    "fc1_bias_gelu": (1.950668e9 + 0.520329e9, "58a3777731bc"),
+    "fc2_shard_fold": (2.203338e9 + 0.083478e9, "58a3777731bc"),
+    "bwd_dY_dgelu": (2.346407e9 + 0.278198e9, "58a3777731bc"),
+    "bwd_dB": (1.099863e9 + 0.515223e9, "58a3777731bc"),
+    "bwd_dA": (1.398121e9 + 0.514170e9, "58a3777731bc"),
+    "bwd_dX_shard_fold": (2.200872e9 + 0.079927e9, "58a3777731bc"),
 }
 
 

@@ -35,6 +35,18 @@ __device__ __forceinline__ void st<__nv_bfloat16>(__nv_bfloat16 *p, int64_t i, f
     p[i] = __float2bfloat16_rn(v);
 }
 
+// v rounded to T and back (round to nearest even), i.e. the value stored as T.
+template <typename T>
+__device__ __forceinline__ float rounded(float v);
+template <>
+__device__ __forceinline__ float rounded<float>(float v) {
+    return v;
+}
+template <>
+__device__ __forceinline__ float rounded<__nv_bfloat16>(float v) {
+    return __bfloat162float(__float2bfloat16_rn(v));
+}
+
 __device__ __forceinline__ float gelu_exact_tanh(float x) {
     const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
     return 0.5f * x * (1.0f + tanhf(u));
@@ -144,9 +156,12 @@ __global__ void __launch_bounds__(256) gemm_kernel(const Params p) {
             const int64_t o = m * p.N + n;
             float v = sum[i][j];
             if constexpr (EPI == EPI_BIAS_GELU) {
+                // Y is GeLU of H as stored (rounded to T), the value the
+                // backward's recomputation rebuilds from the saved H
                 v += ld<T>(static_cast<const T *>(p.bias), n);
-                if (p.out0) st<T>(static_cast<T *>(p.out0), o, v);
-                st<T>(static_cast<T *>(p.out1), o, gelu_exact_tanh(v));
+                const float h = rounded<T>(v);
+                if (p.out0) st<T>(static_cast<T *>(p.out0), o, h);
+                if (p.out1) st<T>(static_cast<T *>(p.out1), o, gelu_exact_tanh(h));
             } else if constexpr (EPI == EPI_FOLD_BIAS) {
                 st<T>(static_cast<T *>(p.out0), o, v + ld<T>(static_cast<const T *>(p.bias), n));
             } else if constexpr (EPI == EPI_DGELU) {

@@ -481,6 +481,16 @@ __device__ __forceinline__ void store_bias_grad(const Params &p, int col, const 
         if (col + i < p.N) out[col + i] = __float2bfloat16_rn(v[i]);
 }
 
+// y = GeLU(h) for 32 bf16 values packed in pairs (fp32 arithmetic, bf16 result).
+__device__ __forceinline__ void gelu_of_packed(const uint32_t (&h)[16], uint32_t (&y)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float a, b;
+        unpack_bf16(h[i], a, b);
+        y[i] = pack_bf16(gelu_f(a), gelu_f(b));
+    }
+}
+
 template <int EPI, bool HEADS = false>
 __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap *tm0, const CUtensorMap *tm1,
                                              const CUtensorMap *tm2, float (&v)[32], int64_t row, int row0,
@@ -511,16 +521,15 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
     if constexpr (EPI == EPI_BIAS_GELU) {
         // out0 = acc + bias (unless null); out1 = GeLU of it, or with out1 null
         // no activation at all (a plain biased projection)
+        // Y is GeLU of H as stored (rounded to bf16), the same value the
+        // backward's recomputation rebuilds from the saved H.
         float bias[32];
         load32(p.bias, col, col, p.N, true, bias);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] += bias[i];
         pack32(v, w0);
         if (p.out1 != nullptr) {
-            float y[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) y[i] = gelu_f(v[i]);
-            pack32(y, w1);
+            gelu_of_packed(w0, w1);
             two = true;
         }
         store0 = p.out0 != nullptr;

@@ -223,9 +223,9 @@ def test_inference_forward_without_H():
 def test_recompute_matches_oracle_and_plain_mode(T, h, F, t, algo):
     """Activation recomputation (only H kept between the passes, Y rebuilt from H
     in the backward GeLU' epilogue) against the oracle, and against the plain
-    mode: Z, dY, dX, dA, da, db come out of identical arithmetic and must be
-    bit-identical; dB uses the rebuilt Y (GeLU of the stored bf16 H instead of
-    the fp32 pre-activation) and is compared within tolerance."""
+    mode.  The forward computes Y as GeLU of H as stored, which is exactly what
+    the recomputation rebuilds, so every output, dB included, must be
+    bit-identical to the plain mode."""
     from tensor_transformer_mlp_tma_gb300 import tpmlp
     a = tpmlp.ALGO_SIMT if algo == "simt" else tpmlp.ALGO_DEFAULT
     inp = inputs.make(T, h, F, "bf16", seed=T * 3 + t, std=STD)
@@ -234,9 +234,8 @@ def test_recompute_matches_oracle_and_plain_mode(T, h, F, t, algo):
     ref = oracle.forward_backward(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], inp["dZ"], t)
     compare_full(rec, ref, TOL_BF16)
     plain, _ = run_gpu(inp, t, algo=a)
-    for k in ("Z", "H", "dY", "dX", "dA", "da", "db"):
+    for k in ("Z", "H", "Y", "dY", "dX", "dA", "da", "db", "dB"):
         assert torch.equal(rec[k].view(torch.int16), plain[k].view(torch.int16)), k
-    compare_full({"dB": rec["dB"]}, {"dB": to_np(plain["dB"])}, {"dB": 2e-2})
 
 
 FULL = [("h2048", 1), ("h2048", 2), ("h2048", 4), ("h4096", 8), ("h8192", 8), ("h12288-b1", 8),
