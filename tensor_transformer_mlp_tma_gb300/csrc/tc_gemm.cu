@@ -285,16 +285,27 @@ __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
     return n;
 }
 
+// The tanh form of GeLU, with c = sqrt(2/pi) and k = 0.044715:
+//   GeLU(x)  = x/2 (1 + tanh u),  u = c (x + k x^3) = x (c + c k x^2)
+//   GeLU'(x) = (1 + tanh u)/2 + (1 - tanh^2 u) x/2 (c + 3 c k x^2)
+// with the constant products folded, so that each costs a handful of FMAs
+// around the one tanh.
+constexpr float kGeluC = 0.7978845608028654f;           // c
+constexpr float kGeluCK = 0.035677408136300125f;        // c k
+constexpr float kGeluHalfC = 0.3989422804014327f;       // c / 2
+constexpr float kGeluThreeHalfCK = 0.05351611220445019f;  // 3 c k / 2
+
 __device__ __forceinline__ float gelu_f(float x) {
-    const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-    return 0.5f * x * (1.0f + ptx::tanh_approx(u));
+    const float u = x * fmaf(kGeluCK, x * x, kGeluC);
+    const float hx = 0.5f * x;
+    return fmaf(hx, ptx::tanh_approx(u), hx);
 }
 
 __device__ __forceinline__ float gelu_prime_f(float x) {
-    const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-    const float th = ptx::tanh_approx(u);
-    const float du = 0.7978845608028654f * (1.0f + 3.0f * 0.044715f * x * x);
-    return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * du;
+    const float x2 = x * x;
+    const float th = ptx::tanh_approx(x * fmaf(kGeluCK, x2, kGeluC));
+    const float hxdu = x * fmaf(kGeluThreeHalfCK, x2, kGeluHalfC);  // x/2 du/dx
+    return fmaf(fmaf(-th, th, 1.0f), hxdu, fmaf(0.5f, th, 0.5f));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -324,6 +335,27 @@ __device__ __forceinline__ void load8(const void *in, int64_t off, float *v) {
     unpack_bf16(w.y, v[2], v[3]);
     unpack_bf16(w.z, v[4], v[5]);
     unpack_bf16(w.w, v[6], v[7]);
+}
+
+// 32 consecutive bf16 bias values fetched ahead of the chunk that adds them, so
+// that the load's latency overlaps the work before it.  Values past N read as
+// zero (the bias is a row-major vector of N bf16).
+struct BiasPre {
+    uint4 w[4];
+};
+__device__ __forceinline__ void bias_fetch(const void *bias, int col, int N, BiasPre &b) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(bias) + col);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) b.w[g] = col + 8 * g < N ? __ldg(src + g) : make_uint4(0u, 0u, 0u, 0u);
+}
+__device__ __forceinline__ void bias_unpack(const BiasPre &b, float (&v)[32]) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        unpack_bf16(b.w[g].x, v[8 * g], v[8 * g + 1]);
+        unpack_bf16(b.w[g].y, v[8 * g + 2], v[8 * g + 3]);
+        unpack_bf16(b.w[g].z, v[8 * g + 4], v[8 * g + 5]);
+        unpack_bf16(b.w[g].w, v[8 * g + 6], v[8 * g + 7]);
+    }
 }
 
 // Row r of a 32 x 32 bf16 box staged for a 64-byte-swizzled TMA store: 16-byte
@@ -407,46 +439,30 @@ __device__ __forceinline__ void load32(const void *in, int64_t off, int col, int
     }
 }
 
-// Column sums of a warp's 32 x 32 chunk (row = lane, column j = x[j]) by a
-// fixed butterfly: after five exchange-and-add steps lane L holds the sum over
-// the 32 rows of column L.  The summation tree is the same on every run.
-__device__ __forceinline__ float warp_colsum32(const float (&x)[32], int lane) {
-    float a[16];
-    const bool h16 = lane & 16;
+// Column sums of the warp's staged 32 x 32 bf16 box (64-byte swizzle, row r at
+// byte 64 r, 16-byte chunk j of the row at chunk j ^ ((r >> 1) & 3)).  Lane l
+// adds the bf16 pair in word l & 15 of its rows over one half of the box, rows
+// 16 (l >> 4) .. +15 in order, the upper half taking the rows of each pair
+// swapped so that the two halves read disjoint banks.  One exchange then adds
+// the two halves' sums: lane l returns the sum over all 32 rows of column
+// 2 (l & 15) + (l >> 4).  The summation order is the same on every run.
+__device__ __forceinline__ float box_colsum32(uint32_t box, int lane) {
+    const int w = lane & 15, hi = lane >> 4;
+    float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const float send = h16 ? x[i] : x[i + 16];
-        const float keep = h16 ? x[i + 16] : x[i];
-        a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        const int r = 16 * hi + (i ^ hi);
+        const int chunk = (w >> 2) ^ ((i >> 1) & 3);  // (r >> 1) & 3 == (i >> 1) & 3
+        const uint32_t addr = box + static_cast<uint32_t>(r) * 64u + (static_cast<uint32_t>(chunk) << 4) +
+                              (static_cast<uint32_t>(w & 3) << 2);
+        float lo, up;
+        unpack_bf16(ptx::ld_shared_u32(addr), lo, up);
+        s0 += lo;
+        s1 += up;
     }
-    float b[8];
-    const bool h8 = lane & 8;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float send = h8 ? a[i] : a[i + 8];
-        const float keep = h8 ? a[i + 8] : a[i];
-        b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-    float c[4];
-    const bool h4 = lane & 4;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float send = h4 ? b[i] : b[i + 4];
-        const float keep = h4 ? b[i + 4] : b[i];
-        c[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
-    float d[2];
-    const bool h2 = lane & 2;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float send = h2 ? c[i] : c[i + 2];
-        const float keep = h2 ? c[i + 2] : c[i];
-        d[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-    }
-    const bool h1 = lane & 1;
-    const float send = h1 ? d[0] : d[1];
-    const float keep = h1 ? d[1] : d[0];
-    return keep + __shfl_xor_sync(0xffffffffu, send, 1);
+    const float send = hi ? s0 : s1;
+    const float keep = hi ? s1 : s0;
+    return keep + __shfl_xor_sync(0xffffffffu, send, 16);
 }
 
 // Finishes one 32-column chunk of this thread's row: applies the epilogue
@@ -496,7 +512,8 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
                                              const CUtensorMap *tm2, float (&v)[32], int64_t row, int row0,
                                              int col, int z, int lane, uint32_t stg, AuxLoad *aux = nullptr,
                                              int next_col = -1, int next_row0 = 0,
-                                             volatile int *abort_flag = nullptr) {
+                                             volatile int *abort_flag = nullptr,
+                                             const BiasPre *bias_pre = nullptr) {
     if constexpr (EPI == EPI_ATTN_SCORE) {
         // S = scale * Q K^T with the causal mask, kept in fp32 for the softmax.
 #pragma unroll
@@ -524,7 +541,10 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
         // Y is GeLU of H as stored (rounded to bf16), the same value the
         // backward's recomputation rebuilds from the saved H.
         float bias[32];
-        load32(p.bias, col, col, p.N, true, bias);
+        if (bias_pre != nullptr)
+            bias_unpack(*bias_pre, bias);
+        else
+            load32(p.bias, col, col, p.N, true, bias);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] += bias[i];
         pack32(v, w0);
@@ -557,16 +577,6 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= gelu_prime_f(hv[i]);
         pack32(v, w0);
-        if (p.colsum_part) {
-            // da = 1^T dY: column sums of the stored (bf16-rounded) dY of this
-            // warp's 32 rows.  Rows past M hold exact zeros (zero-filled operands).
-            float q[32];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) unpack_bf16(w0[i], q[2 * i], q[2 * i + 1]);
-            const float cs = warp_colsum32(q, lane);
-            if (row0 < p.M && col + lane < p.N)
-                p.colsum_part[static_cast<int64_t>(row0 >> 5) * p.N + col + lane] = cs;
-        }
     } else if constexpr (EPI == EPI_FOLD_BIAS) {
         float bias[32];
         load32(p.bias, col, col, p.N, true, bias);
@@ -598,6 +608,14 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
         ptx::bulk_commit();
     }
     if constexpr (EPI == EPI_DGELU) {
+        if (p.colsum_part) {
+            // da = 1^T dY: column sums of the stored (bf16-rounded) dY of this
+            // warp's 32 rows, read back from the staged box (the TMA store only
+            // reads it too).  Rows past M hold exact zeros (zero-filled operands).
+            const float cs = box_colsum32(stg, lane);
+            const int c = col + 2 * (lane & 15) + (lane >> 4);
+            if (row0 < p.M && c < p.N) p.colsum_part[static_cast<int64_t>(row0 >> 5) * p.N + c] = cs;
+        }
         if (p.out1 != nullptr && next_col >= 0) aux_issue(tm1, *aux, stg + STG_BOX, next_col, next_row0, z, lane);
     }
 }
@@ -1195,6 +1213,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int qa = hm == 2 ? 4 : 0, qb = hm == 1 ? 4 : 8;
             const bool ones_tile = EPI == EPI_STORE && A_MN && B_MN && p.bias_tile && mb == p.m_tiles - 1;
             if constexpr (EPI == EPI_DGELU) aux_issue(&tmO1, aux, stg + STG_BOX, col0 + 32 * qa, row0, zb, lane);
+            // The bias of each chunk is fetched one chunk ahead (the first while
+            // the accumulator is still being computed).
+            BiasPre bias_next;
+            if constexpr (EPI == EPI_BIAS_GELU) bias_fetch(p.bias, col0 + 32 * qa, p.N, bias_next);
             bool got = ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_tfull[0]), tcount & 1u, p.wait_ns, &abort_sh);
             ++tcount;
             got = __all_sync(0xffffffffu, got);
@@ -1211,6 +1233,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ok = false;
                     break;
                 }
+                BiasPre bias_cur;
+                if constexpr (EPI == EPI_BIAS_GELU) {
+                    bias_cur = bias_next;
+                    if (q + 1 < qb) bias_fetch(p.bias, col0 + 32 * (q + 1), p.N, bias_next);
+                }
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(taddr, r);
                 ptx::tmem_ld_wait(r);
@@ -1225,7 +1252,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     continue;
                 }
                 finish_chunk<EPI, false>(p, &tmO0, &tmO1, &tmO2, v, row, row0, col0 + 32 * q, zb, lane, stg, &aux,
-                                         q + 1 < qb ? col0 + 32 * (q + 1) : -1, row0, &abort_sh);
+                                         q + 1 < qb ? col0 + 32 * (q + 1) : -1, row0, &abort_sh,
+                                         EPI == EPI_BIAS_GELU ? &bias_cur : nullptr);
             }
         }
         } else {
