@@ -39,21 +39,25 @@ REF_BUDGET_S = 150.0  # wall-time target of the reference arm's warm-up + timed 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes (read + write) per launch of each tensor-core GEMM, from one ncu
-# capture, with the hash of the kernel source they were taken at.  A kernel whose
-# source has changed since reports traffic null.
+# capture, with the hash of the kernel and launch sources they were taken at
+# (kernel_source_hash).  After a change to either, traffic is reported null.
 NCU_TRAFFIC = {  # profiles/dram_traffic_h8192_gemms.md (h8192 workload, one kernel per capture)
-    "fc1_bias_gelu": (1.950668e9 + 0.520329e9, "58a3777731bc"),
-    "fc2_shard_fold": (2.203338e9 + 0.083478e9, "58a3777731bc"),
-    "bwd_dY_dgelu": (2.346407e9 + 0.278198e9, "58a3777731bc"),
-    "bwd_dB": (1.099863e9 + 0.515223e9, "58a3777731bc"),
-    "bwd_dA": (1.398121e9 + 0.514170e9, "58a3777731bc"),
-    "bwd_dX_shard_fold": (2.200872e9 + 0.079927e9, "58a3777731bc"),
+    "fc1_bias_gelu": (1.364074e9 + 0.520902e9, "d01711e7eb43"),
+    "fc2_shard_fold": (2.768337e9 + 0.110188e9, "d01711e7eb43"),
+    "bwd_dY_dgelu": (1.794103e9 + 0.278261e9, "d01711e7eb43"),
+    "bwd_dB": (0.948088e9 + 0.516678e9, "d01711e7eb43"),
+    "bwd_dA": (0.995899e9 + 0.514533e9, "d01711e7eb43"),
+    "bwd_dX_shard_fold": (3.010249e9 + 0.103983e9, "d01711e7eb43"),
 }
 
 
 def kernel_source_hash() -> str:
-    p = os.path.join(ROOT, "tensor_transformer_mlp_tma_gb300", "csrc", "tc_gemm.cu")
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:12]
+    """sha256 prefix of the GEMM kernel source followed by the launch code (which
+    picks the tile order, and so the DRAM traffic)."""
+    h = hashlib.sha256()
+    for name in ("tc_gemm.cu", "api.cu"):
+        h.update(open(os.path.join(ROOT, "tensor_transformer_mlp_tma_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()[:12]
 
 
 def load_peaks():

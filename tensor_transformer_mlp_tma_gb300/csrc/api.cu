@@ -271,6 +271,16 @@ void pick_raster(GemmArgs &g, Epi epi = tpmlp::EPI_FOLD) {
         g.group = std::atoi(env + 2);
         return;
     }
+    // At most 32 M-tiles (M is the token count or the hidden size in every GEMM
+    // of the MLP and attention blocks at these sizes): walk up to 16 of them,
+    // all where there are 16 or fewer, down each group of N columns.  Per GEMM
+    // at h8192 (ncu, one kernel per capture) this order read 8-25% fewer DRAM
+    // bytes than the panel-budget rule below and ran up to 2% faster alone.
+    if (g.batch <= 1 && m_tiles <= 32) {
+        g.raster_n = false;
+        g.group = static_cast<int>(m_tiles < 16 ? m_tiles : 16);
+        return;
+    }
     const char *bud = std::getenv("TPMLP_L2_PANEL_MB");
     const double budget = (bud ? std::atof(bud) : 24.0) * 1048576.0;
     const double a_panel = static_cast<double>(tile_m) * g.K * 2, b_panel = static_cast<double>(tile_n) * g.K * 2;

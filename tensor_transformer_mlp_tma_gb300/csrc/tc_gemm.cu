@@ -146,6 +146,10 @@ struct Params {
     // split into their two 256-column halves, run as separate half-width tiles,
     // so that a last partial wave of wide tiles is spread over twice the units.
     int wide_tail;
+    // Wide tiles: the tiles of every odd wave (slot / units odd) walk K from the
+    // last k-block down to the first, so that a unit's next tile starts on the
+    // k-blocks its wave read last, while they are still in L2.
+    int serpentine;
 };
 
 // Coordinates after (x, y) of problem z in a map of the given rank.
@@ -755,6 +759,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const CUtensorMap *bmap = both ? &tmB : &tmB2;
                 const bool ones_tile = EPI == EPI_STORE && A_MN && B_MN && p.bias_tile && mb == p.m_tiles - 1;
                 const int nkb = p.kb_per_shard;
+                const bool down = p.serpentine && ((tile / num_units) & 1);
                 if (!dbg_ok(mb >= 0 && mb < p.m_tiles && nb >= 0 && nb < p.n_tiles && zb >= 0 && zb < p.batch &&
                                 (hm == 1 || hm == 2 || hm == 3) && n0 % 64 == 0,
                             p, &abort_sh, 0x0201u)) {
@@ -771,9 +776,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t full = ptx::mapa_shared(full_local, 0);
                     const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
                     const uint32_t sb = sa + C::A_STAGE + hs * (C::B_STAGE / 2);
-                    const int k0 = kb * BK;
-                    if (!dbg_ok(stage >= 0 && stage < STAGES && sb + b_blocks * MN_BLOCK_BYTES <= ring_end, p,
-                                &abort_sh, 0x0301u)) {
+                    const int k0 = (down ? nkb - 1 - kb : kb) * BK;
+                    if (!dbg_ok(stage >= 0 && stage < STAGES && sb + b_blocks * MN_BLOCK_BYTES <= ring_end &&
+                                    k0 >= 0 && k0 < nkb * BK,
+                                p, &abort_sh, 0x0301u)) {
                         ok = false;
                         break;
                     }
@@ -1696,6 +1702,11 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     // wide tile's time.  TPMLP_WIDE_TAIL=0 keeps whole tiles (a tuning knob, read
     // per call).
     p.wide_tail = 0;
+    // TPMLP_SERPENTINE=0 walks K upwards in every wave (a tuning knob, read per call).
+    {
+        const char *se = std::getenv("TPMLP_SERPENTINE");
+        p.serpentine = WIDE && !(se && se[0] == '0') ? 1 : 0;
+    }
     if (WIDE) {
         const char *tail_env = std::getenv("TPMLP_WIDE_TAIL");
         const int r = tiles % resident;

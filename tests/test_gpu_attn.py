@@ -244,13 +244,16 @@ def test_wide_tiles_match_oracle(tp, monkeypatch):
 def test_projections_on_square_tiles_match_wide(tp, monkeypatch):
     """The QKV projection (bias, no activation), dO = dZ Wo^T (two K-major
     operands), dWo and dWqkv run on 256 x 512 tiles by default; TPMLP_WIDE=0
-    runs them on 256 x 256 tiles.  Both match the oracle, and each output
-    element is accumulated over k in the same order by the same MMA shape, so
-    the two give the same bits."""
+    runs them on 256 x 256 tiles.  All match the oracle, and with every wave
+    walking K upwards (TPMLP_SERPENTINE=0) each output element is accumulated
+    over k in the same order by the same MMA shape, so the two give the same
+    bits."""
     nb, S, h, heads, t = 2, 264, 1024, 8, 4
-    inp, wide, _ = run_attn(tp, nb, S, h, heads, t, seed=31)
+    inp, default, _ = run_attn(tp, nb, S, h, heads, t, seed=31)
     ref = oracle_ref(inp, nb, heads, t)
-    for out in (wide,):
+    monkeypatch.setenv("TPMLP_SERPENTINE", "0")
+    _, wide, _ = run_attn(tp, nb, S, h, heads, t, seed=31)
+    for out in (default, wide):
         errs = {k: rel(to_np(out[k]), ref[k]) for k in TOL}
         assert all(v <= TOL[k] for k, v in errs.items()), errs
     monkeypatch.setenv("TPMLP_WIDE", "0")

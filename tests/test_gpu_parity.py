@@ -42,6 +42,7 @@ def test_tensor_core_path_matches_oracle(T, h, F, t):
 @pytest.mark.parametrize("env", [{"TPMLP_CTA_PAIR": "0"}, {"TPMLP_MN4": "0"}, {"TPMLP_RASTER": "n:3"},
                                  {"TPMLP_RASTER": "m:1", "TPMLP_CTA_PAIR": "0"}, {"TPMLP_PDL": "0"},
                                  {"TPMLP_WIDE": "0"}, {"TPMLP_WIDE_TAIL": "0"}, {"TPMLP_MAX_UNITS": "4"},
+                                 {"TPMLP_SERPENTINE": "0"}, {"TPMLP_MAX_UNITS": "3"},
                                  {"TPMLP_MAX_UNITS": "3", "TPMLP_RASTER": "n:2"},
                                  {"TPMLP_MAX_UNITS": "2", "TPMLP_WIDE_TAIL": "0", "TPMLP_MN4": "0"}])
 @pytest.mark.parametrize("T,h,F,t", [(300, 384, 1280, 2), (257, 512, 1024, 4)])
@@ -61,13 +62,17 @@ def test_tuning_knobs_keep_parity(T, h, F, t, env, monkeypatch):
 
 @pytest.mark.parametrize("T,h,F,t", [(300, 384, 1280, 2), (1000, 1024, 4096, 4)])
 def test_wide_and_square_tiles_agree(T, h, F, t, monkeypatch):
-    """256 x 512 tiles (default) against 256 x 256 tiles (TPMLP_WIDE=0): both
+    """256 x 512 tiles (default) against 256 x 256 tiles (TPMLP_WIDE=0): all
     within tolerance of the oracle, and within bf16 rounding of each other.
-    The two accumulate every output element over k in the same order with the
-    same MMA shape, so they are expected to agree bit for bit; the test
-    reports whether they do but requires only the tolerance."""
+    With every wave walking K upwards (TPMLP_SERPENTINE=0) the two accumulate
+    every output element over k in the same order with the same MMA shape, so
+    they are expected to agree bit for bit; the test reports whether they do
+    but requires only the tolerance."""
     inp = inputs.make(T, h, F, "bf16", seed=T + 5 * t, std=STD)
     ref = oracle.forward_backward(inp["X"], inp["A"], inp["a"], inp["B"], inp["b"], inp["dZ"], t)
+    default, _ = run_gpu(inp, t)
+    compare_full(default, ref, TOL_BF16)
+    monkeypatch.setenv("TPMLP_SERPENTINE", "0")
     wide, _ = run_gpu(inp, t)
     compare_full(wide, ref, TOL_BF16)
     monkeypatch.setenv("TPMLP_WIDE", "0")
