@@ -130,6 +130,11 @@ struct Params {
     int causal_k;    // K range of an M-tile: 0 all; 1 k < end of the tile's rows; 2 k >= start of its rows
     int skip_upper;  // tiles wholly above the diagonal (every column past every row) are not computed
     int flip_odd;    // odd problems walk their M-tiles in reverse order (load balance under causal ranges)
+    // Causal K ranges over one column of tiles: each unit takes the M-tiles of
+    // a problem in complementary pairs (see tile_coords); `units` is the grid's
+    // unit count, which the pair order is laid out for.
+    int pair_order;
+    int units;
     int a_mn4, b_mn4;  // MN-major operand mapped as 4-D (all of a stage's 64-wide blocks in one copy)
     // Bias gradient from the MMA (EPI_STORE with MN-major A): one extra M-tile
     // whose A is a 64 x 64 block of ones (map tmO2), so its first accumulator
@@ -220,6 +225,38 @@ __device__ __forceinline__ bool tile_active(const Params &p, int mb, int nb) {
 // super-row the grouped index runs fastest, so the CTAs resident at one time
 // share `group` panels of one operand and a few of the other.
 __device__ __forceinline__ void tile_coords(int tile, const Params &p, int &mb, int &nb, int &zb) {
+    if (p.pair_order) {
+        // Causal K ranges with one N-tile per problem (the products against P or
+        // dS, N = d): M-tile i of a problem costs i + 1 k-blocks of 256 keys, or
+        // m_tiles - i, so M-tiles i and m_tiles - 1 - i together cost the same
+        // for every i.  The slots of unit u are u, u + U, u + 2U, ... (U units);
+        // slots 2jU + u and (2j + 1)U + u hold the two M-tiles of pair jU + u,
+        // so every unit runs whole pairs of equal cost.  The R = n / 2U full
+        // double rounds are laid out this way; of the s = n - 2RU slots left,
+        // units that get two take one more pair, the others one tile each.
+        const int U = p.units, half = p.m_tiles >> 1;
+        const int n = p.m_tiles * p.batch;
+        const int R = n / (2 * U), s = n - 2 * R * U;
+        const int k = tile / U, u = tile - k * U;
+        const int twice = s > U ? s - U : 0;  // units with two slots left
+        int pair, member;
+        if (k < 2 * R) {
+            pair = u + (k >> 1) * U;
+            member = k & 1;
+        } else if (u < twice) {
+            pair = R * U + u;
+            member = k - 2 * R;
+        } else {
+            const int v = u - twice;
+            pair = R * U + twice + (v >> 1);
+            member = v & 1;
+        }
+        zb = pair / half;
+        const int i = pair - zb * half;
+        mb = member ? i : p.m_tiles - 1 - i;
+        nb = 0;
+        return;
+    }
     const int per_batch = p.m_tiles * p.n_tiles;
     zb = tile / per_batch;
     tile -= zb * per_batch;
@@ -1688,6 +1725,12 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
         const char *flip = std::getenv("TPMLP_FLIP_ODD");
         p.flip_odd = (g.causal_k != 0 || g.skip_upper) && !(flip && flip[0] == '0') ? 1 : 0;
     }
+    // TPMLP_PAIR_ORDER=0 keeps the reversed odd problems for the causal products
+    // with one N-tile (a tuning knob, read per call).
+    {
+        const char *po = std::getenv("TPMLP_PAIR_ORDER");
+        p.pair_order = g.causal_k != 0 && p.n_tiles == 1 && p.m_tiles % 2 == 0 && !(po && po[0] == '0') ? 1 : 0;
+    }
     // The causal ranges are defined for square per-head problems in one shard.
     if ((g.causal_k != 0 || g.skip_upper) && (g.nshards != 1 || (g.causal_k != 0 && g.M != g.K))) {
         set_last_error("causal K ranges need one shard and M = K (M=%lld K=%lld, %d shards)",
@@ -1714,6 +1757,7 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
         tiles += p.wide_tail;
     }
     const int units = tiles < resident ? tiles : resident;
+    p.units = units;
     if (std::getenv("TPMLP_DEBUG_LAUNCH"))
         std::fprintf(stderr, "tpmlp gemm epi=%d cg=%d M=%lld N=%lld K=%lld tiles=%d resident=%d grid=%d group=%d%c\n",
                      EPI, CG, static_cast<long long>(g.M), static_cast<long long>(g.N), static_cast<long long>(g.K),

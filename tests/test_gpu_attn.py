@@ -291,3 +291,23 @@ def test_p_upper_tiles_flag(tp, pair, monkeypatch):
     assert torch.equal(P0[:, ~upper], P1[:, ~upper])
     for k in ("Z", "O", "QKV", "dX", "dWqkv", "dbqkv", "dWo", "dbo"):
         assert torch.equal(res[False][k], res[True][k]), k
+
+
+@pytest.mark.parametrize("units", [None, "5", "3"])
+def test_pair_order_gives_the_same_bits(tp, units, monkeypatch):
+    """The causal products against P and dS hand each unit complementary pairs
+    of M-tiles (TPMLP_PAIR_ORDER, default) instead of reversing odd problems.
+    Only the unit that computes a tile changes, so every output is bit-identical
+    to the other order, and matches the oracle; small unit counts exercise the
+    full double rounds and the leftover slots on a small shape."""
+    if units:
+        monkeypatch.setenv("TPMLP_MAX_UNITS", units)
+    nb, S, h, heads, t = 2, 1024, 512, 4, 2   # 4 M-tiles of 256 per head, 8 problems
+    inp, paired, _ = run_attn(tp, nb, S, h, heads, t, seed=47)
+    ref = oracle_ref(inp, nb, heads, t)
+    errs = {k: rel(to_np(paired[k]), ref[k]) for k in TOL}
+    assert all(v <= TOL[k] for k, v in errs.items()), errs
+    monkeypatch.setenv("TPMLP_PAIR_ORDER", "0")
+    _, flipped, _ = run_attn(tp, nb, S, h, heads, t, seed=47)
+    for k in TOL:
+        assert torch.equal(paired[k], flipped[k]), k
