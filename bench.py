@@ -42,12 +42,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, with the hash of the kernel and launch sources they were taken at
 # (kernel_source_hash).  After a change to either, traffic is reported null.
 NCU_TRAFFIC = {  # profiles/dram_traffic_h8192_gemms.md (h8192 workload, one kernel per capture)
-    "fc1_bias_gelu": (1.364074e9 + 0.520902e9, "d01711e7eb43"),
-    "fc2_shard_fold": (2.768337e9 + 0.110188e9, "d01711e7eb43"),
-    "bwd_dY_dgelu": (1.794103e9 + 0.278261e9, "d01711e7eb43"),
-    "bwd_dB": (0.948088e9 + 0.516678e9, "d01711e7eb43"),
-    "bwd_dA": (0.995899e9 + 0.514533e9, "d01711e7eb43"),
-    "bwd_dX_shard_fold": (3.010249e9 + 0.103983e9, "d01711e7eb43"),
+    "fc1_bias_gelu": (1.325688e9 + 0.520764e9, "f6c5ff3ec0b8"),
+    "fc2_shard_fold": (2.507555e9 + 0.091267e9, "f6c5ff3ec0b8"),
+    "bwd_dY_dgelu": (1.768033e9 + 0.278109e9, "f6c5ff3ec0b8"),
+    "bwd_dB": (0.929347e9 + 0.515363e9, "f6c5ff3ec0b8"),
+    "bwd_dA": (0.962548e9 + 0.513651e9, "f6c5ff3ec0b8"),
+    "bwd_dX_shard_fold": (2.645486e9 + 0.086963e9, "f6c5ff3ec0b8"),
 }
 
 

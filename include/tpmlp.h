@@ -13,7 +13,11 @@
  * the column-parallel GEMM of every shard is one launch (the shards are disjoint
  * column blocks) and each all-reduce is a fixed-order fp32 sum of the t shard
  * partials, Z = b + (((Z_1 + Z_2) + Z_3) + ... + Z_t), done on chip.  Repeated
- * calls with the same inputs give bit-identical outputs.
+ * calls with the same inputs give bit-identical outputs.  The tensor-core GEMMs
+ * accumulate over k in an order that depends on their tile schedule, and so on
+ * the number of SMs they run on: a GPU with another SM count (or the
+ * TPMLP_MAX_UNITS / TPMLP_SERPENTINE knobs) may round differently, within the
+ * same tolerances.
  *
  * Layout.  Every tensor is row-major, contiguous and in device memory:
  *   X[T,h]  A[h,F]  a[F]  B[F,h]  b[h]  Z[T,h]  H,Y[T,F]  (T tokens, h hidden,
