@@ -282,6 +282,26 @@ def config_of(w, t, world, fwd_only=False, recompute=False, sp=False):
 
 
 # ------------------------------------------------------------------ end to end
+def gpu_local_cpus(dev):
+    """The host cores the system lists as local to the GPU (its PCI device's
+    local_cpulist), or None where that is not known."""
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        bdf = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        with open("/sys/bus/pci/devices/%s/local_cpulist" % bdf) as f:
+            text = f.read().strip()
+        cpus = set()
+        for part in text.split(","):
+            if "-" in part:
+                lo, hi = part.split("-")
+                cpus.update(range(int(lo), int(hi) + 1))
+            elif part:
+                cpus.add(int(part))
+        return cpus or None
+    except (AttributeError, OSError, ValueError):
+        return None
+
+
 def overlapped_e2e(dev, stream, world, steps, warmup, host_in, dev_out, copy_out, fwd, bwd):
     """Times `steps` steps end to end: every step copies `host_in` (pinned host
     tensors) to the device, runs fwd (and bwd, if given) on `stream`, and copies
@@ -295,7 +315,32 @@ def overlapped_e2e(dev, stream, world, steps, warmup, host_in, dev_out, copy_out
     dev_out: name -> (shape, dtype) of the device outputs; copy_out: (names
     copied after the forward, names copied after the backward); fwd(ins, outs)
     and bwd(ins, outs) launch one step's work.  Returns (max over ranks of the
-    ms per step, host-to-device bytes per step, device-to-host bytes per step)."""
+    ms per step, host-to-device bytes per step, device-to-host bytes per step,
+    a note on the host cores used).
+
+    While the pinned buffers are made and the steps run, the calling thread is
+    held to the host cores local to the GPU (where the system names them and the
+    process may use them): a pinned page is placed in the memory of the core
+    that first touches it, and copies from a far memory node cross one more
+    link."""
+    allowed = os.sched_getaffinity(0)
+    local = gpu_local_cpus(dev)
+    near = (local & allowed) if local else set()
+    if near and near != allowed:
+        os.sched_setaffinity(0, near)
+        note = "calling thread on the %d of %d allowed host cores local to the GPU" % (len(near), len(allowed))
+    elif near:
+        note = "all %d allowed host cores are local to the GPU" % len(allowed)
+    else:
+        note = "GPU-local host cores not known or not allowed; %d cores, affinity unchanged" % len(allowed)
+    try:
+        return overlapped_e2e_run(dev, stream, world, steps, warmup, host_in, dev_out, copy_out, fwd,
+                                  bwd) + (note,)
+    finally:
+        os.sched_setaffinity(0, allowed)
+
+
+def overlapped_e2e_run(dev, stream, world, steps, warmup, host_in, dev_out, copy_out, fwd, bwd):
     hin = {k: v.pin_memory() for k, v in host_in.items()}
     din = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in hin.items()} for _ in range(2)]
     dout = [{k: torch.empty(shape, dtype=dt, device=dev) for k, (shape, dt) in dev_out.items()} for _ in range(2)]
@@ -512,14 +557,14 @@ def run_ours(args, rank, world, local, w=None, quiet=False):
             else:
                 tpmlp.backward(ctx, ins["dZ"], stream=stream, **{k: outs[k] for k in g})
 
-        ems, h2d, d2h = overlapped_e2e(dev, stream, world, args.steps, args.warmup, host_in, dev_out,
+        ems, h2d, d2h, host_note = overlapped_e2e(dev, stream, world, args.steps, args.warmup, host_in, dev_out,
                                        (["Z"], [] if args.fwd_only else ["dX", "da", "db"]), fwd,
                                        None if args.fwd_only else bwd)
         e2e = {"value": flops * world / (ems * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ems,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "what": "X and dZ copied in from pinned host memory, Z, dX, da, db copied out, every "
                        "step, on copy streams overlapped with the neighbouring steps' compute; weights "
-                       "and weight gradients stay resident"}
+                       "and weight gradients stay resident", "host": host_note}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -599,14 +644,14 @@ def run_attn_bench(args, rank, world, local):
         def bwd(ins, outs):
             tpmlp.attn_backward(ctx, ins["dZ"], stream=stream, **{k: outs[k] for k in g})
 
-        ems, h2d, d2h = overlapped_e2e(dev, stream, world, args.steps, args.warmup,
+        ems, h2d, d2h, host_note = overlapped_e2e(dev, stream, world, args.steps, args.warmup,
                                        {"X": host["X"], "dZ": host["dZ"]}, dev_out,
                                        (["Z"], ["dX", "dbqkv", "dbo"]), fwd, bwd)
         e2e = {"value": w.flops_fwd_bwd * world / (ems * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ems,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "what": "X and dZ copied in from pinned host memory, Z, dX, dbqkv, dbo copied out, every "
                        "step, on copy streams overlapped with the neighbouring steps' compute; weights "
-                       "and weight gradients stay resident"}
+                       "and weight gradients stay resident", "host": host_note}
     return {"metric": "TP self-attention fwd+bwd TFLOP/s (bf16, 1×GB300)", "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
