@@ -271,14 +271,16 @@ typedef struct {
 /* Bytes of QKV + P + O; 0 for an invalid shape. */
 size_t tpmlp_attn_saved_bytes(const tpmlp_attn_shape *shape);
 /* Bytes of device workspace for forward and backward (status word, the row terms,
- * token-major dO and dQKV, the fp32 scores reused for dS, and an 8 KiB block of
+ * token-major dO and dQKV, the fp16 scores reused for dS, and an 8 KiB block of
  * ones; the per-head GEMMs address Q, K, V, O, dO, dQ, dK, dV in place inside the
  * token-major arrays); 256-byte aligned, first 8 bytes zero before first use. */
 size_t tpmlp_attn_workspace_bytes(const tpmlp_attn_shape *shape);
 
 /* Forward: QKV = X Wqkv + bqkv (one column-parallel GEMM for all shards), per
  * head P = softmax(causal Q K^T / sqrt(d)) and O = P V (batched over heads),
- * Z = bo + fixed-order sum of the t row-parallel partials.
+ * Z = bo + fixed-order sum of the t row-parallel partials.  The scaled scores
+ * are computed in fp32 and kept in fp16 (11 significant bits) between the score
+ * GEMM and the fp32 softmax; P is stored in bf16.
  * Errors: INVALID_ARG for a bad shape or NULL pointer; UNSUPPORTED for a non-bf16
  * dtype, misaligned pointers, d % 64 != 0, seq % 8 != 0, or h/t or 3h/t not a
  * multiple of 64 when t > 1; CUDA when a launch fails. */

@@ -705,7 +705,7 @@ bool attn_shape_valid(const tpmlp_attn_shape *s) {
     // int32 tile and grid arithmetic inside the kernels
     if (s->hidden > (1LL << 28) || s->seq > (1LL << 20) || s->batch * s->seq > (1LL << 30)) return false;
     if (static_cast<int64_t>(s->batch) * s->heads > (1LL << 24)) return false;
-    // tile counts of the projections and the per-head products; the fp32 scores
+    // tile counts of the projections and the per-head products; the scores
     // ([batch*heads][seq][seq]) must be addressable
     const int64_t T = s->batch * s->seq, h = s->hidden, nz = s->batch * s->heads;
     if (!tiles_fit(T, 3 * h) || !tiles_fit(h + 256, 3 * h) || !tiles_fit(s->seq, s->seq, nz)) return false;
@@ -715,7 +715,7 @@ bool attn_shape_valid(const tpmlp_attn_shape *s) {
 
 // Device workspace of the attention block, 1 KB-aligned regions:
 //   status | D [batch*heads*seq] fp32 | dO [T,h] bf16 | dQKV [T,3h] bf16 |
-//   scores [batch*heads][seq][seq] fp32 (the backward reuses it for dS in bf16) |
+//   scores [batch*heads][seq][seq] fp16 (the backward reuses it for dS in bf16) |
 //   a 64 x 64 bf16 block of ones (bias-gradient tiles).
 // The per-head GEMMs address Q, K, V, O, dO, dQ, dK, dV in place inside the
 // token-major QKV, O, dO and dQKV arrays (4-D and 5-D tensor maps).
@@ -735,7 +735,7 @@ AttnLayout attn_layout(const tpmlp_attn_shape *s) {
     L.dQKV = off;
     off += 3 * th;
     L.scores = off;
-    off += align_up(static_cast<size_t>(s->batch) * s->heads * s->seq * s->seq * 4, 1024);
+    off += align_up(static_cast<size_t>(s->batch) * s->heads * s->seq * s->seq * 2, 1024);
     L.ones = off;
     off += ONES_BYTES;
     L.total = off;
@@ -889,7 +889,7 @@ tpmlp_status tpmlp_attn_forward(const tpmlp_attn_shape *s, const void *X, const 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     uint32_t *status = reinterpret_cast<uint32_t *>(ws);
-    float *scores = reinterpret_cast<float *>(ws + L.scores);
+    void *scores = ws + L.scores;
     const tpmlp::HeadView qv = qkv_view(s), tv = tok_view(s);
     const void *Qp = qkv_part(saved->QKV, s, 0), *Kp = qkv_part(saved->QKV, s, 1), *Vp = qkv_part(saved->QKV, s, 2);
 
@@ -977,7 +977,7 @@ tpmlp_status tpmlp_attn_backward(const tpmlp_attn_shape *s, const void *dZ, cons
     const void *Qp = qkv_part(saved->QKV, s, 0), *Kp = qkv_part(saved->QKV, s, 1), *Vp = qkv_part(saved->QKV, s, 2);
     void *dQp = const_cast<void *>(qkv_part(dQKV, s, 0)), *dKp = const_cast<void *>(qkv_part(dQKV, s, 1)),
          *dVp = const_cast<void *>(qkv_part(dQKV, s, 2));
-    void *dS = ws + L.scores;  // bf16 [nz][S][S] over the dead fp32 scores
+    void *dS = ws + L.scores;  // bf16 [nz][S][S] over the dead fp16 scores
     const float scale = 1.0f / std::sqrt(static_cast<float>(d));
 
     // dbo = 1^T dZ and dbqkv = 1^T dQKV come from the ones tiles of the dWo and

@@ -3,10 +3,11 @@
 // the per-head products run on the tensor-core GEMMs, which read and write each
 // head's Q, K, V, O, dO, dQ, dK, dV in place in the token-major arrays; these
 // memory-bound kernels compute the row-wise parts of the attention:
-//   - causal softmax of fp32 scores [nb*heads*S][S] into bf16 P;
+//   - causal softmax of fp16 scores [nb*heads*S][S] (computed in fp32) into bf16 P;
 //   - D[z, s] = sum_e dO[token, head cols] * O[token, head cols], the row term of
 //     the softmax backward.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -35,9 +36,10 @@ __device__ __forceinline__ int64_t write_end(int64_t row, int64_t S, int64_t wti
 // One score row, held in U float4 registers per lane: row r of a head (r = row %
 // S) sees columns 0..last; the others are written as exact zeros (up to wend).
 // Max-subtracted exponentials (the fast __expf), fp32 sum.  The row is read once,
-// 16 bytes per lane at a time; only the columns up to the diagonal are read.
+// four fp16 scores (8 bytes) per lane at a time; only the columns up to the
+// diagonal are read.
 template <int U>
-__device__ __forceinline__ void softmax_row(const float4 *__restrict__ in, uint2 *__restrict__ out, int64_t last,
+__device__ __forceinline__ void softmax_row(const uint2 *__restrict__ in, uint2 *__restrict__ out, int64_t last,
                                             int64_t wend, int lane) {
     float4 x[U];
     float mx = -INFINITY;
@@ -45,7 +47,10 @@ __device__ __forceinline__ void softmax_row(const float4 *__restrict__ in, uint2
     for (int v = 0; v < U; ++v) {
         const int64_t c = 4 * (lane + 32 * v);
         if (c <= last) {
-            x[v] = __ldcs(in + lane + 32 * v);  // streamed: read once
+            const uint2 u = __ldcs(in + lane + 32 * v);  // streamed: read once
+            const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+            const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+            x[v] = make_float4(lo.x, lo.y, hi.x, hi.y);
             if (c + 1 > last) x[v].y = -INFINITY;
             if (c + 2 > last) x[v].z = -INFINITY;
             if (c + 3 > last) x[v].w = -INFINITY;
@@ -93,16 +98,16 @@ __device__ __forceinline__ void softmax_row(const float4 *__restrict__ in, uint2
 // softmax.
 template <int V>
 __global__ void __launch_bounds__(256, V <= 16 ? 3 : 1)  // 24 warps per SM up to 2048 columns
-    softmax_reg_kernel(const float *__restrict__ S_, __nv_bfloat16 *__restrict__ P, int64_t rows, int64_t S,
+    softmax_reg_kernel(const __half *__restrict__ S_, __nv_bfloat16 *__restrict__ P, int64_t rows, int64_t S,
                        bool causal, int64_t wtile) {
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     if (row >= rows) return;
     const int64_t last = causal ? row % S : S - 1;
     const int64_t wend = write_end(row, S, wtile);
-    const float4 *in = reinterpret_cast<const float4 *>(S_ + row * S);
+    const uint2 *in = reinterpret_cast<const uint2 *>(S_ + row * S);
     uint2 *out = reinterpret_cast<uint2 *>(P + row * S);
-    const int64_t need = last / 128 + 1;  // float4 slots per lane up to the diagonal
+    const int64_t need = last / 128 + 1;  // 4-score slots per lane up to the diagonal
     constexpr int V1 = V / 4 > 0 ? V / 4 : 1, V2 = V / 2 > V1 ? V / 2 : V1, V3 = 3 * V / 4 > V2 ? 3 * V / 4 : V2;
     if (need <= V1)
         softmax_row<V1>(in, out, last, wend, lane);
@@ -117,24 +122,24 @@ __global__ void __launch_bounds__(256, V <= 16 ? 3 : 1)  // 24 warps per SM up t
 // Rows longer than the register version holds: the same arithmetic with three
 // passes over the row (max, sum, write).
 __global__ void __launch_bounds__(256)
-    softmax_kernel(const float *__restrict__ S_, __nv_bfloat16 *__restrict__ P, int64_t rows, int64_t S,
+    softmax_kernel(const __half *__restrict__ S_, __nv_bfloat16 *__restrict__ P, int64_t rows, int64_t S,
                    bool causal, int64_t wtile) {
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     if (row >= rows) return;
     const int64_t last = causal ? row % S : S - 1;
-    const float *in = S_ + row * S;
+    const __half *in = S_ + row * S;
     __nv_bfloat16 *out = P + row * S;
     float mx = -INFINITY;
-    for (int64_t c = lane; c <= last; c += 32) mx = fmaxf(mx, in[c]);
+    for (int64_t c = lane; c <= last; c += 32) mx = fmaxf(mx, __half2float(in[c]));
     mx = warp_max(mx);
     float sum = 0.0f;
-    for (int64_t c = lane; c <= last; c += 32) sum += __expf(in[c] - mx);
+    for (int64_t c = lane; c <= last; c += 32) sum += __expf(__half2float(in[c]) - mx);
     sum = warp_sum(sum);
     const float inv = 1.0f / sum;
     const int64_t wend = write_end(row, S, wtile);
     for (int64_t c = lane; c < wend; c += 32)
-        out[c] = __float2bfloat16_rn(c <= last ? __expf(in[c] - mx) * inv : 0.0f);
+        out[c] = __float2bfloat16_rn(c <= last ? __expf(__half2float(in[c]) - mx) * inv : 0.0f);
 }
 
 // D[z*S + s] = sum_e dO[r, g*d + e] * O[r, g*d + e] over the token-major [T, h]
@@ -218,12 +223,13 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace attn
 
-cudaError_t launch_softmax(const float *S, void *P, int64_t rows, int64_t cols, bool causal, int64_t wtile,
+cudaError_t launch_softmax(const void *S_, void *P, int64_t rows, int64_t cols, bool causal, int64_t wtile,
                            cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
     const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+    const __half *S = static_cast<const __half *>(S_);
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(P);
-    // 16-byte row starts (cols a multiple of 4) for the vector loads
+    // 8-byte row starts (cols a multiple of 4) for the vector loads
     if (cols % 4 != 0 || cols > 128 * 32)
         attn::softmax_kernel<<<grid, 256, 0, st>>>(S, out, rows, cols, causal, wtile);
     else if (cols <= 128 * 4)

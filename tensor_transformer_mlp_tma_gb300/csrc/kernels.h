@@ -13,7 +13,7 @@ enum Epi : int {
     EPI_DGELU = 2,      // dY = acc * GeLU'(H)                              -- dZ B^T
     EPI_STORE = 3,      // out = acc                                       -- dB, dA
     EPI_FOLD = 4,       // dX = ((P_1 + P_2) + ...)                        -- dY A^T
-    EPI_ATTN_SCORE = 5, // S = scale * acc, -inf above the diagonal (causal), fp32 out -- Q K^T
+    EPI_ATTN_SCORE = 5, // S = scale * acc, -inf above the diagonal (causal), fp16 out -- Q K^T
     EPI_ATTN_DS = 6,    // dS = P * (acc - D[row]) * scale                  -- dO V^T -> dS
 };
 
@@ -126,7 +126,7 @@ struct HeadLayout {
     int64_t nb, S, h, heads, d;
 };
 // wtile > 0: each row writes P only up to the end of its wtile-wide column tile.
-cudaError_t launch_softmax(const float *S, void *P, int64_t rows, int64_t cols, bool causal, int64_t wtile,
+cudaError_t launch_softmax(const void *S, void *P, int64_t rows, int64_t cols, bool causal, int64_t wtile,
                            cudaStream_t st);
 // D[z*S + s] = row dot of dO and O over head g's columns of token b*S + s (token-major inputs).
 // `ones` (optional): an 8 KiB block the kernel also fills with bf16 ones.

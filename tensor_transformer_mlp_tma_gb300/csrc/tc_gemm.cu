@@ -32,6 +32,7 @@
 // drains its own copies and MMAs and frees its tensor memory before returning.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
@@ -349,6 +350,11 @@ __device__ __forceinline__ float gelu_prime_f(float x) {
     return fmaf(fmaf(-th, th, 1.0f), hxdu, fmaf(0.5f, th, 0.5f));
 }
 
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -448,19 +454,6 @@ __device__ __forceinline__ void unstage_half_row128(uint32_t box, int r, int hf,
     }
 }
 
-// Row r of a 32 x 32 fp32 box (4 KB, both staging boxes of a warp) staged for a
-// 128-byte-swizzled TMA store: 16-byte chunk j of the 128-byte row sits at
-// chunk j ^ (r & 7).
-__device__ __forceinline__ void stage_row_f32(uint32_t box, int r, const float (&v)[32]) {
-    const uint32_t row = box + static_cast<uint32_t>(r) * 128u;
-    const int x = r & 7;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        ptx::st_shared_v4(row + (static_cast<uint32_t>(j ^ x) << 4), __float_as_uint(v[4 * j]),
-                          __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
-                          __float_as_uint(v[4 * j + 3]));
-}
-
 __device__ __forceinline__ void pack32(const float (&v)[32], uint32_t (&w)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) w[i] = pack_bf16(v[2 * i], v[2 * i + 1]);
@@ -556,15 +549,21 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
                                              volatile int *abort_flag = nullptr,
                                              const BiasPre *bias_pre = nullptr) {
     if constexpr (EPI == EPI_ATTN_SCORE) {
-        // S = scale * Q K^T with the causal mask, kept in fp32 for the softmax.
+        // S = scale * Q K^T with the causal mask, stored in fp16 for the softmax
+        // (11 significant bits; finite values clamped to the fp16 range, the
+        // masked ones -inf).
+        uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            v[i] *= p.scale;
-            if (p.causal && col + i > row) v[i] = -INFINITY;
+        for (int i = 0; i < 16; ++i) {
+            float lo = fminf(fmaxf(v[2 * i] * p.scale, -65504.0f), 65504.0f);
+            float hi = fminf(fmaxf(v[2 * i + 1] * p.scale, -65504.0f), 65504.0f);
+            if (p.causal && col + 2 * i > row) lo = -INFINITY;
+            if (p.causal && col + 2 * i + 1 > row) hi = -INFINITY;
+            w[i] = pack_f16(lo, hi);
         }
         if (lane == 0) ptx::bulk_wait_read0();
         __syncwarp();
-        stage_row_f32(stg, lane, v);
+        stage_row(stg, lane, w);
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && row0 < p.M && col < p.N) {
@@ -1475,20 +1474,20 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // (cols, rows, batch); a plain matrix has batch 1.
 static bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, uint32_t box_cols,
                      uint32_t box_rows, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B, int64_t batch = 1,
-                     bool fp32 = false) {
+                     CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto fn = encode_fn();
     if (!fn) {
         set_last_error("cuTensorMapEncodeTiled is not available from the driver");
         return false;
     }
-    const cuuint64_t esz = fp32 ? 4 : 2;
+    const cuuint64_t esz = dt == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                           static_cast<cuuint64_t>(batch)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * esz,
                              static_cast<cuuint64_t>(cols) * static_cast<cuuint64_t>(rows) * esz};
     cuuint32_t box[3] = {box_cols, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+    CUresult r = fn(m, dt, 3,
                     const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -1655,16 +1654,17 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     // The GeLU' epilogue can also write Y rebuilt from H (third map).
     CUtensorMap mo0, mo1, mo2;
     const void *o0 = g.out0 ? g.out0 : g.out1;
-    // The attention scores are fp32 (32 x 32 box, 128-byte swizzle, see stage_row_f32);
-    // dS reads P through the second map; both of its maps have 32 x 64 boxes with
-    // 128-byte swizzle (see stage_half_row128).
+    // The attention scores are fp16 (32 x 32 box, 64-byte swizzle, as the bf16
+    // outputs); dS reads P through the second map; both of its maps have 32 x 64
+    // boxes with 128-byte swizzle (see stage_half_row128).
     const void *o1 = (EPI == EPI_BIAS_GELU) ? (g.out1 ? g.out1 : o0)
                                             : ((EPI == EPI_DGELU || EPI == EPI_ATTN_DS) ? g.aux : o0);
     const void *o2 = (EPI == EPI_DGELU && g.out1) ? g.out1 : o0;
-    const bool f32out = EPI == EPI_ATTN_SCORE;
+    const CUtensorMapDataType odt =
+        EPI == EPI_ATTN_SCORE ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const bool wide = EPI == EPI_ATTN_DS;
     const uint32_t obox = wide ? 64 : 32;
-    const CUtensorMapSwizzle so = (f32out || wide) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const CUtensorMapSwizzle so = wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     if (wide && (o_rank > 3 || g.nshards != 1)) {
         set_last_error("dS epilogue: a plain [problems][M][N] output and one shard only");
         return cudaErrorInvalidValue;
@@ -1676,10 +1676,10 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
         return cudaErrorInvalidValue;
     }
     if (!(o_rank > 3 ? make_map_view(&mo0, o0, g.o_view, 32, 32, so)
-                     : make_map(&mo0, o0, g.M, g.N, obox, 32, so, nb, f32out)) ||
-        !make_map(&mo1, o1, g.M, g.N, obox, 32, so, nb, f32out) ||
+                     : make_map(&mo0, o0, g.M, g.N, obox, 32, so, nb, odt)) ||
+        !make_map(&mo1, o1, g.M, g.N, obox, 32, so, nb, odt) ||
         !(bias_tile ? make_map(&mo2, g.ones, 64, 64, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B, 1)
-                    : make_map(&mo2, o2, g.M, g.N, 32, 32, so, nb, f32out)))
+                    : make_map(&mo2, o2, g.M, g.N, 32, 32, so, nb, odt)))
         return cudaErrorInvalidValue;
 
     Params p;

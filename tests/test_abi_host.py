@@ -212,9 +212,9 @@ def test_attention_size_queries(tp):
     T, h, S, nz = 4096, 8192, 2048, 128
     assert tp.lib.tpmlp_attn_saved_bytes(ctypes.byref(s)) == 2 * (T * 3 * h + T * h + nz * S * S)
     ws = tp.lib.tpmlp_attn_workspace_bytes(ctypes.byref(s))
-    # token-major dO and dQKV, fp32 scores (the per-head operands are views)
-    assert ws >= 4 * T * h * 2 + nz * S * S * 4
-    assert ws < 5 * T * h * 2 + nz * S * S * 4
+    # token-major dO and dQKV, fp16 scores (the per-head operands are views)
+    assert ws >= 4 * T * h * 2 + nz * S * S * 2
+    assert ws < 5 * T * h * 2 + nz * S * S * 2
     assert ws % 1024 == 0
     assert tp.attn_saved_bytes(2, 2048, 8192, 64, 8) == tp.lib.tpmlp_attn_saved_bytes(ctypes.byref(s))
     for bad in (tp.AttnShape(1, 64, 256, 3, 1, tp.BF16, 0),    # h % heads != 0

@@ -98,6 +98,7 @@ def test_attention_matches_oracle(tp, nb, S, h, heads, t):
     inp, out, _ = run_attn(tp, nb, S, h, heads, t, seed=11 + S)
     ref = oracle_ref(inp, nb, heads, t)
     errs = {k: rel(to_np(out[k]), ref[k]) for k in TOL}
+    print("attention %s errors:" % ((nb, S, h, heads, t),), {k: "%.2e" % v for k, v in errs.items()})
     bad = {k: v for k, v in errs.items() if not (v <= TOL[k])}
     assert not bad, "outside tolerance: %s (all: %s)" % (bad, errs)
 
@@ -107,6 +108,7 @@ def test_attention_peaky_logits_match_oracle(tp):
     inp, out, _ = run_attn(tp, nb, S, h, heads, t, seed=7, std=STD_PEAKY)
     ref = oracle_ref(inp, nb, heads, t)
     errs = {k: rel(to_np(out[k]), ref[k]) for k in TOL}
+    print("attention, peaky logits, errors:", {k: "%.2e" % v for k, v in errs.items()})
     bad = {k: v for k, v in errs.items() if not (v <= TOL[k])}
     assert not bad, "outside tolerance: %s (all: %s)" % (bad, errs)
 
@@ -200,6 +202,7 @@ def test_full_size_prefix_matches_oracle(tp):
         got = {"QKV": ctx.QKV[rows], "O": ctx.O[rows], "Z": Z[rows], "P": P[b, :, :pre, :pre]}
         for k, v in got.items():
             e = rel(to_np(v), ref[k].reshape(to_np(v).shape))
+            print("attn-h8192 prefix, sequence %d, %s error %.2e" % (b, k, e))
             assert e <= TOL[k], (b, k, e)
         # probabilities past the prefix are zero on the prefix rows
         assert torch.count_nonzero(P[b, :, :pre, pre:]) == 0
