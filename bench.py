@@ -42,12 +42,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, with the hash of the kernel and launch sources they were taken at
 # (kernel_source_hash).  After a change to either, traffic is reported null.
 NCU_TRAFFIC = {  # profiles/dram_traffic_h8192_gemms.md (h8192 workload, one kernel per capture)
-    "fc1_bias_gelu": (1.325688e9 + 0.520764e9, "f6c5ff3ec0b8"),
-    "fc2_shard_fold": (2.507555e9 + 0.091267e9, "f6c5ff3ec0b8"),
-    "bwd_dY_dgelu": (1.768033e9 + 0.278109e9, "f6c5ff3ec0b8"),
-    "bwd_dB": (0.929347e9 + 0.515363e9, "f6c5ff3ec0b8"),
-    "bwd_dA": (0.962548e9 + 0.513651e9, "f6c5ff3ec0b8"),
-    "bwd_dX_shard_fold": (2.645486e9 + 0.086963e9, "f6c5ff3ec0b8"),
+    "fc1_bias_gelu": (1.337459e9 + 0.521222e9, "f9944539e02b"),
+    "fc2_shard_fold": (2.512475e9 + 0.093454e9, "f9944539e02b"),
+    "bwd_dY_dgelu": (1.778890e9 + 0.278292e9, "f9944539e02b"),
+    "bwd_dB": (0.930835e9 + 0.515377e9, "f9944539e02b"),
+    "bwd_dA": (0.974019e9 + 0.514437e9, "f9944539e02b"),
+    "bwd_dX_shard_fold": (2.516551e9 + 0.085967e9, "f9944539e02b"),
 }
 
 
@@ -316,7 +316,7 @@ def overlapped_e2e(dev, stream, world, steps, warmup, host_in, dev_out, copy_out
     copied after the forward, names copied after the backward); fwd(ins, outs)
     and bwd(ins, outs) launch one step's work.  Returns (max over ranks of the
     ms per step, host-to-device bytes per step, device-to-host bytes per step,
-    a note on the host cores used).
+    a note on the host cores used, the measured copy rates).
 
     While the pinned buffers are made and the steps run, the calling thread is
     held to the host cores local to the GPU (where the system names them and the
@@ -334,8 +334,9 @@ def overlapped_e2e(dev, stream, world, steps, warmup, host_in, dev_out, copy_out
     else:
         note = "GPU-local host cores not known or not allowed; %d cores, affinity unchanged" % len(allowed)
     try:
-        return overlapped_e2e_run(dev, stream, world, steps, warmup, host_in, dev_out, copy_out, fwd,
-                                  bwd) + (note,)
+        ems, h2d, d2h, rates = overlapped_e2e_run(dev, stream, world, steps, warmup, host_in, dev_out, copy_out,
+                                                  fwd, bwd)
+        return ems, h2d, d2h, note, rates
     finally:
         os.sched_setaffinity(0, allowed)
 
@@ -413,7 +414,23 @@ def overlapped_e2e_run(dev, stream, world, steps, warmup, host_in, dev_out, copy
     ems = max_over_ranks(f0.elapsed_time(f1) / steps, world)
     h2d = sum(v.numel() * v.element_size() for v in hin.values())
     d2h = sum(v.numel() * v.element_size() for v in hout[0].values())
-    return ems, h2d, d2h
+    # The copy rates alone, outside the timed region: one step's inputs in and
+    # results out, each timed on its copy stream with nothing else running.  A
+    # step cannot run faster end to end than its copies allow.
+    rates = {}
+    for name, cs, pairs in (("h2d_gbs", s_in, [(din[0][k], v) for k, v in hin.items()]),
+                            ("d2h_gbs", s_out, [(hout[0][k], dout[0][k]) for k in hout[0]])):
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(cs)
+        with torch.cuda.stream(cs):
+            for dst, src in pairs:
+                dst.copy_(src, non_blocking=True)
+        c1.record(cs)
+        torch.cuda.synchronize(dev)
+        nbytes = sum(dst.numel() * dst.element_size() for dst, _ in pairs)
+        rates[name] = nbytes / (c0.elapsed_time(c1) * 1e-3) / 1e9 if nbytes else None
+    return ems, h2d, d2h, rates
 
 
 # ------------------------------------------------------------------ timed passes
@@ -557,14 +574,16 @@ def run_ours(args, rank, world, local, w=None, quiet=False):
             else:
                 tpmlp.backward(ctx, ins["dZ"], stream=stream, **{k: outs[k] for k in g})
 
-        ems, h2d, d2h, host_note = overlapped_e2e(dev, stream, world, args.steps, args.warmup, host_in, dev_out,
+        ems, h2d, d2h, host_note, rates = overlapped_e2e(dev, stream, world, args.steps, args.warmup, host_in,
+                                                         dev_out,
                                        (["Z"], [] if args.fwd_only else ["dX", "da", "db"]), fwd,
                                        None if args.fwd_only else bwd)
         e2e = {"value": flops * world / (ems * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ems,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "what": "X and dZ copied in from pinned host memory, Z, dX, da, db copied out, every "
                        "step, on copy streams overlapped with the neighbouring steps' compute; weights "
-                       "and weight gradients stay resident", "host": host_note}
+                       "and weight gradients stay resident", "host": host_note,
+               "copy_rates_gbs": rates}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -644,14 +663,15 @@ def run_attn_bench(args, rank, world, local):
         def bwd(ins, outs):
             tpmlp.attn_backward(ctx, ins["dZ"], stream=stream, **{k: outs[k] for k in g})
 
-        ems, h2d, d2h, host_note = overlapped_e2e(dev, stream, world, args.steps, args.warmup,
+        ems, h2d, d2h, host_note, rates = overlapped_e2e(dev, stream, world, args.steps, args.warmup,
                                        {"X": host["X"], "dZ": host["dZ"]}, dev_out,
                                        (["Z"], ["dX", "dbqkv", "dbo"]), fwd, bwd)
         e2e = {"value": w.flops_fwd_bwd * world / (ems * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ems,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "what": "X and dZ copied in from pinned host memory, Z, dX, dbqkv, dbo copied out, every "
                        "step, on copy streams overlapped with the neighbouring steps' compute; weights "
-                       "and weight gradients stay resident", "host": host_note}
+                       "and weight gradients stay resident", "host": host_note,
+               "copy_rates_gbs": rates}
     return {"metric": "TP self-attention fwd+bwd TFLOP/s (bf16, 1×GB300)", "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
