@@ -408,6 +408,14 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
                  : "memory");
 }
 
+// Two fp32 values to an fp16 pair (lo in the low half), rounded to nearest even,
+// with values beyond the fp16 range saturated to its largest finite magnitude.
+__device__ __forceinline__ uint32_t f16x2_satfinite(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // tanh via the MUFU approximation (max relative error about 2^-11), used where the
 // result is rounded to bf16 anyway.
 __device__ __forceinline__ float tanh_approx(float x) {

@@ -32,7 +32,6 @@
 // drains its own copies and MMAs and frees its tensor memory before returning.
 #include <cuda.h>
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
@@ -350,11 +349,6 @@ __device__ __forceinline__ float gelu_prime_f(float x) {
     return fmaf(fmaf(-th, th, 1.0f), hxdu, fmaf(0.5f, th, 0.5f));
 }
 
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -550,16 +544,19 @@ __device__ __forceinline__ void finish_chunk(const Params &p, const CUtensorMap 
                                              const BiasPre *bias_pre = nullptr) {
     if constexpr (EPI == EPI_ATTN_SCORE) {
         // S = scale * Q K^T with the causal mask, stored in fp16 for the softmax
-        // (11 significant bits; finite values clamped to the fp16 range, the
-        // masked ones -inf).
+        // (11 significant bits; finite values saturate at the fp16 range, the
+        // masked ones are -inf).  Only a chunk that reaches past the diagonal
+        // (its last column beyond its first row) has masked entries.
         uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float lo = fminf(fmaxf(v[2 * i] * p.scale, -65504.0f), 65504.0f);
-            float hi = fminf(fmaxf(v[2 * i + 1] * p.scale, -65504.0f), 65504.0f);
-            if (p.causal && col + 2 * i > row) lo = -INFINITY;
-            if (p.causal && col + 2 * i + 1 > row) hi = -INFINITY;
-            w[i] = pack_f16(lo, hi);
+        for (int i = 0; i < 16; ++i) w[i] = ptx::f16x2_satfinite(v[2 * i] * p.scale, v[2 * i + 1] * p.scale);
+        if (p.causal && col + 31 > row0) {
+            constexpr uint32_t NEG_INF_LO = 0x0000FC00u, NEG_INF_HI = 0xFC000000u;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (col + 2 * i > row) w[i] = NEG_INF_HI | NEG_INF_LO;
+                else if (col + 2 * i + 1 > row) w[i] = (w[i] & 0x0000FFFFu) | NEG_INF_HI;
+            }
         }
         if (lane == 0) ptx::bulk_wait_read0();
         __syncwarp();
