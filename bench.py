@@ -42,12 +42,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, with the hash of the kernel and launch sources they were taken at
 # (kernel_source_hash).  After a change to either, traffic is reported null.
 NCU_TRAFFIC = {  # profiles/dram_traffic_h8192_gemms.md (h8192 workload, one kernel per capture)
-    "fc1_bias_gelu": (1.337459e9 + 0.521222e9, "f9944539e02b"),
-    "fc2_shard_fold": (2.512475e9 + 0.093454e9, "f9944539e02b"),
-    "bwd_dY_dgelu": (1.778890e9 + 0.278292e9, "f9944539e02b"),
-    "bwd_dB": (0.930835e9 + 0.515377e9, "f9944539e02b"),
-    "bwd_dA": (0.974019e9 + 0.514437e9, "f9944539e02b"),
-    "bwd_dX_shard_fold": (2.516551e9 + 0.085967e9, "f9944539e02b"),
+    "fc1_bias_gelu": (1.333403e9 + 0.521086e9, "3fda96bd9f4c"),
+    "fc2_shard_fold": (2.505877e9 + 0.092050e9, "3fda96bd9f4c"),
+    "bwd_dY_dgelu": (1.775990e9 + 0.278265e9, "3fda96bd9f4c"),
+    "bwd_dB": (0.916102e9 + 0.514674e9, "3fda96bd9f4c"),
+    "bwd_dA": (0.962493e9 + 0.514380e9, "3fda96bd9f4c"),
+    "bwd_dX_shard_fold": (2.524709e9 + 0.084896e9, "3fda96bd9f4c"),
 }
 
 
