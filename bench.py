@@ -364,19 +364,9 @@ def overlapped_e2e_run(dev, stream, world, steps, warmup, host_in, dev_out, copy
                 din[b][k].copy_(v, non_blocking=True)
         in_ready[b].record(s_in)
 
-    def one_step(i, last):
-        b = i % 2
-        stream.wait_event(in_ready[b])
-        if pend["out"][b]:  # results of step i-2 have left buffer b
-            stream.wait_event(out_done[b])
-        fwd(din[b], dout[b])
-        fwd_done[b].record(stream)
-        if bwd is not None:
-            bwd(din[b], dout[b])
-        step_done[b].record(stream)
-        pend["done"][b] = True
-        if not last:
-            copy_in(b ^ 1)
+    def copy_out(b):
+        # results of the step that used buffer b, each copy gated on the event that
+        # makes it ready
         s_out.wait_event(fwd_done[b])
         with torch.cuda.stream(s_out):
             for k in out_fwd:
@@ -388,6 +378,27 @@ def overlapped_e2e_run(dev, stream, world, steps, warmup, host_in, dev_out, copy
                     hout[b][k].copy_(dout[b][k], non_blocking=True)
         out_done[b].record(s_out)
         pend["out"][b] = True
+
+    def one_step(i, last):
+        # Host order: this step's kernels first, then the copies of the previous
+        # step's results and of the next step's inputs, so that a copy call that
+        # returns late cannot hold back the kernels queued behind it.
+        b = i % 2
+        stream.wait_event(in_ready[b])
+        if pend["out"][b]:  # results of step i-2 have left buffer b
+            stream.wait_event(out_done[b])
+        fwd(din[b], dout[b])
+        fwd_done[b].record(stream)
+        if bwd is not None:
+            bwd(din[b], dout[b])
+        step_done[b].record(stream)
+        pend["done"][b] = True
+        if i > 0:
+            copy_out(b ^ 1)
+        if not last:
+            copy_in(b ^ 1)
+        else:
+            copy_out(b)
 
     def run_steps(n, start_event=None, end_event=None):
         if start_event is not None:
@@ -423,9 +434,12 @@ def overlapped_e2e_run(dev, stream, world, steps, warmup, host_in, dev_out, copy
         c0 = torch.cuda.Event(enable_timing=True)
         c1 = torch.cuda.Event(enable_timing=True)
         c0.record(cs)
+        h0 = time.perf_counter()
         with torch.cuda.stream(cs):
             for dst, src in pairs:
                 dst.copy_(src, non_blocking=True)
+        # host time to enqueue them: near zero when the copies run asynchronously
+        rates[name.replace("gbs", "enqueue_ms")] = (time.perf_counter() - h0) * 1e3
         c1.record(cs)
         torch.cuda.synchronize(dev)
         nbytes = sum(dst.numel() * dst.element_size() for dst, _ in pairs)
