@@ -426,24 +426,30 @@ def overlapped_e2e_run(dev, stream, world, steps, warmup, host_in, dev_out, copy
     h2d = sum(v.numel() * v.element_size() for v in hin.values())
     d2h = sum(v.numel() * v.element_size() for v in hout[0].values())
     # The copy rates alone, outside the timed region: one step's inputs in and
-    # results out, each timed on its copy stream with nothing else running.  A
-    # step cannot run faster end to end than its copies allow.
+    # results out, each timed on its copy stream with nothing else running (best
+    # of three).  A step cannot run faster end to end than its copies allow.
     rates = {}
     for name, cs, pairs in (("h2d_gbs", s_in, [(din[0][k], v) for k, v in hin.items()]),
                             ("d2h_gbs", s_out, [(hout[0][k], dout[0][k]) for k in hout[0]])):
-        c0 = torch.cuda.Event(enable_timing=True)
-        c1 = torch.cuda.Event(enable_timing=True)
-        c0.record(cs)
-        h0 = time.perf_counter()
-        with torch.cuda.stream(cs):
-            for dst, src in pairs:
-                dst.copy_(src, non_blocking=True)
-        # host time to enqueue them: near zero when the copies run asynchronously
-        rates[name.replace("gbs", "enqueue_ms")] = (time.perf_counter() - h0) * 1e3
-        c1.record(cs)
-        torch.cuda.synchronize(dev)
+        best_ms, best_enq = None, None
+        for _ in range(3):
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            c0.record(cs)
+            h0 = time.perf_counter()
+            with torch.cuda.stream(cs):
+                for dst, src in pairs:
+                    dst.copy_(src, non_blocking=True)
+            # host time to enqueue them: near zero when the copies run asynchronously
+            enq = (time.perf_counter() - h0) * 1e3
+            c1.record(cs)
+            torch.cuda.synchronize(dev)
+            ms = c0.elapsed_time(c1)
+            best_ms = ms if best_ms is None else min(best_ms, ms)
+            best_enq = enq if best_enq is None else min(best_enq, enq)
         nbytes = sum(dst.numel() * dst.element_size() for dst, _ in pairs)
-        rates[name] = nbytes / (c0.elapsed_time(c1) * 1e-3) / 1e9 if nbytes else None
+        rates[name] = nbytes / (best_ms * 1e-3) / 1e9 if nbytes else None
+        rates[name.replace("gbs", "enqueue_ms")] = best_enq
     return ems, h2d, d2h, rates
 
 
