@@ -12,7 +12,9 @@
  * pass sums the shard contributions to dX.  Here all t shards live on one GPU:
  * the column-parallel GEMM of every shard is one launch (the shards are disjoint
  * column blocks) and each all-reduce is a fixed-order fp32 sum of the t shard
- * partials, Z = b + (((Z_1 + Z_2) + Z_3) + ... + Z_t), done on chip.  Repeated
+ * partials, Z = b + (((Z_1 + Z_2) + Z_3) + ... + Z_t), done on chip (the tiles
+ * that the tensor-core schedule walks down K sum the same partials in the
+ * opposite order, b + (((Z_t + Z_t-1) + ...) + Z_1)).  Repeated
  * calls with the same inputs give bit-identical outputs.  The tensor-core GEMMs
  * accumulate over k in an order that depends on their tile schedule, and so on
  * the number of SMs they run on: a GPU with another SM count (or the

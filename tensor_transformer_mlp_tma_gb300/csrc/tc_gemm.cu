@@ -23,9 +23,10 @@
 // Z = sum_i Y_i B_i; section 4.2 for dX in the backward direction) becomes the
 // FOLD epilogues: each shard's K range is its own accumulation unit, so each
 // partial Z_i is a complete fp32 product in TMEM; the epilogue threads pull it
-// into registers and add it to their running sum in shard order
-// ((Z_1 + Z_2) + Z_3) + ..., releasing the TMEM buffer at once so the tensor
-// core starts the next shard in the other buffer without waiting.
+// into registers and add it to their running sum in the order the shards come,
+// ((Z_1 + Z_2) + Z_3) + ... (descending, ((Z_t + Z_t-1) + ...), for the tiles of
+// odd waves, which walk K downwards), releasing the TMEM buffer at once so the
+// tensor core starts the next shard in the other buffer without waiting.
 //
 // Every wait is bounded (mbar_wait); a wait that runs out records
 // TPMLP_ERR_TIMEOUT in the status word, raises a CTA-wide abort flag, and the CTA
@@ -918,6 +919,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         continue;
                     }
                 }
+                // Odd waves walk the tile's K range downwards (serpentine): for a
+                // shard fold, the shards in descending order, each from its last
+                // k-block; the MMA and the fold take the units in the order they come.
+                const bool down = !HEADS && p.serpentine && ((tile / num_units) & 1);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!ptx::mbar_wait_scoped<false>(ptx::smem_u32(&bar_empty[stage]), phase ^ 1u, p.wait_ns,
                                                      &abort_sh)) {
@@ -928,7 +933,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t full = PAIR ? ptx::mapa_shared(full_local, 0) : full_local;
                     const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
                     const uint32_t sb = sa + C::A_STAGE;
-                    const int k0 = kb * BK;
+                    const int k0 = (down ? kb0 + kb1 - 1 - kb : kb) * BK;
                     if (!dbg_ok(stage >= 0 && stage < STAGES && sb + C::B_STAGE <= ring_end, p, &abort_sh, 0x0501u)) {
                         ok = false;
                         break;
@@ -1745,7 +1750,7 @@ static cudaError_t launch_t(const GemmArgs &g, int num_sms, cudaStream_t st) {
     // TPMLP_SERPENTINE=0 walks K upwards in every wave (a tuning knob, read per call).
     {
         const char *se = std::getenv("TPMLP_SERPENTINE");
-        p.serpentine = WIDE && !(se && se[0] == '0') ? 1 : 0;
+        p.serpentine = (WIDE || (!HEADS && g.causal_k == 0 && !g.skip_upper)) && !(se && se[0] == '0') ? 1 : 0;
     }
     if (WIDE) {
         const char *tail_env = std::getenv("TPMLP_WIDE_TAIL");
