@@ -42,12 +42,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture, with the hash of the kernel and launch sources they were taken at
 # (kernel_source_hash).  After a change to either, traffic is reported null.
 NCU_TRAFFIC = {  # profiles/dram_traffic_h8192_gemms.md (h8192 workload, one kernel per capture)
-    "fc1_bias_gelu": (1.333403e9 + 0.521086e9, "3fda96bd9f4c"),
-    "fc2_shard_fold": (2.505877e9 + 0.092050e9, "3fda96bd9f4c"),
-    "bwd_dY_dgelu": (1.775990e9 + 0.278265e9, "3fda96bd9f4c"),
-    "bwd_dB": (0.916102e9 + 0.514674e9, "3fda96bd9f4c"),
-    "bwd_dA": (0.962493e9 + 0.514380e9, "3fda96bd9f4c"),
-    "bwd_dX_shard_fold": (2.524709e9 + 0.084896e9, "3fda96bd9f4c"),
+    "fc1_bias_gelu": (1.343788e9 + 0.520588e9, "20c49dd1ab49"),
+    "fc2_shard_fold": (2.323672e9 + 0.095526e9, "20c49dd1ab49"),
+    "bwd_dY_dgelu": (1.780639e9 + 0.278026e9, "20c49dd1ab49"),
+    "bwd_dB": (0.931116e9 + 0.515468e9, "20c49dd1ab49"),
+    "bwd_dA": (0.983755e9 + 0.514475e9, "20c49dd1ab49"),
+    "bwd_dX_shard_fold": (2.323205e9 + 0.083362e9, "20c49dd1ab49"),
 }
 
 
